@@ -1,0 +1,306 @@
+// gpt_forward, gpt_forward_host and gpt_status: the launch sequence of one
+// forward pass plus loss.
+//
+// bf16 path, pre-norm ("第 25 章 从小 GPT 到 GPT-2" §25.1-25.4):
+//   K1 embed + LN1(block 0)           x fp32, a bf16
+//   per block l:
+//     K3 c_attn   a . W_attn^T + b          -> qkv bf16 [M, 3C]
+//     K4 attention (causal, online softmax) -> y bf16 [M, C]
+//     K3 c_proj   x += y . W_proj^T + b     (residual in the epilogue)
+//     K2 LN2      x -> a
+//     K3 c_fc     a . W_fc^T + b, GELU      -> g bf16 [M, ffn]
+//     K3 mlp.c_proj x += g . W_mp^T + b
+//     K2 LN1 of block l+1, or ln_f after the last block: x -> a
+//   K5 tied head with the cross-entropy epilogue: per (row, 256-column tile)
+//      partial max / sum-exp and the target's logit; logits stored only if asked
+//   K6 combine the partials per row -> nll; mean -> loss
+// Post-norm ("GPT-1 学习笔记" §3.1-3.2): c_attn reads x itself (a = bf16 copy),
+// the LayerNorms read the residual sums and write back into x, no ln_f.
+#include "model.h"
+
+#include <cuda_runtime.h>
+
+using namespace gptgb;
+
+namespace {
+
+int cu(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return GPT_OK;
+  set_detail(what, e);
+  return GPT_ECUDA;
+}
+
+bool probe_hit(const gpt_model* m, int step, int layer) {
+  return m->prof_ev0 != nullptr && m->prof_step == step && (layer < 0 || m->prof_layer == layer);
+}
+
+// One step = one kernel launch, optionally bracketed by the armed probe events.
+#define GPT_STEP(step, layer, expr)                                                 \
+  do {                                                                              \
+    const bool hit_ = probe_hit(m, (step), (layer));                                \
+    if (hit_) cudaEventRecord(m->prof_ev0, s);                                      \
+    const int rc_ = (expr);                                                         \
+    if (rc_ != GPT_OK) return rc_;                                                  \
+    ++m->launches;                                                                  \
+    if (hit_) cudaEventRecord(m->prof_ev1, s);                                      \
+  } while (0)
+
+int ensure_act_maps(gpt_model* m, int B, int T) {
+  if (m->cached_B == B && m->cached_T == T) return GPT_OK;
+  const int M = B * T, C = m->cfg.C, F = m->cfg.ffn;
+  const bool ok = make_tmap_2d_bf16(&m->tm_a, m->a, M, C, kGemmBM) &&
+                  make_tmap_2d_bf16(&m->tm_y, m->y, M, C, kGemmBM) &&
+                  make_tmap_2d_bf16(&m->tm_g, m->g, M, F, kGemmBM) &&
+                  make_tmap_qkv(&m->tm_qkv, m->qkv, B, T, 3 * C, C / m->cfg.H);
+  if (!ok) {
+    set_detail_text("activation tensor map");
+    m->cached_B = m->cached_T = -1;
+    return GPT_ECUDA;
+  }
+  m->cached_B = B;
+  m->cached_T = T;
+  return GPT_OK;
+}
+
+int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, const float* bias,
+            void* out, int epi, cudaStream_t s) {
+  GemmArgs a{};
+  a.M = M; a.N = N; a.K = K;
+  a.bias = bias;
+  a.out = out;
+  a.ldo = N;
+  a.gelu_erf = m->cfg.gelu;
+  a.err = m->err;
+  a.m_fastest = (N > M) ? 1 : 0;        // keep the larger operand's tiles shared by co-running CTAs
+  GPT_CUDA(launch_gemm_tc(tmA, tmB, a, epi, m->num_sms, s));
+  return GPT_OK;
+}
+
+// The LayerNorm that follows the residual add of a block (or ln_f / nothing).
+// Pre-norm: a = LN(x). Post-norm: x = LN(x) and a = copy of it.
+struct NextLN { const float* g; const float* b; };
+
+int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss, float* d_logits,
+                 cudaStream_t s) {
+  const gpt_config& c = m->cfg;
+  const int M = B * T, C = c.C, F = c.ffn, L = c.L;
+  const bool pre = c.norm_mode == 0;
+  int rc = ensure_act_maps(m, B, T);
+  if (rc != GPT_OK) return rc;
+
+  // K1: embedding (+ the first LayerNorm of the pre-norm stack)
+  {
+    int out_mode = 1;
+    const float* g = nullptr;
+    const float* b = nullptr;
+    if (pre) {
+      if (L > 0) { out_mode = 2; g = m->layers[0].ln1_g; b = m->layers[0].ln1_b; }
+      else if (c.final_ln) { out_mode = 2; g = m->lnf_g; b = m->lnf_b; }
+    }
+    GPT_STEP(GPT_STEP_EMBED, -1,
+             cu(launch_embed(ids, m->wte, m->wpe, 1, m->x, m->a, out_mode, 1, g, b, M, T, C, c.V, c.ln_eps, m->err, s),
+                "embed"));
+  }
+  for (int l = 0; l < L; ++l) {
+    const gpt_layer_dev& w = m->layers[l];
+    GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
+    GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_tc(m->tm_qkv, m->y, B, T, c.H, C / c.H, m->err, s), "attention"));
+    GPT_STEP(GPT_STEP_C_PROJ, l, tc_gemm(m, m->tm_y, w.tm_proj_w, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
+    if (pre)
+      GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
+    else
+      GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln1_g, w.ln1_b, m->a, 1, m->x, M, C, c.ln_eps, s), "ln"));
+    GPT_STEP(GPT_STEP_C_FC, l, tc_gemm(m, m->tm_a, w.tm_fc_w, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
+    GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm(m, m->tm_g, w.tm_mp_w, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
+    if (pre) {
+      NextLN n{nullptr, nullptr};
+      if (l + 1 < L) n = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
+      else if (c.final_ln) n = {m->lnf_g, m->lnf_b};
+      GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, n.g, n.b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
+    } else {
+      GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, m->a, 1, m->x, M, C, c.ln_eps, s), "ln"));
+    }
+  }
+  if (!pre && L == 0 && c.final_ln)
+    GPT_STEP(GPT_STEP_LN_OUT, -1, cu(launch_layernorm(m->x, m->lnf_g, m->lnf_b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
+
+  // K5/K6: tied head
+  if (tg) {
+    GemmArgs a{};
+    a.M = M; a.N = c.V; a.K = C;
+    a.ldo = c.V;
+    a.targets = tg;
+    a.pmax = m->pmax;
+    a.psum = m->psum;
+    a.ztgt = m->ztgt;
+    a.logits = d_logits;
+    a.err = m->err;
+    a.m_fastest = 1;
+    GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, a, EPI_CE, m->num_sms, s), "head"));
+    GPT_STEP(GPT_STEP_CE, -1,
+             cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, M, gemm_tc_num_ntiles(c.V), c.V, m->err, s),
+                "ce_combine"));
+    if (d_loss) GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->nll, M, d_loss, s), "mean"));
+  } else if (d_logits) {
+    GPT_STEP(GPT_STEP_HEAD, -1, tc_gemm(m, m->tm_a, m->tm_wte, M, c.V, C, nullptr, d_logits, EPI_F32, s));
+  }
+  return GPT_OK;
+}
+
+int forward_f32(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss, float* d_logits,
+                cudaStream_t s) {
+  const gpt_config& c = m->cfg;
+  const int M = B * T, C = c.C, F = c.ffn, L = c.L, H = c.H;
+  const bool pre = c.norm_mode == 0;
+  float* a = reinterpret_cast<float*>(m->a);
+  float* qkv = reinterpret_cast<float*>(m->qkv);
+  float* y = reinterpret_cast<float*>(m->y);
+  float* g = reinterpret_cast<float*>(m->g);
+  {
+    int out_mode = 1;
+    const float* lg = nullptr;
+    const float* lb = nullptr;
+    if (pre) {
+      if (L > 0) { out_mode = 2; lg = m->layers[0].ln1_g; lb = m->layers[0].ln1_b; }
+      else if (c.final_ln) { out_mode = 2; lg = m->lnf_g; lb = m->lnf_b; }
+    }
+    GPT_STEP(GPT_STEP_EMBED, -1,
+             cu(launch_embed(ids, m->wte, m->wpe, 0, m->x, a, out_mode, 0, lg, lb, M, T, C, c.V, c.ln_eps, m->err, s),
+                "embed"));
+  }
+  for (int l = 0; l < L; ++l) {
+    const gpt_layer_dev& w = m->layers[l];
+    GPT_STEP(GPT_STEP_C_ATTN, l,
+             cu(launch_gemm_simt(a, reinterpret_cast<const float*>(w.attn_w), w.attn_b, qkv, M, 3 * C, C, 3 * C,
+                                 EPI_BIAS_OUT, c.gelu, s), "gemm"));
+    GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_simt(qkv, y, B, T, H, C / H, s), "attention"));
+    GPT_STEP(GPT_STEP_C_PROJ, l,
+             cu(launch_gemm_simt(y, reinterpret_cast<const float*>(w.proj_w), w.proj_b, m->x, M, C, C, C,
+                                 EPI_BIAS_RESID, c.gelu, s), "gemm"));
+    if (pre)
+      GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, a, 0, nullptr, M, C, c.ln_eps, s), "ln"));
+    else
+      GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln1_g, w.ln1_b, a, 0, m->x, M, C, c.ln_eps, s), "ln"));
+    GPT_STEP(GPT_STEP_C_FC, l,
+             cu(launch_gemm_simt(a, reinterpret_cast<const float*>(w.fc_w), w.fc_b, g, M, F, C, F,
+                                 EPI_BIAS_GELU_OUT, c.gelu, s), "gemm"));
+    GPT_STEP(GPT_STEP_MLP_PROJ, l,
+             cu(launch_gemm_simt(g, reinterpret_cast<const float*>(w.mp_w), w.mp_b, m->x, M, C, F, C,
+                                 EPI_BIAS_RESID, c.gelu, s), "gemm"));
+    if (pre) {
+      NextLN n{nullptr, nullptr};
+      if (l + 1 < L) n = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
+      else if (c.final_ln) n = {m->lnf_g, m->lnf_b};
+      GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, n.g, n.b, a, 0, nullptr, M, C, c.ln_eps, s), "ln"));
+    } else {
+      GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, a, 0, m->x, M, C, c.ln_eps, s), "ln"));
+    }
+  }
+  if (!pre && L == 0 && c.final_ln)
+    GPT_STEP(GPT_STEP_LN_OUT, -1, cu(launch_layernorm(m->x, m->lnf_g, m->lnf_b, a, 0, nullptr, M, C, c.ln_eps, s), "ln"));
+  if (!tg && !d_logits) return GPT_OK;
+  float* z = d_logits ? d_logits : m->logits_ws;
+  GPT_STEP(GPT_STEP_HEAD, -1,
+           cu(launch_gemm_simt(a, reinterpret_cast<const float*>(m->wte), nullptr, z, M, c.V, C, c.V, EPI_F32, 0, s),
+              "head"));
+  if (tg) {
+    GPT_STEP(GPT_STEP_CE, -1, cu(launch_ce_rows(z, tg, m->nll, M, c.V, m->err, s), "ce_rows"));
+    if (d_loss) GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->nll, M, d_loss, s), "mean"));
+  }
+  return GPT_OK;
+}
+
+int check_shape(const gpt_model* m, int B, int T) {
+  if (B < 1 || T < 1) return GPT_EINVAL;
+  if (T > m->cfg.ctx) return GPT_ESEQ;
+  if ((int64_t)B * T > m->cfg.max_tokens) return GPT_EINVAL;
+  return GPT_OK;
+}
+
+int map_device_error(int code) {
+  switch (code) {
+    case GPT_DEV_OK: return GPT_OK;
+    case GPT_DEV_ETOKEN:
+    case GPT_DEV_ETARGET: return GPT_ETOKEN;
+    default: return GPT_EDEVICE;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int gpt_forward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, int32_t B, int32_t T, float* d_loss,
+                float* d_logits, void* stream) {
+  if (!m || !d_ids) return GPT_EINVAL;
+  int rc = check_shape(m, B, T);
+  if (rc != GPT_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  m->launches = 0;
+  rc = m->bf16 ? forward_bf16(m, d_ids, d_targets, B, T, d_loss, d_logits, s)
+               : forward_f32(m, d_ids, d_targets, B, T, d_loss, d_logits, s);
+  m->prof_ev0 = m->prof_ev1 = nullptr;       // a probe covers one forward
+  m->prof_step = m->prof_layer = -1;
+  return rc;
+}
+
+int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_stop) {
+  if (!m) return GPT_EINVAL;
+  if (!ev_start) {
+    m->prof_ev0 = m->prof_ev1 = nullptr;
+    m->prof_step = m->prof_layer = -1;
+    return GPT_OK;
+  }
+  if (!ev_stop || step < GPT_STEP_EMBED || step > GPT_STEP_MEAN) return GPT_EINVAL;
+  m->prof_step = step;
+  m->prof_layer = layer;
+  m->prof_ev0 = reinterpret_cast<cudaEvent_t>(ev_start);
+  m->prof_ev1 = reinterpret_cast<cudaEvent_t>(ev_stop);
+  return GPT_OK;
+}
+
+int gpt_last_launch_count(const gpt_model* m) { return m ? m->launches : 0; }
+
+int gpt_status(gpt_model* m, void* stream) {
+  if (!m) return GPT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GPT_CUDA(cudaMemcpyAsync(m->h_pinned, m->err, sizeof(int), cudaMemcpyDeviceToHost, s));
+  GPT_CUDA(cudaMemsetAsync(m->err, 0, sizeof(int), s));
+  GPT_CUDA(cudaStreamSynchronize(s));
+  return map_device_error(m->h_pinned[0]);
+}
+
+int gpt_forward_host(gpt_model* m, const int32_t* h_ids, const int32_t* h_targets, int32_t B, int32_t T,
+                     float* h_loss, float* h_logits, void* stream) {
+  if (!m || !h_ids) return GPT_EINVAL;
+  if (h_targets && !h_loss) return GPT_EINVAL;
+  int rc = check_shape(m, B, T);
+  if (rc != GPT_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t M = static_cast<size_t>(B) * T;
+  float* d_logits = nullptr;
+  if (h_logits) {
+    const size_t need = M * static_cast<size_t>(m->cfg.V);
+    if (m->stage_logits_elems < need) {
+      cudaFree(m->stage_logits);
+      m->stage_logits = nullptr;
+      m->stage_logits_elems = 0;
+      if (cudaMalloc(&m->stage_logits, need * sizeof(float)) != cudaSuccess) return GPT_ENOMEM;
+      m->stage_logits_elems = need;
+    }
+    d_logits = m->stage_logits;
+  }
+  GPT_CUDA(cudaMemcpyAsync(m->stage_ids, h_ids, M * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  if (h_targets) GPT_CUDA(cudaMemcpyAsync(m->stage_tg, h_targets, M * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  rc = gpt_forward(m, m->stage_ids, h_targets ? m->stage_tg : nullptr, B, T, h_targets ? m->stage_loss : nullptr,
+                   d_logits, stream);
+  if (rc != GPT_OK) return rc;
+  if (h_targets) GPT_CUDA(cudaMemcpyAsync(m->h_pinned + 1, m->stage_loss, sizeof(float), cudaMemcpyDeviceToHost, s));
+  if (h_logits)
+    GPT_CUDA(cudaMemcpyAsync(h_logits, d_logits, M * m->cfg.V * sizeof(float), cudaMemcpyDeviceToHost, s));
+  rc = gpt_status(m, stream);
+  if (h_targets) *h_loss = reinterpret_cast<const float*>(m->h_pinned)[1];
+  return rc;
+}
+
+}  // extern "C"

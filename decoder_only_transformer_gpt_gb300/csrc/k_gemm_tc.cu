@@ -1,0 +1,369 @@
+// Persistent tcgen05 GEMM for sm_103a: out = epilogue(A[M,K] . W[N,K]^T).
+//
+// Used for c_attn, attention c_proj, c_fc and mlp c_proj ("第 25 章 从小 GPT 到
+// GPT-2" §25.2-25.3: every projection is an nn.Linear, W stored [out, in]) and
+// for the tied LM head with its cross-entropy epilogue (§25.4; "预训练一个 Mini
+// GPT" 第6步).
+//
+// Layout: A and W are K-major bf16; TMA copies 128 x 64 (A) and BN x 64 (W)
+// boxes with the 128-byte swizzle into a STAGES-deep shared-memory ring. One
+// thread issues tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
+// accumulators of BN fp32 columns, so the epilogue of tile i overlaps the main
+// loop of tile i+1. Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one elected lane)
+//   warp 1      TMEM allocator and MMA issuer (one elected lane)
+//   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4).., one output row per thread
+#include "common.cuh"
+#include "kernels.h"
+
+#include <math.h>
+
+namespace gptgb {
+
+namespace {
+
+constexpr int BM = kGemmBM;
+constexpr int BK = kGemmBK;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;              // 16 KB
+constexpr int B_BYTES = BN * BK * 2;              // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                 // 512: two accumulators
+constexpr int THREADS = 192;
+constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;   // + barriers + alignment slack
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct __align__(8) Bars {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+__device__ __forceinline__ void tile_coords(int tile, int MB, int NB, int m_fastest, int& mb, int& nb) {
+  if (m_fastest) { mb = tile % MB; nb = tile / MB; }
+  else           { nb = tile % NB; mb = tile / NB; }
+}
+
+// Wait without looking at the abort flag: used only while draining on exit.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 200000000ull) return;     // 200 ms
+  }
+}
+
+__device__ __forceinline__ float gelu_f(float x, int erf_form) {
+  if (erf_form) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+  return 0.5f * x * (1.0f + tanh_approx(u));
+}
+
+// ---------------------------------------------------------------- epilogues
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32], int grow,
+                                               int n0) {
+  const bool full = (n0 + 32 <= a.N);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  if (a.bias != nullptr) {
+    if (full) {
+      const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 bb = __ldg(b4 + q);
+        v[4 * q + 0] += bb.x; v[4 * q + 1] += bb.y; v[4 * q + 2] += bb.z; v[4 * q + 3] += bb.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += (n0 + i < a.N) ? __ldg(a.bias + n0 + i) : 0.0f;
+    }
+  }
+  if (EPI == EPI_BIAS_GELU_OUT) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i], a.gelu_erf);
+  }
+  if (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)grow * a.ldo + n0;
+    if (full) {
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+        o4[q] = w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < a.N) o[i] = __float2bfloat16_rn(v[i]);
+    }
+  } else if (EPI == EPI_BIAS_RESID) {
+    float* o = reinterpret_cast<float*>(a.out) + (size_t)grow * a.ldo + n0;
+    if (full) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 x = o4[q];
+        x.x += v[4 * q + 0]; x.y += v[4 * q + 1]; x.z += v[4 * q + 2]; x.w += v[4 * q + 3];
+        o4[q] = x;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < a.N) o[i] += v[i];
+    }
+  } else if (EPI == EPI_F32) {
+    float* o = reinterpret_cast<float*>(a.out) + (size_t)grow * a.ldo + n0;
+    if (full) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < a.N) o[i] = v[i];
+    }
+  }
+}
+
+// Cross-entropy epilogue for one 32-column chunk: fold the chunk into the
+// row's running (max m, sum s of exp(z - m)) for this tile, capture the
+// target's logit, and store logits if asked.
+__device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t (&r)[32], int grow, int n0,
+                                         int tgt, float& m, float& s) {
+  float z[32];
+  float cm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
+    cm = fmaxf(cm, z[i]);
+  }
+  if (cm != -INFINITY) {
+    const float nm = fmaxf(m, cm);
+    const float nml = nm * kLog2e;
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc += ex2_approx(fmaf(z[i], kLog2e, -nml));
+    s = s * ex2_approx((m - nm) * kLog2e) + acc;   // m = -inf on the first chunk: scale 0
+    m = nm;
+  }
+  if (static_cast<unsigned>(tgt - n0) < 32u) {
+    float zt = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i == tgt - n0) zt = z[i];
+    a.ztgt[grow] = zt;
+  }
+  if (a.logits != nullptr) {
+    float* o = a.logits + (size_t)grow * a.ldo + n0;
+    if (n0 + 32 <= a.N && (a.ldo & 3) == 0) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o4[q] = make_float4(z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < a.N) o[i] = z[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  Bars* bars = reinterpret_cast<Bars*>(smem + BAR_OFFSET);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int MB = (args.M + BM - 1) / BM;
+  const int NB = (args.N + BN - 1) / BN;
+  const int KB = (args.K + BK - 1) / BK;
+  const int num_tiles = MB * NB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&bars->full[s], 1); mbar_init(&bars->empty[s], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bars->tfull[i], 1); mbar_init(&bars->tempty[i], 4); }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 1) tmem_alloc(&bars->tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
+          tma_load_2d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, nb * BN);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // never leave with copies in flight into this CTA's shared memory
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) mbar_wait_drain(&bars->full[s], (last_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&bars->full[stage], phase, abort_flag, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = smem_desc(a0 + k * 32, 16, 1024, SWZ_128B);
+            const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, SWZ_128B);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&bars->empty[stage]);           // frees the stage once these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&bars->tfull[acc]);               // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      tc_commit(&bars->drain);                      // all issued MMAs have completed after this
+      mbar_wait_drain(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int sub = warp & 3;
+    const int row = sub * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
+      if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, args.err)) break;
+      tc_fence_after();
+      const int grow = mb * BM + row;
+      const bool row_ok = grow < args.M;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (EPI == EPI_CE) {
+        const int tgt = row_ok ? __ldg(args.targets + grow) : -1;
+        float m = -INFINITY, s = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_ld_wait();
+          const int n0 = nb * BN + c * 32;
+          if (row_ok && n0 < args.N) ce_chunk(args, r, grow, n0, tgt, m, s);
+        }
+        if (row_ok) {
+          args.pmax[(size_t)nb * args.M + grow] = m;
+          args.psum[(size_t)nb * args.M + grow] = s;
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_ld_wait();
+          const int n0 = nb * BN + c * 32;
+          if (row_ok && n0 < args.N) epilogue_chunk<EPI>(args, r, grow, n0);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                       int grid_limit, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int MB = (a.M + BM - 1) / BM;
+  const int NB = (a.N + BN - 1) / BN;
+  const int tiles = MB * NB;
+  const int grid = tiles < grid_limit ? tiles : grid_limit;
+  if (grid <= 0) return cudaSuccess;
+  gemm_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tc_bn() { return BN; }
+int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int epi,
+                           int grid_limit, cudaStream_t s) {
+  switch (epi) {
+    case EPI_BIAS_OUT: return launch_one<EPI_BIAS_OUT>(tmA, tmB, a, grid_limit, s);
+    case EPI_BIAS_GELU_OUT: return launch_one<EPI_BIAS_GELU_OUT>(tmA, tmB, a, grid_limit, s);
+    case EPI_BIAS_RESID: return launch_one<EPI_BIAS_RESID>(tmA, tmB, a, grid_limit, s);
+    case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, a, grid_limit, s);
+    case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, a, grid_limit, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gptgb

@@ -1,0 +1,80 @@
+// Host-side launchers of the library's kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gptgb {
+
+// device error codes written to the error word (the host maps them to GPT_E* values)
+enum : int {
+  GPT_DEV_OK = 0,
+  GPT_DEV_ETOKEN = 1,     // a token id outside [0, V)
+  GPT_DEV_ETARGET = 2,    // a target outside [0, V)
+  GPT_DEV_ETIMEOUT = 3,   // a bounded wait expired
+  GPT_DEV_EALIGN = 4,     // dynamic shared memory not 1024-byte aligned
+};
+
+enum Epilogue : int {
+  EPI_BIAS_OUT = 0,       // out (bf16 or fp32) = acc + bias
+  EPI_BIAS_GELU_OUT = 1,  // out = gelu(acc + bias)
+  EPI_BIAS_RESID = 2,     // out fp32 += acc + bias
+  EPI_F32 = 3,            // out fp32 = acc (+ bias)
+  EPI_CE = 4,             // per-row partial logsumexp of the tile, target capture
+};
+
+struct GemmArgs {
+  int M, N, K;
+  const float* bias;        // [N] or nullptr
+  void* out;                // row-major, row stride ldo
+  int ldo;
+  int gelu_erf;             // 0 tanh form, 1 erf form
+  const int32_t* targets;   // EPI_CE: [M]
+  float* pmax;              // EPI_CE: [NB, M] tile maxima of the logits
+  float* psum;              // EPI_CE: [NB, M] sum of exp(z - tile max)
+  float* ztgt;              // EPI_CE: [M] the target's logit
+  float* logits;            // EPI_CE: [M, ldo] fp32 or nullptr
+  int* err;                 // device error word
+  int m_fastest;            // tile order: 1 = consecutive tiles walk M
+};
+
+// ---- tensor-core (bf16) path
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;
+int gemm_tc_bn();                      // N extent of a GEMM tile (TMA box rows of W)
+int gemm_tc_num_ntiles(int N);
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int epi, int grid_limit, cudaStream_t s);
+
+constexpr int kAttnBQ = 128;
+cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T, int H, int D,
+                                int* err, cudaStream_t s);
+
+// ---- row-wise kernels (both paths)
+cudaError_t launch_embed(const int32_t* ids, const void* wte, const void* wpe, int wdt, float* x,
+                         void* out, int out_mode, int odt, const float* g, const float* b,
+                         int M, int T, int C, int V, float eps, int* err, cudaStream_t s);
+cudaError_t launch_layernorm(const float* x, const float* g, const float* b, void* out, int odt,
+                             float* out_f32, int M, int C, float eps, cudaStream_t s);
+cudaError_t launch_ce_combine(const float* pmax, const float* psum, const float* ztgt,
+                              const int32_t* targets, float* nll, int M, int NB, int V, int* err,
+                              cudaStream_t s);
+cudaError_t launch_mean(const float* nll, int M, float* loss, cudaStream_t s);
+
+// ---- fp32 SIMT parity path
+cudaError_t launch_gemm_simt(const float* A, const float* W, const float* bias, float* out,
+                             int M, int N, int K, int ldo, int epi, int gelu_erf, cudaStream_t s);
+cudaError_t launch_attention_simt(const float* qkv, float* y, int B, int T, int H, int D,
+                                  cudaStream_t s);
+cudaError_t launch_ce_rows(const float* logits, const int32_t* targets, float* nll, int M, int V,
+                           int* err, cudaStream_t s);
+
+// ---- TMA descriptors (host)
+// 2-D row-major bf16 matrix [rows, cols] with a box of box_rows x 64 columns, 128-byte swizzle.
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows);
+// qkv viewed as [B][T][3C] bf16 with a box of 128 rows x D columns (one batch).
+bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int D);
+
+}  // namespace gptgb

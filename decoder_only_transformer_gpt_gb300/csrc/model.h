@@ -1,0 +1,69 @@
+// Internal state of a model handle (shared by the library's translation units).
+#pragma once
+
+#include "../../include/gpt.h"
+#include "kernels.h"
+
+#include <vector>
+
+struct gpt_layer_dev {
+  void *attn_w, *proj_w, *fc_w, *mp_w;                     // bf16 or fp32 [out, in]
+  float *attn_b, *proj_b, *fc_b, *mp_b, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  CUtensorMap tm_attn_w, tm_proj_w, tm_fc_w, tm_mp_w;      // bf16 path only
+};
+
+struct gpt_model {
+  gpt_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  int bf16 = 0;
+  // weights
+  uint8_t* wbuf = nullptr;
+  void* wte = nullptr;
+  void* wpe = nullptr;
+  std::vector<gpt_layer_dev> layers;
+  float* lnf_g = nullptr;
+  float* lnf_b = nullptr;
+  CUtensorMap tm_wte;
+  // workspace
+  uint8_t* ws = nullptr;
+  float* x = nullptr;       // residual stream fp32 [Mx, C]
+  void* a = nullptr;        // LN output / GEMM input [Mx, C] (bf16 or fp32)
+  void* qkv = nullptr;      // [Mx, 3C]
+  void* y = nullptr;        // attention output [Mx, C]
+  void* g = nullptr;        // MLP hidden [Mx, ffn]
+  float* pmax = nullptr;    // [NB, Mx]
+  float* psum = nullptr;
+  float* ztgt = nullptr;    // [Mx]
+  float* nll = nullptr;     // [Mx]
+  float* logits_ws = nullptr;   // fp32 path: [Mx, V]
+  int* err = nullptr;       // device error word
+  int32_t* stage_ids = nullptr;
+  int32_t* stage_tg = nullptr;
+  float* stage_loss = nullptr;
+  float* stage_logits = nullptr;   // lazily allocated for gpt_forward_host with logits
+  size_t stage_logits_elems = 0;
+  int* h_pinned = nullptr;  // [0] error word, [1] loss bits
+  // activation descriptors, rebuilt when (B, T) changes
+  // timing probe (gpt_time_step) and launch counter
+  int prof_step = -1, prof_layer = -1;
+  cudaEvent_t prof_ev0 = nullptr, prof_ev1 = nullptr;
+  int launches = 0;
+  int cached_B = -1, cached_T = -1;
+  CUtensorMap tm_a, tm_y, tm_g, tm_qkv;
+};
+
+namespace gptgb {
+// thread-local text of the last failing CUDA call
+void set_detail(const char* what, cudaError_t e);
+void set_detail_text(const char* text);
+}  // namespace gptgb
+
+#define GPT_CUDA(call)                                  \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) {                            \
+      ::gptgb::set_detail(#call, e_);                   \
+      return GPT_ECUDA;                                 \
+    }                                                   \
+  } while (0)

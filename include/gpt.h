@@ -1,0 +1,167 @@
+/*
+ * gpt.h - C ABI of the GB300 (sm_103a) GPT forward + next-token cross-entropy library.
+ *
+ * What the library computes (the definitions it follows, by page and section):
+ *   x0[b,t]  = E[ids[b,t]] + P[t]                 "第 25 章 从小 GPT 到 GPT-2" §25.1;
+ *                                                "预训练一个 Mini GPT（1.24 亿参数）" 第1步
+ *   L blocks, pre-norm:  x += attn(LN1 x); x += mlp(LN2 x)              §25.1, 第4步
+ *            post-norm:  n = LN1(x + attn x); x = LN2(n + mlp n)        "GPT-1 学习笔记" §3.1-3.2
+ *   attn: qkv = a W_attn^T + b (C -> 3C), split into Q, K, U and H heads of D = C/H,
+ *         y = softmax(Q K^T / sqrt(D) + M) U with M = -inf for s > t, heads merged,
+ *         then c_proj (C -> C)                                          §25.2
+ *   mlp:  C -> ffn -> C with GELU (tanh form by default)                §25.3; "GPT-1 学习笔记" §3.6
+ *   LN:   (x - mean) / sqrt(var + eps) * g + b, biased variance         第4步; "GPT-1 学习笔记" §3.2
+ *   head: logits = h E^T, tied to the token table, no bias              §25.4
+ *   loss: mean over all B*T positions of -log softmax(logits)[target]   §25.7; 第6步
+ *
+ * Conventions
+ *   - Every function returns an int status (GPT_OK = 0, else a GPT_E* code);
+ *     nothing is thrown across the ABI. gpt_strerror() names a code.
+ *   - Weight matrices use the nn.Linear orientation [out, in] (row-major).
+ *     A source that stores Conv1D weights [in, out] must transpose exactly
+ *     the four projection matrices (§25.5); tables, LayerNorms and biases
+ *     are not transposed.
+ *   - Device pointers are CUDA device memory of the current device; host
+ *     pointers are ordinary (pageable or pinned) host memory.
+ *   - Streams are cudaStream_t values passed as void* (NULL = legacy default stream).
+ */
+#ifndef GPT_GB300_H
+#define GPT_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  GPT_OK = 0,
+  GPT_EINVAL = 1,      /* null pointer, B or T < 1, B*T > max_tokens, a dimension not a multiple of 8 */
+  GPT_ECONFIG = 2,     /* C not divisible by H ("Day 16 从零组装 MiniGPT" §三十八), unsupported head width or C */
+  GPT_ESEQ = 3,        /* T > ctx: the position table has no row for it ("Day 16 从零组装 MiniGPT" §三十九) */
+  GPT_ETOKEN = 4,      /* a token id or a target outside [0, V); found on the device */
+  GPT_ECUDA = 5,       /* a CUDA runtime or driver call failed */
+  GPT_ENOMEM = 6,      /* device or pinned-host allocation failed */
+  GPT_EDEVICE = 7,     /* a kernel's bounded wait expired or its shared memory was misaligned */
+  GPT_EUNSUPPORTED = 8 /* the device is not sm_103 (GB300) or lacks the resources */
+};
+
+/* Model hyper-parameters ("Day 16 从零组装 MiniGPT" §三, GPTConfig). */
+typedef struct gpt_config {
+  int32_t V;           /* vocabulary size */
+  int32_t C;           /* hidden width; multiple of 8 */
+  int32_t H;           /* attention heads; C % H == 0; D = C/H in {32, 64} on the bf16 path */
+  int32_t L;           /* blocks, >= 0 */
+  int32_t ctx;         /* rows of the position table = longest sequence */
+  int32_t ffn;         /* MLP hidden width (4C in GPT-2); multiple of 8 */
+  int32_t norm_mode;   /* 0 pre-norm (GPT-2), 1 post-norm (GPT-1) */
+  int32_t final_ln;    /* 1: apply ln_f before the head (pre-norm models); 0: none */
+  int32_t gelu;        /* 0 tanh approximation, 1 exact erf form */
+  int32_t dtype;       /* 0 fp32 SIMT parity mode, 1 bf16 tensor-core path (fp32 accumulation) */
+  float ln_eps;        /* LayerNorm eps inside the square root, 1e-5 */
+  int64_t max_tokens;  /* workspace bound: the largest B*T a forward call may use */
+} gpt_config;
+
+/* One block's parameters, all fp32, HOST memory, nn.Linear orientation. */
+typedef struct gpt_layer_weights {
+  const float* ln1_g;  const float* ln1_b;     /* [C], [C] */
+  const float* attn_w; const float* attn_b;    /* c_attn  [3C, C], [3C] */
+  const float* proj_w; const float* proj_b;    /* c_proj  [C, C],  [C]  */
+  const float* ln2_g;  const float* ln2_b;     /* [C], [C] */
+  const float* fc_w;   const float* fc_b;      /* c_fc    [ffn, C], [ffn] */
+  const float* mp_w;   const float* mp_b;      /* mlp c_proj [C, ffn], [C] */
+} gpt_layer_weights;
+
+typedef struct gpt_weights {
+  const float* wte;                  /* token table E [V, C]; also the tied head */
+  const float* wpe;                  /* position table P [ctx, C] */
+  const gpt_layer_weights* layers;   /* L entries */
+  const float* lnf_g;                /* [C]; may be NULL when final_ln == 0 */
+  const float* lnf_b;
+} gpt_weights;
+
+typedef struct gpt_model gpt_model;
+
+/*
+ * Create a model on the current CUDA device.
+ * cfg and weights are read during the call only: the library copies every
+ * weight into library-owned device memory (bf16 for matrices and tables when
+ * dtype == 1, fp32 otherwise; biases and LayerNorm parameters stay fp32), so
+ * the caller may free its buffers on return. It also allocates the workspace
+ * for cfg->max_tokens tokens and builds the TMA descriptors of the weights.
+ * On success *out receives the handle; on failure *out is NULL and nothing leaks.
+ */
+int gpt_create(const gpt_config* cfg, const gpt_weights* weights, gpt_model** out);
+
+/*
+ * One forward pass and (if d_targets is non-NULL) the mean cross-entropy.
+ *   d_ids      device int32 [B, T], row-major, values in [0, V)
+ *   d_targets  device int32 [B, T] or NULL (then no loss is computed)
+ *   d_loss     device fp32 scalar or NULL
+ *   d_logits   device fp32 [B, T, V] or NULL; logits are written only when
+ *              non-NULL (otherwise the head never writes them to memory)
+ * Stream-ordered and asynchronous: host-checkable errors (pointers, shapes)
+ * return immediately; device-found errors (token ids, targets, timeouts) are
+ * recorded on the device and returned by the next gpt_status(). Calls on one
+ * model share its workspace, so they must be ordered on one stream.
+ */
+int gpt_forward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, int32_t B,
+                int32_t T, float* d_loss, float* d_logits, void* stream);
+
+/*
+ * The same forward pass from HOST buffers: copies h_ids/h_targets to the
+ * device, runs gpt_forward, copies the loss (and logits if h_logits is
+ * non-NULL) back, and synchronises the stream. Returns the device status too.
+ * h_loss may be NULL only when h_targets is NULL.
+ */
+int gpt_forward_host(gpt_model* m, const int32_t* h_ids, const int32_t* h_targets, int32_t B,
+                     int32_t T, float* h_loss, float* h_logits, void* stream);
+
+/* Steps of the forward pass, for gpt_time_step(). */
+enum {
+  GPT_STEP_EMBED = 0,      /* embedding gather-add (+ first LayerNorm on pre-norm models) */
+  GPT_STEP_C_ATTN = 1,     /* fused QKV projection of block `layer` */
+  GPT_STEP_ATTN = 2,       /* causal attention of block `layer` */
+  GPT_STEP_C_PROJ = 3,     /* attention output projection + residual */
+  GPT_STEP_LN_MID = 4,     /* the LayerNorm between attention and MLP */
+  GPT_STEP_C_FC = 5,       /* MLP up-projection + GELU */
+  GPT_STEP_MLP_PROJ = 6,   /* MLP down-projection + residual */
+  GPT_STEP_LN_OUT = 7,     /* the LayerNorm after the block (next ln_1, ln_f or post-norm ln_2) */
+  GPT_STEP_HEAD = 8,       /* tied LM head (+ fused cross-entropy partials) */
+  GPT_STEP_CE = 9,         /* cross-entropy combine */
+  GPT_STEP_MEAN = 10       /* mean of the per-position losses */
+};
+
+/*
+ * Arm a timing probe for the NEXT gpt_forward on this model: ev_start
+ * (cudaEvent_t) is recorded on the forward's stream just before the kernel of
+ * `step` (in block `layer`; ignored for steps outside the blocks) and ev_stop
+ * just after it. The probe disarms after that forward. Pass ev_start == NULL
+ * to disarm.
+ */
+int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_stop);
+
+/* Number of kernels the last gpt_forward call launched (0 before the first). */
+int gpt_last_launch_count(const gpt_model* m);
+
+/* Synchronise the stream, read and clear the model's device error word. */
+int gpt_status(gpt_model* m, void* stream);
+
+/* Free everything the model owns. Safe on NULL. */
+void gpt_destroy(gpt_model* m);
+
+/* Static description of a status code. */
+const char* gpt_strerror(int code);
+
+/* Text of the last failing CUDA call made by this thread inside the library
+ * (empty if none); valid until the thread's next library call. */
+const char* gpt_last_error_detail(void);
+
+/* Unique parameter count of cfg with the tied head ("第 25 章" §25.4). */
+int64_t gpt_param_count(const gpt_config* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT_GB300_H */

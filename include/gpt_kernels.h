@@ -1,0 +1,82 @@
+/*
+ * gpt_kernels.h - per-step entry points of the GB300 GPT library.
+ *
+ * Each call runs ONE step of the forward pass (the same kernels gpt_forward
+ * launches) on caller-owned device buffers, so that every step can be checked
+ * on its own against the definitions it implements. All pointers are device
+ * pointers, 16-byte aligned; all calls are stream-ordered and asynchronous.
+ * Device-side errors (out-of-range ids, expired waits) are recorded in a
+ * library-wide device error word that gptk_status() reads and clears.
+ *
+ * dtype selects the arithmetic: 0 = fp32 SIMT kernels (fp32 operands),
+ * 1 = bf16 operands on the tcgen05 tensor-core kernels with fp32 accumulation.
+ */
+#ifndef GPT_GB300_KERNELS_H
+#define GPT_GB300_KERNELS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* GEMM epilogues */
+enum {
+  GPTK_EPI_BIAS = 0,        /* out = A W^T + bias, stored in dtype (bf16 or fp32) */
+  GPTK_EPI_BIAS_GELU = 1,   /* out = gelu_tanh(A W^T + bias) ("第 25 章" §25.3) */
+  GPTK_EPI_BIAS_RESID = 2,  /* out (fp32) += A W^T + bias: the residual add (§25.1) */
+  GPTK_EPI_F32 = 3          /* out (fp32) = A W^T (+ bias if non-NULL) */
+};
+
+/*
+ * out[M,N] = epilogue(A[M,K] . W[N,K]^T + bias[N]).
+ * A and W are row-major in dtype (nn.Linear orientation, §25.5); bias fp32
+ * [N] or NULL; out row-major with row stride N. K and N must be multiples of
+ * 8 on the bf16 path (16-byte TMA row strides).
+ */
+int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_t M, int32_t N,
+              int32_t K, int32_t epilogue, int32_t dtype, void* stream);
+
+/*
+ * Causal self-attention of one layer ("第 25 章" §25.2).
+ * qkv: [B, T, 3C] in dtype (Q, K, U thirds; head h = columns [hD, (h+1)D) of each);
+ * y:   [B, T, C] in dtype, heads merged. C = H*D; bf16 path: D in {32, 64}.
+ */
+int gptk_attention(const void* qkv, void* y, int32_t B, int32_t T, int32_t H, int32_t D,
+                   int32_t dtype, void* stream);
+
+/*
+ * LayerNorm over rows of x [M, C] fp32 ("预训练一个 Mini GPT" 第4步; "GPT-1 学习笔记" §3.2):
+ * out (dtype) = (x - mean)/sqrt(var + eps) * g + b; out_f32 (fp32, may alias x, may be NULL)
+ * receives the same values in fp32. C must be a multiple of 8 and at most 2048.
+ */
+int gptk_layernorm(const float* x, const float* g, const float* b, void* out, float* out_f32,
+                   int32_t M, int32_t C, float eps, int32_t dtype, void* stream);
+
+/*
+ * x[b,t,:] = E[ids[b,t],:] + P[t,:] as fp32 [B*T, C] ("第 25 章" §25.1).
+ * wte [V, C] and wpe [>=T, C] in dtype.
+ */
+int gptk_embed(const int32_t* ids, const void* wte, const void* wpe, float* x, int32_t B,
+               int32_t T, int32_t C, int32_t V, int32_t dtype, void* stream);
+
+/*
+ * Tied head + per-row cross-entropy: nll[m] = logsumexp_j(h_m . E_j) - h_m . E_{targets[m]}
+ * ("第 25 章" §25.4, "预训练一个 Mini GPT" 第6步). h [M, C] and wte [V, C] in dtype;
+ * nll fp32 [M]; logits fp32 [M, V] or NULL (written only when non-NULL).
+ * The bf16 path allocates its partial-logsumexp scratch on the stream.
+ */
+int gptk_lmhead_ce(const void* h, const void* wte, const int32_t* targets, float* nll,
+                   float* logits, int32_t M, int32_t V, int32_t C, int32_t dtype, void* stream);
+
+/* Deterministic mean of nll[0..M) into *loss (device fp32). */
+int gptk_mean(const float* nll, int32_t M, float* loss, void* stream);
+
+/* Synchronise the stream, then read and clear the per-step device error word. */
+int gptk_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT_GB300_KERNELS_H */

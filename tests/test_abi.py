@@ -1,0 +1,69 @@
+"""The C-ABI library builds, loads without a GPU, and exports every declared symbol."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(gptk?_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decoder_only_transformer_gpt_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for required in ("gpt_create", "gpt_forward", "gpt_destroy", "gpt_strerror", "gpt_forward_host",
+                     "gpt_status", "gptk_gemm", "gptk_attention", "gptk_lmhead_ce"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_strerror_and_param_count(lib):
+    from decoder_only_transformer_gpt_gb300 import binding
+    from workloads import workload
+    assert lib.gpt_strerror(0) == b"ok"
+    assert b"T > ctx" in lib.gpt_strerror(binding.GPT_ESEQ)
+    for name in ("toy", "minigpt", "gpt2_small", "gpt1_postnorm"):
+        import oracle
+        cfg = workload(name).cfg
+        assert binding.param_count(cfg) == oracle.param_count(cfg)
+
+
+def test_create_rejects_bad_config_without_gpu(lib):
+    import ctypes
+    from decoder_only_transformer_gpt_gb300 import binding
+    from workloads import GPTConfig
+    bad = binding.make_config(GPTConfig(V=17, C=16, H=3, L=1, ctx=12, ffn=64), 24)
+    h = ctypes.c_void_p()
+    assert lib.gpt_create(ctypes.byref(bad), None, ctypes.byref(h)) == binding.GPT_ECONFIG
+    odd = binding.make_config(GPTConfig(V=17, C=12, H=2, L=1, ctx=12, ffn=64), 24)
+    assert lib.gpt_create(ctypes.byref(odd), None, ctypes.byref(h)) == binding.GPT_EINVAL
+    assert not h.value
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "decoder_only_transformer_gpt_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("oracle-free", ""), f

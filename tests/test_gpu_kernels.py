@@ -1,0 +1,171 @@
+"""Each CUDA step against the fp64 oracle, element by element, through the C ABI.
+
+Inputs are seeded and bf16-exact, so the only differences come from the
+kernel's arithmetic; the bounds below are derived from it:
+  * fp32 accumulation of exact bf16 products over K terms: |err| <= K * 2^-23 * sum|a||w|
+  * a bf16 output adds one bf16 ulp of the value
+  * tanh.approx (GELU) adds at most 0.5|x| * 6e-4
+  * attention rounds P to bf16 (relative 2^-9 per weight): |err| <= 2^-8 * max|U| + 1 ulp
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from gpu_util import bf16_ulp, dev_bf16, dev_f32, dev_i32, host, rand_bf16  # noqa: E402
+
+EPS23 = 2.0 ** -23
+
+
+def _gemm_case(gpt_lib, M, N, K, epi, seed=0):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(seed)
+    A = rand_bf16(rng, (M, K))
+    W = rand_bf16(rng, (N, K), 0.5)
+    b = rng.standard_normal(N).astype(np.float32)
+    ref_lin = oracle.linear(A, W, b)
+    acc_bound = K * EPS23 * (np.abs(A).astype(np.float64) @ np.abs(W).astype(np.float64).T) + 1e-6
+    if epi in (binding.EPI_BIAS, binding.EPI_BIAS_GELU):
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    else:
+        x0 = rng.standard_normal((M, N)).astype(np.float32)
+        out = dev_f32(x0) if epi == binding.EPI_BIAS_RESID else torch.empty((M, N), dtype=torch.float32, device="cuda")
+    binding.gemm(dev_bf16(A), dev_bf16(W), dev_f32(b), out, epi)
+    binding.status()
+    got = host(out)
+    if epi == binding.EPI_BIAS:
+        ref = ref_lin
+        tol = bf16_ulp(ref) + acc_bound
+    elif epi == binding.EPI_BIAS_GELU:
+        ref = oracle.gelu(ref_lin)
+        tol = bf16_ulp(ref) + 1.2 * acc_bound + 0.5 * np.abs(ref_lin) * 6e-4
+    elif epi == binding.EPI_BIAS_RESID:
+        ref = x0.astype(np.float64) + ref_lin
+        tol = acc_bound + 4 * EPS23 * np.abs(ref)
+    else:
+        ref = ref_lin
+        tol = acc_bound
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside bound; worst {np.max(np.abs(got - ref) - tol)}"
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 192), (1, 8, 8), (200, 2304, 768)])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+def test_gemm_tc_epilogues(gpt_lib, M, N, K, epi):
+    _gemm_case(gpt_lib, M, N, K, epi)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 2304, 768), (1536, 768, 3072), (2000, 3072, 768)])
+def test_gemm_tc_many_tiles_per_cta(gpt_lib, M, N, K):
+    # more tiles than SMs: exercises the TMEM double buffer and the stage ring across tiles
+    _gemm_case(gpt_lib, M, N, K, 0, seed=M)
+
+
+def _attn_case(B, T, H, D, seed=0, qk_scale=1.5):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(seed)
+    C = H * D
+    qkv = rand_bf16(rng, (B, T, 3 * C))
+    qkv[..., :2 * C] = qkv[..., :2 * C] * qk_scale          # peaky softmax (power of two keeps bf16 exact)
+    y = torch.empty((B, T, C), dtype=torch.bfloat16, device="cuda")
+    binding.attention(dev_bf16(qkv), y, H)
+    binding.status()
+    ref = oracle.causal_self_attention(qkv.astype(np.float64), H)
+    got = host(y)
+    umax = np.abs(qkv[..., 2 * C:]).max()
+    tol = 2.0 ** -8 * umax + bf16_ulp(ref) + 1e-5
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside bound; worst {np.max(np.abs(got - ref) - tol)}"
+
+
+@pytest.mark.parametrize("B,T,H,D", [(1, 128, 1, 64), (2, 200, 2, 64), (1, 1, 3, 64), (3, 64, 4, 32),
+                                     (2, 777, 2, 64), (1, 1024, 2, 64), (2, 300, 3, 32)])
+def test_attention_tc(gpt_lib, B, T, H, D):
+    _attn_case(B, T, H, D, qk_scale=2.0)
+
+
+@pytest.mark.parametrize("C,M", [(768, 37), (128, 300), (16, 5), (2048, 9)])
+@pytest.mark.parametrize("odt", ["bf16", "f32"])
+def test_layernorm(gpt_lib, C, M, odt):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(C)
+    x = (rng.standard_normal((M, C)) * 3 + 0.5).astype(np.float32)
+    g = (1 + 0.2 * rng.standard_normal(C)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(C)).astype(np.float32)
+    out = torch.empty((M, C), dtype=torch.bfloat16 if odt == "bf16" else torch.float32, device="cuda")
+    xf = dev_f32(x)
+    binding.layernorm(xf, dev_f32(g), dev_f32(b), out, out_f32=xf)
+    binding.status()
+    ref = oracle.layernorm(x, g, b)
+    tol = (bf16_ulp(ref) if odt == "bf16" else 0) + 2e-6 * (np.abs(ref) + 1)
+    assert np.all(np.abs(host(out) - ref) <= tol)
+    assert np.all(np.abs(host(xf) - ref) <= 2e-6 * (np.abs(ref) + 1))      # the in-place fp32 copy
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_embed(gpt_lib, dt):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(3)
+    V, C, B, T = 1000, 768, 3, 50
+    E = rand_bf16(rng, (V, C), 0.02)
+    P = rand_bf16(rng, (64, C), 0.02)
+    ids = rng.integers(0, V, size=(B, T)).astype(np.int32)
+    x = torch.empty((B * T, C), dtype=torch.float32, device="cuda")
+    mk = dev_bf16 if dt == "bf16" else dev_f32
+    binding.embed(dev_i32(ids), mk(E), mk(P), x)
+    binding.status()
+    ref = oracle.embed(E, P, ids).reshape(B * T, C)
+    assert np.all(np.abs(host(x) - ref) <= 1e-7 * np.abs(ref))
+
+
+def test_embed_rejects_bad_token(gpt_lib):
+    from decoder_only_transformer_gpt_gb300 import binding
+    E = torch.zeros((10, 16), dtype=torch.bfloat16, device="cuda")
+    P = torch.zeros((4, 16), dtype=torch.bfloat16, device="cuda")
+    x = torch.empty((4, 16), dtype=torch.float32, device="cuda")
+    binding.embed(dev_i32(np.array([[1, 2, 10, 3]])), E, P, x)
+    with pytest.raises(binding.GptError) as e:
+        binding.status()
+    assert e.value.code == binding.GPT_ETOKEN
+    binding.status()                                                    # the word was cleared
+
+
+@pytest.mark.parametrize("M,V,C", [(300, 1000, 128), (128, 256, 64), (77, 50257, 768), (1, 17, 16)])
+def test_lmhead_ce(gpt_lib, M, V, C):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(V)
+    h = rand_bf16(rng, (M, C))
+    E = rand_bf16(rng, (V, C), 0.1)
+    tg = rng.integers(0, V, size=M).astype(np.int32)
+    nll = torch.empty(M, dtype=torch.float32, device="cuda")
+    logits = torch.empty((M, V), dtype=torch.float32, device="cuda")
+    if C % 8:
+        pytest.skip("bf16 path needs C % 8 == 0")
+    binding.lmhead_ce(dev_bf16(h), dev_bf16(E), dev_i32(tg), nll, logits)
+    binding.status()
+    zref = oracle.lm_head(h, E)
+    acc_bound = C * EPS23 * (np.abs(h).astype(np.float64) @ np.abs(E).astype(np.float64).T) + 1e-6
+    assert np.all(np.abs(host(logits) - zref) <= acc_bound)
+    nref = oracle.cross_entropy_rows(zref, tg)
+    assert np.max(np.abs(host(nll) - nref)) < 1e-4
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    binding.mean(nll, loss)
+    assert abs(float(loss.item()) - float(host(nll).mean())) < 1e-5
+
+
+def test_lmhead_ce_without_logits_matches(gpt_lib):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(9)
+    M, V, C = 500, 5000, 128
+    h = dev_bf16(rand_bf16(rng, (M, C)))
+    E = dev_bf16(rand_bf16(rng, (V, C), 0.1))
+    tg = dev_i32(rng.integers(0, V, size=M))
+    n1 = torch.empty(M, dtype=torch.float32, device="cuda")
+    n2 = torch.empty(M, dtype=torch.float32, device="cuda")
+    binding.lmhead_ce(h, E, tg, n1, torch.empty((M, V), dtype=torch.float32, device="cuda"))
+    binding.lmhead_ce(h, E, tg, n2, None)
+    binding.status()
+    assert torch.equal(n1, n2)
