@@ -183,6 +183,8 @@ def run_ours(args, rank, world, local_rank):
     # timed region: K steps, the head launch of each step bracketed by events
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in ev0 + ev1:
+        e.record(stream)          # torch creates the CUDA event on first record; the library re-records it
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
