@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
         "gptk_embed": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_lmhead_ce": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
+        "gptk_lmhead_ce_noalloc": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, vp, vp]),
         "gptk_mean": (ctypes.c_int, [vp, i32, vp, vp]),
         "gptk_status": (ctypes.c_int, [vp]),
     }
@@ -230,6 +231,18 @@ def lmhead_ce(h, wte, targets, nll, logits=None, stream=None):
     dtype = 1 if h.element_size() == 2 else 0
     _check(lib.gptk_lmhead_ce(_ptr(h), _ptr(wte), _ptr(targets), _ptr(nll), _ptr(logits), M, V, C, dtype,
                               _stream(stream)), "gptk_lmhead_ce")
+
+
+def lmhead_ce_noalloc(h, wte, targets, nll, err=None, stream=None):
+    """Head + cross-entropy with no device allocation: for callers that cannot
+    allocate while they run (a fixed start-up memory budget, a caching allocator
+    that owns the free memory, or a loop that must not synchronise). Uses the
+    library's fixed 8 MiB scratch array; `err` is an optional device int32."""
+    lib = load()
+    M, C = h.shape
+    V = wte.shape[0]
+    _check(lib.gptk_lmhead_ce_noalloc(_ptr(h), _ptr(wte), _ptr(targets), _ptr(nll), M, V, C, _ptr(err),
+                                      _stream(stream)), "gptk_lmhead_ce_noalloc")
 
 
 def mean(nll, loss, stream=None):

@@ -69,6 +69,25 @@ int gptk_embed(const int32_t* ids, const void* wte, const void* wpe, float* x, i
 int gptk_lmhead_ce(const void* h, const void* wte, const int32_t* targets, float* nll,
                    float* logits, int32_t M, int32_t V, int32_t C, int32_t dtype, void* stream);
 
+/*
+ * gptk_lmhead_ce without any device allocation (bf16 path only; the source
+ * pages have no counterpart: this is an operational variant of the step
+ * above). For callers that cannot allocate device memory while they run: a
+ * server whose memory budget is fixed at start-up, a framework whose caching
+ * allocator already holds the free memory, or a loop that cannot take the
+ * synchronisation an allocation may cause. The scratch lives in a fixed
+ * library array of 2,097,152 floats (8 MiB) that every GPU loading the library
+ * keeps until the process exits; the call returns GPT_EINVAL when
+ * M * (2 * ceil(V / 256) + 1) exceeds it (e.g. at most 5,309 rows for V = 50257).
+ * The first call on each device looks up that array's device address (with the
+ * device current); make that first call before any stream capture. All calls
+ * share the array, so calls whose GPU work overlaps race; order them on one
+ * stream. d_err: caller-owned device int that receives a nonzero code if a
+ * target is outside [0, V), or NULL; nll as in gptk_lmhead_ce. No logits.
+ */
+int gptk_lmhead_ce_noalloc(const void* h, const void* wte, const int32_t* targets, float* nll,
+                           int32_t M, int32_t V, int32_t C, int32_t* d_err, void* stream);
+
 /* Deterministic mean of nll[0..M) into *loss (device fp32). */
 int gptk_mean(const float* nll, int32_t M, float* loss, void* stream);
 
