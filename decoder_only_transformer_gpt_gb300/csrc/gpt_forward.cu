@@ -51,7 +51,10 @@ int ensure_act_maps(gpt_model* m, int B, int T) {
   const bool ok = make_tmap_2d_bf16(&m->tm_a, m->a, M, C, kGemmBM) &&
                   make_tmap_2d_bf16(&m->tm_y, m->y, M, C, kGemmBM) &&
                   make_tmap_2d_bf16(&m->tm_g, m->g, M, F, kGemmBM) &&
-                  make_tmap_qkv(&m->tm_qkv, m->qkv, B, T, 3 * C, C / m->cfg.H);
+                  make_tmap_qkv(&m->tm_qkv, m->qkv, B, T, 3 * C, C / m->cfg.H) &&
+                  make_tmap_2d(&m->tm_qkv_out, m->qkv, 2, M, 3 * C, 64, kEpiRows) &&
+                  make_tmap_2d(&m->tm_g_out, m->g, 2, M, F, 64, kEpiRows) &&
+                  make_tmap_2d(&m->tm_x_out, m->x, 4, M, C, 32, kEpiRows);
   if (!ok) {
     set_detail_text("activation tensor map");
     m->cached_B = m->cached_T = -1;
@@ -62,8 +65,8 @@ int ensure_act_maps(gpt_model* m, int B, int T) {
   return GPT_OK;
 }
 
-int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K, const float* bias,
-            void* out, int epi, cudaStream_t s) {
+int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
+            int K, const float* bias, void* out, int epi, cudaStream_t s) {
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K;
   a.bias = bias;
@@ -72,7 +75,7 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, int M,
   a.gelu_erf = m->cfg.gelu;
   a.err = m->err;
   a.m_fastest = (N > M) ? 1 : 0;        // keep the larger operand's tiles shared by co-running CTAs
-  GPT_CUDA(launch_gemm_tc(tmA, tmB, a, epi, m->num_sms, s));
+  GPT_CUDA(launch_gemm_tc(tmA, tmB, tmC, a, epi, m->num_sms, s));
   return GPT_OK;
 }
 
@@ -103,15 +106,15 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
   }
   for (int l = 0; l < L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
-    GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
+    GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
     GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_tc(m->tm_qkv, m->y, B, T, c.H, C / c.H, m->err, s), "attention"));
-    GPT_STEP(GPT_STEP_C_PROJ, l, tc_gemm(m, m->tm_y, w.tm_proj_w, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
+    GPT_STEP(GPT_STEP_C_PROJ, l, tc_gemm(m, m->tm_y, w.tm_proj_w, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
     if (pre)
       GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
     else
       GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln1_g, w.ln1_b, m->a, 1, m->x, M, C, c.ln_eps, s), "ln"));
-    GPT_STEP(GPT_STEP_C_FC, l, tc_gemm(m, m->tm_a, w.tm_fc_w, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
-    GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm(m, m->tm_g, w.tm_mp_w, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
+    GPT_STEP(GPT_STEP_C_FC, l, tc_gemm(m, m->tm_a, w.tm_fc_w, m->tm_g_out, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
+    GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm(m, m->tm_g, w.tm_mp_w, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
     if (pre) {
       NextLN n{nullptr, nullptr};
       if (l + 1 < L) n = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
@@ -136,13 +139,13 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     a.logits = d_logits;
     a.err = m->err;
     a.m_fastest = 1;
-    GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, a, EPI_CE, m->num_sms, s), "head"));
+    GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
     GPT_STEP(GPT_STEP_CE, -1,
              cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, M, gemm_tc_num_ntiles(c.V), c.V, m->err, s),
                 "ce_combine"));
     if (d_loss) GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->nll, M, d_loss, s), "mean"));
   } else if (d_logits) {
-    GPT_STEP(GPT_STEP_HEAD, -1, tc_gemm(m, m->tm_a, m->tm_wte, M, c.V, C, nullptr, d_logits, EPI_F32, s));
+    GPT_STEP(GPT_STEP_HEAD, -1, tc_gemm(m, m->tm_a, m->tm_wte, m->tm_a, M, c.V, C, nullptr, d_logits, EPI_F32, s));
   }
   return GPT_OK;
 }

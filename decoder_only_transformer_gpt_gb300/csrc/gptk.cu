@@ -50,9 +50,16 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
   if (dtype != 1 || (K % 8) || (N % 8) || !aligned16(A) || !aligned16(W) || !aligned16(out)) return GPT_EINVAL;
   int* err = err_word();
   if (!err) return GPT_ENOMEM;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC = {};
   if (!make_tmap_2d_bf16(&tmA, A, M, K, kGemmBM) || !make_tmap_2d_bf16(&tmB, W, N, K, gemm_tc_bn())) {
     set_detail_text("gemm tensor map");
+    return GPT_ECUDA;
+  }
+  bool ok_c = true;
+  if (epilogue == GPTK_EPI_BIAS || epilogue == GPTK_EPI_BIAS_GELU) ok_c = make_tmap_2d(&tmC, out, 2, M, N, 64, kEpiRows);
+  else if (epilogue == GPTK_EPI_BIAS_RESID) ok_c = make_tmap_2d(&tmC, out, 4, M, N, 32, kEpiRows);
+  if (!ok_c) {
+    set_detail_text("gemm output tensor map");
     return GPT_ECUDA;
   }
   GemmArgs a{};
@@ -60,7 +67,7 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
   a.bias = bias; a.out = out; a.ldo = N;
   a.err = err;
   a.m_fastest = N > M ? 1 : 0;
-  GPT_CUDA(launch_gemm_tc(tmA, tmB, a, epilogue, num_sms(), s));
+  GPT_CUDA(launch_gemm_tc(tmA, tmB, tmC, a, epilogue, num_sms(), s));
   return GPT_OK;
 }
 
@@ -138,7 +145,7 @@ int gptk_lmhead_ce(const void* h, const void* wte, const int32_t* targets, float
   a.logits = logits;
   a.err = err;
   a.m_fastest = 1;
-  cudaError_t e = launch_gemm_tc(tmA, tmB, a, EPI_CE, num_sms(), s);
+  cudaError_t e = launch_gemm_tc(tmA, tmB, tmA, a, EPI_CE, num_sms(), s);
   if (e == cudaSuccess) e = launch_ce_combine(a.pmax, a.psum, a.ztgt, targets, nll, M, NB, V, err, s);
   cudaFreeAsync(scratch, s);
   if (e != cudaSuccess) {

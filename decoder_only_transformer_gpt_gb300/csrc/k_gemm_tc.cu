@@ -31,8 +31,12 @@ constexpr int B_BYTES = BN * BK * 2;              // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                 // 512: two accumulators
 constexpr int THREADS = 192;
-constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF = kEpiRows * 128;            // one warp's 32-row x 128-byte staging box
+constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES;
+constexpr int BAR_OFFSET = STAGING_OFFSET + EPI_WARPS * 2 * EPI_BUF;
 constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;   // + barriers + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct __align__(8) Bars {
@@ -180,17 +184,65 @@ __device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t (&r)[
   }
 }
 
+// One warp's 32 x 128-byte chunk into its staging box: row = lane, 16-byte unit u
+// of the row at position u ^ (row & 7) (the 128-byte swizzle the TMA store reads).
+__device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const uint32_t (&w)[32]) {
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+}
+
+// Bias (+ GELU) of CW consecutive columns starting at n0, packed for the store:
+// bf16 pairs when CW == 64, fp32 bits when CW == 32.
+template <int EPI, int CW>
+__device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                             int n0, uint32_t (&w)[32]) {
+  float v[CW];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
+  if (CW == 64) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[(32 + i) % CW] = __uint_as_float(r1[i]);
+  }
+  if (a.bias != nullptr) {
+    if (n0 + CW <= a.N) {
+      const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);
+#pragma unroll
+      for (int q = 0; q < CW / 4; ++q) {
+        const float4 bb = __ldg(b4 + q);
+        v[4 * q + 0] += bb.x; v[4 * q + 1] += bb.y; v[4 * q + 2] += bb.z; v[4 * q + 3] += bb.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) v[i] += (n0 + i < a.N) ? __ldg(a.bias + n0 + i) : 0.0f;
+    }
+  }
+  if (EPI == EPI_BIAS_GELU_OUT) {
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = gelu_f(v[i], a.gelu_erf);
+  }
+  if (CW == 64) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[(2 * i + 1) % CW]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i % CW]);
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmArgs args) {
+               const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
+  uint8_t* sE = smem + STAGING_OFFSET;
   Bars* bars = reinterpret_cast<Bars*>(smem + BAR_OFFSET);
   volatile int* abort_flag = &bars->abort_flag;
 
@@ -208,7 +260,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  constexpr bool kTmaOut = (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (kTmaOut) tma_prefetch_desc(&tmC);
+  }
   if (warp == 1) tmem_alloc(&bars->tmem_base, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -278,6 +335,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------ epilogue warps
     const int sub = warp & 3;
     const int row = sub * 32 + lane;
+    uint8_t* my_stage = sE + sub * 2 * EPI_BUF;
+    int buf_sel = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -296,6 +355,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + c * 32, r);
           tmem_ld_wait();
+          if (c == BN / 32 - 1) {                     // accumulator fully read: hand it back early
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+          }
           const int n0 = nb * BN + c * 32;
           if (row_ok && n0 < args.N) ce_chunk(args, r, grow, n0, tgt, m, s);
         }
@@ -303,22 +367,56 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           args.pmax[(size_t)nb * args.M + grow] = m;
           args.psum[(size_t)nb * args.M + grow] = s;
         }
+      } else if (kTmaOut) {
+        constexpr int CW = (EPI == EPI_BIAS_RESID) ? 32 : 64;    // columns per 128-byte staged row
+        const int m0 = mb * BM + sub * 32;
+#pragma unroll 1
+        for (int c = 0; c < BN / CW; ++c) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(tbase + c * CW, r0);
+          if (CW == 64) tmem_ld_32x32b_x32(tbase + c * CW + 32, r1);
+          tmem_ld_wait();
+          if (c == BN / CW - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+          }
+          const int n0 = nb * BN + c * CW;
+          if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
+          uint32_t w[32];
+          finish_chunk<EPI, CW>(args, r0, r1, n0, w);
+          uint8_t* buf = my_stage + buf_sel * EPI_BUF;
+          if (lane == 0) bulk_wait_read_1();           // the store that last used this buffer has read it
+          __syncwarp();
+          stage_row(buf, lane, w);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (EPI == EPI_BIAS_RESID) tma_reduce_add_2d(&tmC, buf, n0, m0);   // x += tile, in L2
+            else tma_store_2d(&tmC, buf, n0, m0);
+            bulk_commit();
+          }
+          buf_sel ^= 1;
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + c * 32, r);
           tmem_ld_wait();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+          }
           const int n0 = nb * BN + c * 32;
           if (row_ok && n0 < args.N) epilogue_chunk<EPI>(args, r, grow, n0);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (kTmaOut && lane == 0) bulk_wait_all();        // stores complete before the CTA exits
   }
 
   __syncwarp();
@@ -331,7 +429,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 template <int EPI>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                        int grid_limit, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -345,7 +443,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gem
   const int tiles = MB * NB;
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
-  gemm_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
+  gemm_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, a);
   return cudaGetLastError();
 }
 
@@ -354,14 +452,14 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gem
 int gemm_tc_bn() { return BN; }
 int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
 
-cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int epi,
-                           int grid_limit, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                           int epi, int grid_limit, cudaStream_t s) {
   switch (epi) {
-    case EPI_BIAS_OUT: return launch_one<EPI_BIAS_OUT>(tmA, tmB, a, grid_limit, s);
-    case EPI_BIAS_GELU_OUT: return launch_one<EPI_BIAS_GELU_OUT>(tmA, tmB, a, grid_limit, s);
-    case EPI_BIAS_RESID: return launch_one<EPI_BIAS_RESID>(tmA, tmB, a, grid_limit, s);
-    case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, a, grid_limit, s);
-    case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, a, grid_limit, s);
+    case EPI_BIAS_OUT: return launch_one<EPI_BIAS_OUT>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_BIAS_GELU_OUT: return launch_one<EPI_BIAS_GELU_OUT>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_BIAS_RESID: return launch_one<EPI_BIAS_RESID>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, tmC, a, grid_limit, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -44,8 +44,11 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;
 int gemm_tc_bn();                      // N extent of a GEMM tile (TMA box rows of W)
 int gemm_tc_num_ntiles(int N);
-cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                           int epi, int grid_limit, cudaStream_t s);
+// tmC: the output for the TMA-store epilogues (bf16 [M,N] box 64x32 for EPI_BIAS_OUT /
+// EPI_BIAS_GELU_OUT, fp32 [M,N] box 32x32 for EPI_BIAS_RESID / EPI_F32; unused by EPI_CE).
+constexpr int kEpiRows = 32;
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                           const GemmArgs& a, int epi, int grid_limit, cudaStream_t s);
 
 constexpr int kAttnBQ = 128;
 cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T, int H, int D,
@@ -74,6 +77,10 @@ cudaError_t launch_ce_rows(const float* logits, const int32_t* targets, float* n
 // 2-D row-major bf16 matrix [rows, cols] with a box of box_rows x 64 columns, 128-byte swizzle.
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
+// General 2-D row-major matrix (bf16 or fp32) with a box of box_rows x box_cols, box_cols * elem_bytes == 128,
+// 128-byte swizzle (the GEMM epilogue's staging layout).
+bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t rows, uint64_t cols,
+                  uint32_t box_cols, uint32_t box_rows);
 // qkv viewed as [B][T][3C] bf16 with a box of 128 rows x D columns (one batch).
 bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int D);
 

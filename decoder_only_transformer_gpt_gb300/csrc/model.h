@@ -50,7 +50,8 @@ struct gpt_model {
   cudaEvent_t prof_ev0 = nullptr, prof_ev1 = nullptr;
   int launches = 0;
   int cached_B = -1, cached_T = -1;
-  CUtensorMap tm_a, tm_y, tm_g, tm_qkv;
+  CUtensorMap tm_a, tm_y, tm_g, tm_qkv;            // GEMM A operands and the attention input
+  CUtensorMap tm_qkv_out, tm_g_out, tm_x_out;      // GEMM epilogue outputs (TMA store / reduce-add)
 };
 
 namespace gptgb {
