@@ -2,8 +2,8 @@
 // waits, TMA tile loads, and the tcgen05 (5th-generation tensor core) operations
 // with their shared-memory and instruction descriptors.
 //
-// Every spin-wait is bounded by a wall-clock limit read from %globaltimer. On
-// expiry the waiting thread records GPT_DEV_ETIMEOUT in the device error word,
+// Every spin-wait is bounded (about 2 s of SM clock cycles). On expiry the
+// waiting thread records GPT_DEV_ETIMEOUT in the device error word,
 // raises the CTA's abort flag in shared memory, and returns false; every other
 // waiter of the CTA sees the abort flag and returns false as well, so a kernel
 // never hangs: it drains, frees its tensor memory and exits, and the host reads
@@ -19,16 +19,8 @@
 
 namespace gptgb {
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 __device__ __forceinline__ void record_error(int* err, int code) {
@@ -93,21 +85,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Returns false if
-// the CTA is aborting or the wall-clock limit passed (which starts the abort).
+// the CTA is aborting or the limit passed (which starts the abort). The limit
+// is counted in SM clock cycles (clock64, a cheap per-SM counter), read only
+// after 64 unsuccessful tries so that a wait on the fast path costs no timer read.
+constexpr long long kWaitLimitCycles = 4000000000LL;       // about 2 s at 2 GHz
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (clock64() - t0 > kWaitLimitCycles) {
       record_error(err, GPT_DEV_ETIMEOUT);
       *abort_flag = 1;
       return false;
     }
+  }
+}
+
+// Wait without looking at the abort flag, for at most `limit` SM cycles: used
+// only while draining a CTA's own copies and MMAs before it exits.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit = 400000000LL) {
+  if (mbar_try_wait(bar, parity)) return;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return;
   }
 }
 
@@ -152,6 +160,9 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 
 // Wait until at most one committed bulk group of this thread still reads shared memory.
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+// Wait until no committed bulk group of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Wait until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -207,6 +218,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+
+// Store 32 consecutive 32-bit columns of 32 TMEM lanes (lane i of the warp writes row lane base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+         "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+         "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

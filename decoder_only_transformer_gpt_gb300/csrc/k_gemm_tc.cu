@@ -34,7 +34,8 @@ constexpr int THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF = kEpiRows * 128;            // one warp's 32-row x 128-byte staging box
 constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES;
-constexpr int BAR_OFFSET = STAGING_OFFSET + EPI_WARPS * 2 * EPI_BUF;
+constexpr int BIAS_OFFSET = STAGING_OFFSET + EPI_WARPS * EPI_BUF;   // each warp's copy of the tile's bias
+constexpr int BAR_OFFSET = BIAS_OFFSET + EPI_WARPS * BN * 4;
 constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;   // + barriers + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,13 +56,6 @@ __device__ __forceinline__ void tile_coords(int tile, int MB, int NB, int m_fast
   else           { nb = tile % NB; mb = tile / NB; }
 }
 
-// Wait without looking at the abort flag: used only while draining on exit.
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > 200000000ull) return;     // 200 ms
-  }
-}
 
 __device__ __forceinline__ float gelu_f(float x, int erf_form) {
   if (erf_form) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
@@ -193,11 +187,12 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const uint32_t
     *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
 }
 
-// Bias (+ GELU) of CW consecutive columns starting at n0, packed for the store:
-// bf16 pairs when CW == 64, fp32 bits when CW == 32.
+// Bias (+ GELU) of CW consecutive columns, packed for the store: bf16 pairs when
+// CW == 64, fp32 bits when CW == 32. sbias: the chunk's bias in shared memory
+// (zeros past N), or nullptr.
 template <int EPI, int CW>
 __device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t (&r0)[32], const uint32_t (&r1)[32],
-                                             int n0, uint32_t (&w)[32]) {
+                                             const float* sbias, uint32_t (&w)[32]) {
   float v[CW];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
@@ -205,17 +200,12 @@ __device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t (
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[(32 + i) % CW] = __uint_as_float(r1[i]);
   }
-  if (a.bias != nullptr) {
-    if (n0 + CW <= a.N) {
-      const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);
+  if (sbias != nullptr) {
+    const float4* b4 = reinterpret_cast<const float4*>(sbias);     // same address in every lane: broadcast
 #pragma unroll
-      for (int q = 0; q < CW / 4; ++q) {
-        const float4 bb = __ldg(b4 + q);
-        v[4 * q + 0] += bb.x; v[4 * q + 1] += bb.y; v[4 * q + 2] += bb.z; v[4 * q + 3] += bb.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] += (n0 + i < a.N) ? __ldg(a.bias + n0 + i) : 0.0f;
+    for (int q = 0; q < CW / 4; ++q) {
+      const float4 bb = b4[q];
+      v[4 * q + 0] += bb.x; v[4 * q + 1] += bb.y; v[4 * q + 2] += bb.z; v[4 * q + 3] += bb.w;
     }
   }
   if (EPI == EPI_BIAS_GELU_OUT) {
@@ -243,6 +233,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   uint8_t* sE = smem + STAGING_OFFSET;
+  float* sBias = reinterpret_cast<float*>(smem + BIAS_OFFSET);
   Bars* bars = reinterpret_cast<Bars*>(smem + BAR_OFFSET);
   volatile int* abort_flag = &bars->abort_flag;
 
@@ -300,6 +291,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+      // base descriptors of stage 0 (K-major, 128-byte swizzle, 8-row groups 1024 bytes apart);
+      // the start address is the low field, so other stages and K steps are plain adds
+      const uint64_t da0 = smem_desc(smem_u32(sA), 16, 1024, SWZ_128B);
+      const uint64_t db0 = smem_desc(smem_u32(sB), 16, 1024, SWZ_128B);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -312,14 +307,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&bars->full[stage], phase, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+          const uint64_t da = da0 + static_cast<uint64_t>((stage * A_BYTES) >> 4);
+          const uint64_t db = db0 + static_cast<uint64_t>((stage * B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = smem_desc(a0 + k * 32, 16, 1024, SWZ_128B);
-            const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, SWZ_128B);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
           tc_commit(&bars->empty[stage]);           // frees the stage once these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -335,13 +327,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------ epilogue warps
     const int sub = warp & 3;
     const int row = sub * 32 + lane;
-    uint8_t* my_stage = sE + sub * 2 * EPI_BUF;
-    int buf_sel = 0;
+    uint8_t* my_stage = sE + sub * EPI_BUF;
+    float* my_bias = sBias + sub * BN;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
+      if (kTmaOut && args.bias != nullptr) {
+        // this tile's BN bias values into the warp's shared copy, while the main loop runs
+        const int nbase = nb * BN + lane * (BN / 32);
+#pragma unroll
+        for (int i = 0; i < BN / 32; ++i)
+          my_bias[lane * (BN / 32) + i] = (nbase + i < args.N) ? __ldg(args.bias + nbase + i) : 0.0f;
+        __syncwarp();
+      }
       if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, args.err)) break;
       tc_fence_after();
       const int grow = mb * BM + row;
@@ -384,9 +384,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const int n0 = nb * BN + c * CW;
           if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
           uint32_t w[32];
-          finish_chunk<EPI, CW>(args, r0, r1, n0, w);
-          uint8_t* buf = my_stage + buf_sel * EPI_BUF;
-          if (lane == 0) bulk_wait_read_1();           // the store that last used this buffer has read it
+          finish_chunk<EPI, CW>(args, r0, r1, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
+          uint8_t* buf = my_stage;
+          if (lane == 0) bulk_wait_read_0();           // the previous store has finished reading the buffer
           __syncwarp();
           stage_row(buf, lane, w);
           fence_proxy_async_smem();
@@ -396,7 +396,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             else tma_store_2d(&tmC, buf, n0, m0);
             bulk_commit();
           }
-          buf_sel ^= 1;
         }
       } else {
 #pragma unroll 1

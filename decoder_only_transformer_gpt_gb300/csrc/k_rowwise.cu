@@ -139,22 +139,36 @@ embed_kernel(const int32_t* __restrict__ ids, const WT* __restrict__ wte, const 
   if (out_mode == 2) ln_row<NV, OT>(v, lane, C, eps, g, b, out + (size_t)warp * C, nullptr);
 }
 
+// kLnRowsPerWarp rows per warp, all loads issued before any arithmetic.
+constexpr int kLnRowsPerWarp = 1;
+
 template <int NV, typename OT>
 __global__ void __launch_bounds__(kRowThreads)
 layernorm_kernel(const float* x, const float* __restrict__ g, const float* __restrict__ b, OT* __restrict__ out,
                  float* out_f32, int M, int C, float eps) {
   const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= M) return;
-  const float* xrow = x + (size_t)warp * C;
-  float v[NV][8];
+  const int row0 = warp * kLnRowsPerWarp;
+  if (row0 >= M) return;
+  float v[kLnRowsPerWarp][NV][8];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int e = (k * 32 + lane) * 8;
-    if (e < C) load8(xrow + e, v[k]);
+  for (int rr = 0; rr < kLnRowsPerWarp; ++rr) {
+    const int row = row0 + rr;
+    if (row >= M) break;
+    const float* xrow = x + (size_t)row * C;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int e = (k * 32 + lane) * 8;
+      if (e < C) load8(xrow + e, v[rr][k]);
+    }
   }
-  ln_row<NV, OT>(v, lane, C, eps, g, b, out + (size_t)warp * C,
-                 out_f32 ? out_f32 + (size_t)warp * C : nullptr);
+#pragma unroll
+  for (int rr = 0; rr < kLnRowsPerWarp; ++rr) {
+    const int row = row0 + rr;
+    if (row >= M) break;
+    ln_row<NV, OT>(v[rr], lane, C, eps, g, b, out + (size_t)row * C,
+                   out_f32 ? out_f32 + (size_t)row * C : nullptr);
+  }
 }
 
 template <typename WT, typename OT>
@@ -180,7 +194,8 @@ cudaError_t embed_dispatch(const int32_t* ids, const WT* wte, const WT* wpe, flo
 template <typename OT>
 cudaError_t ln_dispatch(const float* x, const float* g, const float* b, OT* out, float* out_f32, int M, int C,
                         float eps, cudaStream_t s) {
-  const int blocks = (M + 7) / 8;
+  const int rows_per_block = 8 * kLnRowsPerWarp;
+  const int blocks = (M + rows_per_block - 1) / rows_per_block;
   const int nv = (C + 255) / 256;
 #define GPT_LN(NVV) layernorm_kernel<NVV, OT><<<blocks, kRowThreads, 0, s>>>(x, g, b, out, out_f32, M, C, eps)
   switch (nv) {

@@ -1,0 +1,88 @@
+"""Time one step kernel of the library in isolation (CUDA events, warm-up, mean of N).
+
+    python -m decoder_only_transformer_gpt_gb300.kbench attention --B 16 --T 1024 --H 12 --D 64
+    python -m decoder_only_transformer_gpt_gb300.kbench gemm --M 16384 --N 768 --K 768 --epi 2
+    python -m decoder_only_transformer_gpt_gb300.kbench head --M 16384 --V 50257 --C 768
+    python -m decoder_only_transformer_gpt_gb300.kbench layernorm --M 16384 --C 768
+
+Inputs are random device tensors; the figure printed is algorithmic TFLOP/s
+(or GB/s for the row-wise kernels) over the mean launch time.
+"""
+import argparse
+import json
+
+import torch
+
+from . import binding
+
+
+def _time(fn, warmup, iters):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    binding.status()
+    return sum(a.elapsed_time(b) for a, b in evs) / iters
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", choices=["attention", "gemm", "head", "layernorm"])
+    ap.add_argument("--B", type=int, default=16)
+    ap.add_argument("--T", type=int, default=1024)
+    ap.add_argument("--H", type=int, default=12)
+    ap.add_argument("--D", type=int, default=64)
+    ap.add_argument("--M", type=int, default=16384)
+    ap.add_argument("--N", type=int, default=768)
+    ap.add_argument("--K", type=int, default=768)
+    ap.add_argument("--V", type=int, default=50257)
+    ap.add_argument("--C", type=int, default=768)
+    ap.add_argument("--epi", type=int, default=0)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--iters", type=int, default=10)
+    a = ap.parse_args()
+    binding.load()
+    torch.manual_seed(0)
+    dev = "cuda"
+    if a.kernel == "attention":
+        C = a.H * a.D
+        qkv = torch.randn(a.B, a.T, 3 * C, device=dev).to(torch.bfloat16)
+        y = torch.empty(a.B, a.T, C, device=dev, dtype=torch.bfloat16)
+        ms = _time(lambda: binding.attention(qkv, y, a.H), a.warmup, a.iters)
+        flop = 2.0 * C * a.T * (a.T + 1) * a.B
+        out = {"kernel": "attention", "shape": [a.B, a.T, a.H, a.D], "ms": ms, "tflops": flop / ms / 1e9}
+    elif a.kernel == "gemm":
+        A = torch.randn(a.M, a.K, device=dev).to(torch.bfloat16)
+        W = (0.05 * torch.randn(a.N, a.K, device=dev)).to(torch.bfloat16)
+        bias = torch.randn(a.N, device=dev)
+        odt = torch.bfloat16 if a.epi in (0, 1) else torch.float32
+        out_t = torch.zeros(a.M, a.N, device=dev, dtype=odt)
+        ms = _time(lambda: binding.gemm(A, W, bias, out_t, a.epi), a.warmup, a.iters)
+        flop = 2.0 * a.M * a.N * a.K
+        out = {"kernel": f"gemm_epi{a.epi}", "shape": [a.M, a.N, a.K], "ms": ms, "tflops": flop / ms / 1e9}
+    elif a.kernel == "head":
+        h = torch.randn(a.M, a.C, device=dev).to(torch.bfloat16)
+        E = (0.02 * torch.randn(a.V, a.C, device=dev)).to(torch.bfloat16)
+        tg = torch.randint(0, a.V, (a.M,), device=dev, dtype=torch.int32)
+        nll = torch.empty(a.M, device=dev)
+        ms = _time(lambda: binding.lmhead_ce(h, E, tg, nll), a.warmup, a.iters)
+        flop = 2.0 * a.M * a.V * a.C
+        out = {"kernel": "head_ce", "shape": [a.M, a.V, a.C], "ms": ms, "tflops": flop / ms / 1e9}
+    else:
+        x = torch.randn(a.M, a.C, device=dev)
+        g = torch.ones(a.C, device=dev)
+        b = torch.zeros(a.C, device=dev)
+        o = torch.empty(a.M, a.C, device=dev, dtype=torch.bfloat16)
+        ms = _time(lambda: binding.layernorm(x, g, b, o), a.warmup, a.iters)
+        byts = a.M * a.C * (4 + 2)
+        out = {"kernel": "layernorm", "shape": [a.M, a.C], "ms": ms, "gbs": byts / ms / 1e6}
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()
