@@ -27,6 +27,12 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic Dependent Launch: wait for the previous grid's completion (and
+// the visibility of its writes) before touching global memory; then let the
+// next grid begin its own prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- bf16 packing
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

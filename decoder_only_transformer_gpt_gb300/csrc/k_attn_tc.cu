@@ -31,6 +31,7 @@
 //   warps 2-5   softmax group A, warps 6-9 softmax group B
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 
 #include <math.h>
 
@@ -177,6 +178,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  pdl_wait();                       // qkv written by the previous kernel is now visible
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -450,9 +453,8 @@ cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* e
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   const float scale_log2 = kLog2e / sqrtf(static_cast<float>(D));
-  attn_fwd_tc_kernel<D><<<grid, THREADS, Cfg::SMEM, s>>>(tm, reinterpret_cast<__nv_bfloat16*>(y), B, T, H,
-                                                           n_qtiles, n_pairs, scale_log2, err);
-  return cudaGetLastError();
+  return launch_k(attn_fwd_tc_kernel<D>, dim3(grid), dim3(THREADS), Cfg::SMEM, s, tm,
+                  reinterpret_cast<__nv_bfloat16*>(y), B, T, H, n_qtiles, n_pairs, scale_log2, err);
 }
 
 }  // namespace

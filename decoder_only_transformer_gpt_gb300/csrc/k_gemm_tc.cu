@@ -15,6 +15,7 @@
 //   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4).., one output row per thread
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 
 #include <math.h>
 
@@ -262,6 +263,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  pdl_wait();                       // inputs written by the previous kernel are now visible
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -442,8 +445,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   const int tiles = MB * NB;
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
-  gemm_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmC, a);
-  return cudaGetLastError();
+  return launch_k(gemm_tc_kernel<EPI>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA, tmB, tmC, a);
 }
 
 }  // namespace

@@ -7,6 +7,7 @@
 // only: no shared memory, no block barrier.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 
 #include <math.h>
 
@@ -110,6 +111,8 @@ __global__ void __launch_bounds__(kRowThreads)
 embed_kernel(const int32_t* __restrict__ ids, const WT* __restrict__ wte, const WT* __restrict__ wpe,
              float* __restrict__ x, OT* __restrict__ out, int out_mode, const float* __restrict__ g,
              const float* __restrict__ b, int M, int T, int C, int V, float eps, int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= M) return;
@@ -146,6 +149,8 @@ template <int NV, typename OT>
 __global__ void __launch_bounds__(kRowThreads)
 layernorm_kernel(const float* x, const float* __restrict__ g, const float* __restrict__ b, OT* __restrict__ out,
                  float* out_f32, int M, int C, float eps) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int row0 = warp * kLnRowsPerWarp;
@@ -177,7 +182,8 @@ cudaError_t embed_dispatch(const int32_t* ids, const WT* wte, const WT* wpe, flo
                            cudaStream_t s) {
   const int blocks = (M + 7) / 8;
   const int nv = (C + 255) / 256;
-#define GPT_EMB(NVV) embed_kernel<NVV, WT, OT><<<blocks, kRowThreads, 0, s>>>(ids, wte, wpe, x, out, out_mode, g, b, M, T, C, V, eps, err)
+  cudaError_t e = cudaSuccess;
+#define GPT_EMB(NVV) e = launch_k(embed_kernel<NVV, WT, OT>, dim3(blocks), dim3(kRowThreads), 0, s, ids, wte, wpe, x, out, out_mode, g, b, M, T, C, V, eps, err)
   switch (nv) {
     case 1: GPT_EMB(1); break;
     case 2: GPT_EMB(2); break;
@@ -188,7 +194,7 @@ cudaError_t embed_dispatch(const int32_t* ids, const WT* wte, const WT* wpe, flo
     default: return cudaErrorInvalidValue;
   }
 #undef GPT_EMB
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename OT>
@@ -197,7 +203,8 @@ cudaError_t ln_dispatch(const float* x, const float* g, const float* b, OT* out,
   const int rows_per_block = 8 * kLnRowsPerWarp;
   const int blocks = (M + rows_per_block - 1) / rows_per_block;
   const int nv = (C + 255) / 256;
-#define GPT_LN(NVV) layernorm_kernel<NVV, OT><<<blocks, kRowThreads, 0, s>>>(x, g, b, out, out_f32, M, C, eps)
+  cudaError_t e = cudaSuccess;
+#define GPT_LN(NVV) e = launch_k(layernorm_kernel<NVV, OT>, dim3(blocks), dim3(kRowThreads), 0, s, x, g, b, out, out_f32, M, C, eps)
   switch (nv) {
     case 1: GPT_LN(1); break;
     case 2: GPT_LN(2); break;
@@ -208,7 +215,7 @@ cudaError_t ln_dispatch(const float* x, const float* g, const float* b, OT* out,
     default: return cudaErrorInvalidValue;
   }
 #undef GPT_LN
-  return cudaGetLastError();
+  return e;
 }
 
 // nll[m] = logsumexp over the row's tile partials - target logit. One thread per
@@ -217,6 +224,8 @@ __global__ void __launch_bounds__(256)
 ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum,
                   const float* __restrict__ ztgt, const int32_t* __restrict__ targets,
                   float* __restrict__ nll, int M, int NB, int V, int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   const int tg = __ldg(targets + m);
@@ -236,6 +245,8 @@ ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum
 // fp64, then a shared-memory tree in fp64. One block.
 __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ nll, int M, float* loss) {
   __shared__ double red[1024];
+  pdl_wait();
+  pdl_trigger();
   double s = 0.0;
   for (int i = threadIdx.x; i < M; i += 1024) s += static_cast<double>(nll[i]);
   red[threadIdx.x] = s;
@@ -277,14 +288,13 @@ cudaError_t launch_layernorm(const float* x, const float* g, const float* b, voi
 cudaError_t launch_ce_combine(const float* pmax, const float* psum, const float* ztgt, const int32_t* targets,
                               float* nll, int M, int NB, int V, int* err, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  ce_combine_kernel<<<(M + 255) / 256, 256, 0, s>>>(pmax, psum, ztgt, targets, nll, M, NB, V, err);
-  return cudaGetLastError();
+  return launch_k(ce_combine_kernel, dim3((M + 255) / 256), dim3(256), 0, s, pmax, psum, ztgt, targets, nll, M, NB, V,
+                  err);
 }
 
 cudaError_t launch_mean(const float* nll, int M, float* loss, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  mean_kernel<<<1, 1024, 0, s>>>(nll, M, loss);
-  return cudaGetLastError();
+  return launch_k(mean_kernel, dim3(1), dim3(1024), 0, s, nll, M, loss);
 }
 
 }  // namespace gptgb
