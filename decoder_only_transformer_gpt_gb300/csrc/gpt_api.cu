@@ -235,6 +235,7 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
   } else {
     o_logits = ws.take(Mx * V * 4);
   }
+  const size_t o_bsum = ws.take(static_cast<size_t>(ce_combine_blocks(static_cast<int>(Mx))) * 4);
   const size_t o_nll = ws.take(Mx * 4), o_err = ws.take(256), o_ids = ws.take(Mx * 4), o_tg = ws.take(Mx * 4),
                o_loss = ws.take(256);
   if (cudaMalloc(&m->ws, ws.off) != cudaSuccess) { free_model(m); return GPT_ENOMEM; }
@@ -251,6 +252,7 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
     m->logits_ws = reinterpret_cast<float*>(m->ws + o_logits);
   }
   m->nll = reinterpret_cast<float*>(m->ws + o_nll);
+  m->block_sums = reinterpret_cast<float*>(m->ws + o_bsum);
   m->err = reinterpret_cast<int*>(m->ws + o_err);
   m->stage_ids = reinterpret_cast<int32_t*>(m->ws + o_ids);
   m->stage_tg = reinterpret_cast<int32_t*>(m->ws + o_tg);

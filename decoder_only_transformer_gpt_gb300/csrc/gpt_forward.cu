@@ -141,9 +141,11 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     a.m_fastest = 1;
     GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
     GPT_STEP(GPT_STEP_CE, -1,
-             cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, M, gemm_tc_num_ntiles(c.V), c.V, m->err, s),
+             cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, m->block_sums, M, gemm_tc_num_ntiles(c.V),
+                                  c.V, m->err, s),
                 "ce_combine"));
-    if (d_loss) GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->nll, M, d_loss, s), "mean"));
+    if (d_loss)
+      GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->block_sums, ce_combine_blocks(M), M, d_loss, s), "mean"));
   } else if (d_logits) {
     GPT_STEP(GPT_STEP_HEAD, -1, tc_gemm(m, m->tm_a, m->tm_wte, m->tm_a, M, c.V, C, nullptr, d_logits, EPI_F32, s));
   }
@@ -208,7 +210,7 @@ int forward_f32(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int 
               "head"));
   if (tg) {
     GPT_STEP(GPT_STEP_CE, -1, cu(launch_ce_rows(z, tg, m->nll, M, c.V, m->err, s), "ce_rows"));
-    if (d_loss) GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->nll, M, d_loss, s), "mean"));
+    if (d_loss) GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->nll, M, M, d_loss, s), "mean"));
   }
   return GPT_OK;
 }

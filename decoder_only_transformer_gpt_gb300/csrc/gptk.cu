@@ -146,7 +146,7 @@ int gptk_lmhead_ce(const void* h, const void* wte, const int32_t* targets, float
   a.err = err;
   a.m_fastest = 1;
   cudaError_t e = launch_gemm_tc(tmA, tmB, tmA, a, EPI_CE, num_sms(), s);
-  if (e == cudaSuccess) e = launch_ce_combine(a.pmax, a.psum, a.ztgt, targets, nll, M, NB, V, err, s);
+  if (e == cudaSuccess) e = launch_ce_combine(a.pmax, a.psum, a.ztgt, targets, nll, nullptr, M, NB, V, err, s);
   cudaFreeAsync(scratch, s);
   if (e != cudaSuccess) {
     set_detail("lmhead_ce", e);
@@ -157,7 +157,7 @@ int gptk_lmhead_ce(const void* h, const void* wte, const int32_t* targets, float
 
 int gptk_mean(const float* nll, int32_t M, float* loss, void* stream) {
   if (!nll || !loss || M < 1) return GPT_EINVAL;
-  GPT_CUDA(launch_mean(nll, M, loss, reinterpret_cast<cudaStream_t>(stream)));
+  GPT_CUDA(launch_mean(nll, M, M, loss, reinterpret_cast<cudaStream_t>(stream)));
   return GPT_OK;
 }
 

@@ -94,6 +94,6 @@ extern "C" int gptk_lmhead_ce_noalloc(const void* h, const void* wte, const int3
   a.err = reinterpret_cast<int*>(d_err);
   a.m_fastest = 1;
   GPT_CUDA(launch_gemm_tc(tmA, tmB, tmA, a, EPI_CE, sm_count(), s));
-  GPT_CUDA(launch_ce_combine(a.pmax, a.psum, a.ztgt, targets, nll, M, NB, V, a.err, s));
+  GPT_CUDA(launch_ce_combine(a.pmax, a.psum, a.ztgt, targets, nll, nullptr, M, NB, V, a.err, s));
   return GPT_OK;
 }

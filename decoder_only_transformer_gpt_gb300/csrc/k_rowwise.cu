@@ -142,38 +142,23 @@ embed_kernel(const int32_t* __restrict__ ids, const WT* __restrict__ wte, const 
   if (out_mode == 2) ln_row<NV, OT>(v, lane, C, eps, g, b, out + (size_t)warp * C, nullptr);
 }
 
-// kLnRowsPerWarp rows per warp, all loads issued before any arithmetic.
-constexpr int kLnRowsPerWarp = 1;
-
+// One warp per row; the row's loads are all issued before any arithmetic.
 template <int NV, typename OT>
 __global__ void __launch_bounds__(kRowThreads)
 layernorm_kernel(const float* x, const float* __restrict__ g, const float* __restrict__ b, OT* __restrict__ out,
                  float* out_f32, int M, int C, float eps) {
   pdl_wait();
   pdl_trigger();
-  const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int row0 = warp * kLnRowsPerWarp;
-  if (row0 >= M) return;
-  float v[kLnRowsPerWarp][NV][8];
+  const int row = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  float v[NV][8];
 #pragma unroll
-  for (int rr = 0; rr < kLnRowsPerWarp; ++rr) {
-    const int row = row0 + rr;
-    if (row >= M) break;
-    const float* xrow = x + (size_t)row * C;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int e = (k * 32 + lane) * 8;
-      if (e < C) load8(xrow + e, v[rr][k]);
-    }
+  for (int k = 0; k < NV; ++k) {
+    const int e = (k * 32 + lane) * 8;
+    if (e < C) load8(x + (size_t)row * C + e, v[k]);
   }
-#pragma unroll
-  for (int rr = 0; rr < kLnRowsPerWarp; ++rr) {
-    const int row = row0 + rr;
-    if (row >= M) break;
-    ln_row<NV, OT>(v[rr], lane, C, eps, g, b, out + (size_t)row * C,
-                   out_f32 ? out_f32 + (size_t)row * C : nullptr);
-  }
+  ln_row<NV, OT>(v, lane, C, eps, g, b, out + (size_t)row * C, out_f32 ? out_f32 + (size_t)row * C : nullptr);
 }
 
 template <typename WT, typename OT>
@@ -200,8 +185,7 @@ cudaError_t embed_dispatch(const int32_t* ids, const WT* wte, const WT* wpe, flo
 template <typename OT>
 cudaError_t ln_dispatch(const float* x, const float* g, const float* b, OT* out, float* out_f32, int M, int C,
                         float eps, cudaStream_t s) {
-  const int rows_per_block = 8 * kLnRowsPerWarp;
-  const int blocks = (M + rows_per_block - 1) / rows_per_block;
+  const int blocks = (M + 7) / 8;
   const int nv = (C + 255) / 256;
   cudaError_t e = cudaSuccess;
 #define GPT_LN(NVV) e = launch_k(layernorm_kernel<NVV, OT>, dim3(blocks), dim3(kRowThreads), 0, s, x, g, b, out, out_f32, M, C, eps)
@@ -218,37 +202,73 @@ cudaError_t ln_dispatch(const float* x, const float* g, const float* b, OT* out,
   return e;
 }
 
-// nll[m] = logsumexp over the row's tile partials - target logit. One thread per
-// row; partials are stored tile-major ([NB][M]) so a warp reads 128 contiguous bytes.
-__global__ void __launch_bounds__(256)
+// nll[m] = logsumexp over the row's tile partials - target logit, in one pass.
+// A block owns 32 rows (lane = row); its 8 warps split the NB column tiles and
+// fold them online into (max, sum), then merge through shared memory. The
+// block also writes the sum of its rows' nll for the mean (fixed order).
+constexpr int kCeRows = 32;
+constexpr int kCeWarps = 8;
+
+__global__ void __launch_bounds__(kCeRows * kCeWarps)
 ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum,
                   const float* __restrict__ ztgt, const int32_t* __restrict__ targets,
-                  float* __restrict__ nll, int M, int NB, int V, int* err) {
+                  float* __restrict__ nll, float* __restrict__ block_sums, int M, int NB, int V, int* err) {
   pdl_wait();
   pdl_trigger();
-  const int m = blockIdx.x * blockDim.x + threadIdx.x;
-  if (m >= M) return;
-  const int tg = __ldg(targets + m);
-  if (tg < 0 || tg >= V) {
-    record_error(err, GPT_DEV_ETARGET);
-    nll[m] = 0.0f;
-    return;
+  __shared__ float sm_m[kCeWarps][kCeRows];
+  __shared__ float sm_s[kCeWarps][kCeRows];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int m = blockIdx.x * kCeRows + lane;
+  float mx = -INFINITY, s = 0.0f;
+  if (m < M) {
+    for (int t = warp; t < NB; t += kCeWarps) {
+      const float pm = __ldg(pmax + (size_t)t * M + m);
+      const float ps = __ldg(psum + (size_t)t * M + m);
+      if (pm > mx) {
+        s = s * expf(mx - pm) + ps;              // mx = -inf on the first tile: scale 0
+        mx = pm;
+      } else {
+        s += ps * expf(pm - mx);
+      }
+    }
   }
-  float mx = -INFINITY;
-  for (int t = 0; t < NB; ++t) mx = fmaxf(mx, __ldg(pmax + (size_t)t * M + m));
-  float s = 0.0f;
-  for (int t = 0; t < NB; ++t) s += __ldg(psum + (size_t)t * M + m) * expf(__ldg(pmax + (size_t)t * M + m) - mx);
-  nll[m] = mx + logf(s) - __ldg(ztgt + m);
+  sm_m[warp][lane] = mx;
+  sm_s[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0) {
+    float v = 0.0f;
+    if (m < M) {
+      float gm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kCeWarps; ++w) gm = fmaxf(gm, sm_m[w][lane]);
+      float gs = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kCeWarps; ++w)
+        if (sm_m[w][lane] != -INFINITY) gs += sm_s[w][lane] * expf(sm_m[w][lane] - gm);
+      const int tg = __ldg(targets + m);
+      if (tg < 0 || tg >= V) {
+        record_error(err, GPT_DEV_ETARGET);
+      } else {
+        v = gm + logf(gs) - __ldg(ztgt + m);
+      }
+      nll[m] = v;
+    }
+    // fixed-order sum of this block's 32 values
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0 && block_sums) block_sums[blockIdx.x] = v;
+  }
 }
 
-// loss = (sum of nll) / M in a fixed order: each thread sums a strided slice in
-// fp64, then a shared-memory tree in fp64. One block.
-__global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ nll, int M, float* loss) {
+// loss = (sum of the partial sums) / M in a fixed order: each thread sums a
+// strided slice in fp64, then a shared-memory tree in fp64. One block.
+__global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ part, int n, int M, float* loss) {
   __shared__ double red[1024];
   pdl_wait();
   pdl_trigger();
   double s = 0.0;
-  for (int i = threadIdx.x; i < M; i += 1024) s += static_cast<double>(nll[i]);
+  for (int i = threadIdx.x; i < n; i += 1024) s += static_cast<double>(part[i]);
   red[threadIdx.x] = s;
   __syncthreads();
   for (int w = 512; w > 0; w >>= 1) {
@@ -286,15 +306,17 @@ cudaError_t launch_layernorm(const float* x, const float* g, const float* b, voi
 }
 
 cudaError_t launch_ce_combine(const float* pmax, const float* psum, const float* ztgt, const int32_t* targets,
-                              float* nll, int M, int NB, int V, int* err, cudaStream_t s) {
+                              float* nll, float* block_sums, int M, int NB, int V, int* err, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  return launch_k(ce_combine_kernel, dim3((M + 255) / 256), dim3(256), 0, s, pmax, psum, ztgt, targets, nll, M, NB, V,
-                  err);
+  return launch_k(ce_combine_kernel, dim3((M + kCeRows - 1) / kCeRows), dim3(kCeRows * kCeWarps), 0, s, pmax, psum,
+                  ztgt, targets, nll, block_sums, M, NB, V, err);
 }
 
-cudaError_t launch_mean(const float* nll, int M, float* loss, cudaStream_t s) {
-  if (M <= 0) return cudaSuccess;
-  return launch_k(mean_kernel, dim3(1), dim3(1024), 0, s, nll, M, loss);
+int ce_combine_blocks(int M) { return (M + kCeRows - 1) / kCeRows; }
+
+cudaError_t launch_mean(const float* part, int n, int M, float* loss, cudaStream_t s) {
+  if (M <= 0 || n <= 0) return cudaSuccess;
+  return launch_k(mean_kernel, dim3(1), dim3(1024), 0, s, part, n, M, loss);
 }
 
 }  // namespace gptgb

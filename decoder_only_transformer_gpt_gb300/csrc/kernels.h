@@ -60,10 +60,14 @@ cudaError_t launch_embed(const int32_t* ids, const void* wte, const void* wpe, i
                          int M, int T, int C, int V, float eps, int* err, cudaStream_t s);
 cudaError_t launch_layernorm(const float* x, const float* g, const float* b, void* out, int odt,
                              float* out_f32, int M, int C, float eps, cudaStream_t s);
+// nll per row from the head's partials; block_sums (nullable) receives one sum of
+// nll per ce_combine_blocks(M) block, in a fixed order, for launch_mean.
 cudaError_t launch_ce_combine(const float* pmax, const float* psum, const float* ztgt,
-                              const int32_t* targets, float* nll, int M, int NB, int V, int* err,
-                              cudaStream_t s);
-cudaError_t launch_mean(const float* nll, int M, float* loss, cudaStream_t s);
+                              const int32_t* targets, float* nll, float* block_sums, int M, int NB, int V,
+                              int* err, cudaStream_t s);
+int ce_combine_blocks(int M);
+// loss = sum(part[0..n)) / M in a fixed order
+cudaError_t launch_mean(const float* part, int n, int M, float* loss, cudaStream_t s);
 
 // ---- fp32 SIMT parity path
 cudaError_t launch_gemm_simt(const float* A, const float* W, const float* bias, float* out,

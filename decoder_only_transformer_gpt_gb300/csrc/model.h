@@ -36,6 +36,7 @@ struct gpt_model {
   float* psum = nullptr;
   float* ztgt = nullptr;    // [Mx]
   float* nll = nullptr;     // [Mx]
+  float* block_sums = nullptr;  // [ce_combine_blocks(Mx)] per-block sums of nll
   float* logits_ws = nullptr;   // fp32 path: [Mx, V]
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
