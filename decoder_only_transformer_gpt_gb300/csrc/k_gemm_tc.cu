@@ -26,7 +26,7 @@ namespace {
 constexpr int BM = kGemmBM;
 constexpr int BK = kGemmBK;
 constexpr int BN = 256;
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;              // 16 KB
 constexpr int B_BYTES = BN * BK * 2;              // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -34,16 +34,26 @@ constexpr int TMEM_COLS = 2 * BN;                 // 512: two accumulators
 constexpr int THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF = kEpiRows * 128;            // one warp's 32-row x 128-byte staging box
-constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES;
-constexpr int BIAS_OFFSET = STAGING_OFFSET + EPI_WARPS * EPI_BUF;   // each warp's copy of the tile's bias
-constexpr int BAR_OFFSET = BIAS_OFFSET + EPI_WARPS * BN * 4;
-constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;   // + barriers + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int EPI_NBUF = 1;                        // staging boxes per warp
+
+// Shared-memory layout per epilogue kind: the TMA-store epilogues add a staging
+// box per epilogue warp and a copy of the tile's bias.
+template <int EPI>
+struct Layout {
+  static constexpr bool kTmaOut = (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID);
+  static constexpr int STAGES = 4;
+  static constexpr int STAGING = STAGES * STAGE_BYTES;
+  static constexpr int BIAS = STAGING + (kTmaOut ? EPI_WARPS * EPI_NBUF * EPI_BUF : 0);   // each warp's copy of the tile's bias
+  static constexpr int BAR = BIAS + (kTmaOut ? EPI_WARPS * BN * 4 : 0);
+  static constexpr int SMEM = BAR + 256 + 1024;      // + barriers + alignment slack
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(STAGES <= MAX_STAGES, "barrier arrays");
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct __align__(8) Bars {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -228,14 +238,16 @@ template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+  using LY = Layout<EPI>;
+  constexpr int STAGES = LY::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint8_t* sE = smem + STAGING_OFFSET;
-  float* sBias = reinterpret_cast<float*>(smem + BIAS_OFFSET);
-  Bars* bars = reinterpret_cast<Bars*>(smem + BAR_OFFSET);
+  uint8_t* sE = smem + LY::STAGING;
+  float* sBias = reinterpret_cast<float*>(smem + LY::BIAS);
+  Bars* bars = reinterpret_cast<Bars*>(smem + LY::BAR);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -252,7 +264,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  constexpr bool kTmaOut = (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID);
+  constexpr bool kTmaOut = LY::kTmaOut;
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -263,8 +275,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
-  pdl_wait();                       // inputs written by the previous kernel are now visible
-  pdl_trigger();
+  pdl_trigger();                    // the next kernel may begin its prologue
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -273,14 +284,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t phase = 0;
       uint32_t issued = 0, last_par = 0;
       bool ok = true;
+      // The weights (B) do not depend on the previous kernel: the first tile's
+      // first stages of B are requested before waiting for that kernel to finish.
+      int pre = 0;
+      if (static_cast<int>(blockIdx.x) < num_tiles) {
+        int mb0, nb0;
+        tile_coords(blockIdx.x, MB, NB, args.m_fastest, mb0, nb0);
+        pre = KB < STAGES ? KB : STAGES;
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_arrive_expect_tx(&bars->full[kb], STAGE_BYTES);
+          tma_load_2d(sB + kb * B_BYTES, &tmB, &bars->full[kb], kb * BK, nb0 * BN);
+        }
+      }
+      pdl_wait();                     // A, written by the previous kernel, is now visible
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
-          tma_load_2d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, nb * BN);
+          if (pre > 0) {                // stage armed and its B requested above
+            --pre;
+            tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
+          } else {
+            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
+            tma_load_2d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, nb * BN);
+          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -330,8 +359,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------ epilogue warps
     const int sub = warp & 3;
     const int row = sub * 32 + lane;
-    uint8_t* my_stage = sE + sub * EPI_BUF;
+    uint8_t* my_stage = sE + sub * EPI_NBUF * EPI_BUF;
     float* my_bias = sBias + sub * BN;
+    uint32_t n_staged = 0;                           // chunks this warp has staged (buffer ring position)
+    pdl_wait();                                      // outputs may be read-modified-written below
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -388,8 +419,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
           uint32_t w[32];
           finish_chunk<EPI, CW>(args, r0, r1, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
-          uint8_t* buf = my_stage;
-          if (lane == 0) bulk_wait_read_0();           // the previous store has finished reading the buffer
+          uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
+          ++n_staged;
+          if (lane == 0) bulk_wait_read<EPI_NBUF - 1>();   // the store that last used this box has read it
           __syncwarp();
           stage_row(buf, lane, w);
           fence_proxy_async_smem();
@@ -436,7 +468,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+                                         Layout<EPI>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -445,7 +477,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   const int tiles = MB * NB;
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
-  return launch_k(gemm_tc_kernel<EPI>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA, tmB, tmC, a);
+  return launch_k(gemm_tc_kernel<EPI>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
 }
 
 }  // namespace
