@@ -40,6 +40,80 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+# The steps of one forward pass, as numbered by the library's GPT_STEP_* probe
+# ids: (name, probe id, launched once per block).
+STEP_KINDS = [("embed", 0, False), ("c_attn", 1, True), ("attention", 2, True), ("c_proj", 3, True),
+              ("ln_mid", 4, True), ("c_fc", 5, True), ("mlp_proj", 6, True), ("ln_out", 7, True),
+              ("head", 8, False), ("ce_combine", 9, False), ("mean", 10, False)]
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the same
+# launch configuration, valid only while the kernel's sources hash to the digest recorded with it.
+NCU_TRAFFIC = {
+    "attention": {"bytes": 76.324608e6 + 6.569472e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
+                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
+                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
+                  "digest": "8c31ccb209d8b5c5d1df6f69fb2bcaa646363b12"},
+    "head": {"bytes": 102.534656e6 + 18.057728e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+             "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
+                         "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
+             "digest": "83834d9049d502883ec01d1e1aa2b3039e73f6d3"},
+}
+
+
+KERNEL_OF_STEP = {
+    "embed": "embed_kernel (token + position rows, fused first LayerNorm)",
+    "c_attn": "gemm_tc_kernel<EPI_BIAS_OUT> (fused QKV projection)",
+    "attention": "attn_fwd_tc_kernel<64> (causal attention, online softmax)",
+    "c_proj": "gemm_tc_kernel<EPI_BIAS_RESID> (attention output projection + residual)",
+    "ln_mid": "layernorm_kernel (ln_2)",
+    "c_fc": "gemm_tc_kernel<EPI_BIAS_GELU_OUT> (MLP up-projection + GELU)",
+    "mlp_proj": "gemm_tc_kernel<EPI_BIAS_RESID> (MLP down-projection + residual)",
+    "ln_out": "layernorm_kernel (next ln_1 / ln_f)",
+    "head": "gemm_tc_kernel<EPI_CE> (tied LM head + cross-entropy partials)",
+    "ce_combine": "ce_combine_kernel",
+    "mean": "mean_kernel",
+}
+
+
+def source_digest(files):
+    import hashlib
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def step_work(name, cfg, B, T):
+    """Algorithmic work of one launch of a step: (amount, bound, unit of the rate).
+
+    Contractions count 2 flops per multiply-add of the unique products (the causal
+    half of QK^T and PV for attention); row-wise steps count the bytes they must
+    move once: fp32 residual read + bf16 output for a LayerNorm, token rows of wte
+    and wpe + fp32 x + bf16 LN output for the embedding, the head's partials for
+    the combine.
+    """
+    M, C, F, V = B * T, cfg.C, cfg.ffn, cfg.V
+    nb = (V + 255) // 256
+    if name == "c_attn":
+        return 2.0 * M * 3 * C * C, "tensor"
+    if name == "attention":
+        return 2.0 * B * C * T * (T + 1), "tensor"
+    if name == "c_proj":
+        return 2.0 * M * C * C, "tensor"
+    if name in ("c_fc", "mlp_proj"):
+        return 2.0 * M * C * F, "tensor"
+    if name == "head":
+        return 2.0 * M * V * C, "tensor"
+    if name in ("ln_mid", "ln_out"):
+        return M * C * (4.0 + 2.0), "hbm"
+    if name == "embed":
+        return M * 4.0 + M * C * 2.0 + T * C * 2.0 + M * C * (4.0 + 2.0), "hbm"
+    if name == "ce_combine":
+        return 2.0 * nb * M * 4 + 3.0 * M * 4, "hbm"
+    return M * 4.0, "hbm"
+
+
 def step_flops(cfg, B, T):
     """2 * unique params * tokens + causal attention 2*L*C*T*(T+1)*B (the stated convention)."""
     from decoder_only_transformer_gpt_gb300 import binding
@@ -104,22 +178,31 @@ class ClockSampler:
 
 
 def cpu_baseline(wl, w, ids, tg, budget_s: float = 12.0):
-    """The fp64 oracle, as it stands, on a bounded sample: the first row's prefix."""
+    """The fp64 oracle, as it stands, on a bounded sample of the workload.
+
+    Sequence prefixes of row 0 double in length until one costs a sizeable part
+    of the budget (or the whole row is reached); then whole rows 1, 2, ... are
+    added until about `budget_s` seconds of oracle time have been spent.
+    """
     import oracle
     T = 128
-    best = None
     while True:
         t0 = time.perf_counter()
         oracle.forward(wl.cfg, w, ids[:1, :T], tg[:1, :T])
         dt = time.perf_counter() - t0
-        best = (T, dt)
         if dt * 2.2 > budget_s or T >= ids.shape[1]:
             break
         T = min(ids.shape[1], T * 2)
-    T, dt = best
-    return {"value": T / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"1 sequence x {T} tokens of the same workload (prefix of row 0), numpy float64",
-            "seconds": dt}
+    rows, tokens, spent = 1, T, dt
+    while T == ids.shape[1] and spent + dt < budget_s and rows < ids.shape[0]:
+        t0 = time.perf_counter()
+        oracle.forward(wl.cfg, w, ids[rows:rows + 1, :T], tg[rows:rows + 1, :T])
+        spent += time.perf_counter() - t0
+        tokens += T
+        rows += 1
+    return {"value": tokens / spent, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows} sequence(s) x {T} tokens of the same workload (rows 0..{rows - 1}), numpy float64",
+            "seconds": spent}
 
 
 def run_reference(args, rank, world):
@@ -180,11 +263,30 @@ def run_ours(args, rank, world, local_rank):
     model.status()
     launches_per_step = lib.gpt_last_launch_count(model.handle)
 
-    # timed region: K steps, the head launch of each step bracketed by events
+    # per-step breakdown (untimed): every launch of one forward bracketed by events, one probe per forward
+    pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pa.record(stream)             # torch creates the CUDA event on first record; the library re-records it
+    pb.record(stream)
+    breakdown = {}
+    for name, sid, per_block in STEP_KINDS:
+        times = []
+        for layer in (range(cfg.L) if per_block else [-1]):
+            lib.gpt_time_step(model.handle, sid, layer, pa.cuda_event, pb.cuda_event)
+            model.forward(ids, tg, loss, None, check=False)
+            torch.cuda.synchronize()
+            times.append(pa.elapsed_time(pb))
+        work, bound = step_work(name, cfg, B, T)
+        breakdown[name] = {"launches_per_step": len(times), "avg_ms": statistics.mean(times),
+                           "ms_per_step": sum(times), "work": work, "bound": bound}
+    lib.gpt_time_step(model.handle, -1, -1, None, None)
+    dom = max(breakdown, key=lambda k: breakdown[k]["ms_per_step"])
+    dom_sid, dom_per_block = next((sid, pb_) for n, sid, pb_ in STEP_KINDS if n == dom)
+
+    # timed region: K steps, one launch of the dominant step in each bracketed by events
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for e in ev0 + ev1:
-        e.record(stream)          # torch creates the CUDA event on first record; the library re-records it
+        e.record(stream)
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
@@ -194,7 +296,8 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)
     start.record(stream)
     for k in range(args.steps):
-        lib.gpt_time_step(model.handle, 8, -1, ev0[k].cuda_event, ev1[k].cuda_event)   # GPT_STEP_HEAD
+        lib.gpt_time_step(model.handle, dom_sid, (k % cfg.L) if dom_per_block else -1,
+                          ev0[k].cuda_event, ev1[k].cuda_event)
         model.forward(ids, tg, loss, None, check=False)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -202,7 +305,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     model.status()
     ms = start.elapsed_time(stop)
-    head_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    lib.gpt_time_step(model.handle, -1, -1, None, None)
+    dom_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     t = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -232,10 +336,29 @@ def run_ours(args, rank, world, local_rank):
         return
     pk, pk_src = peaks()
     flops = step_flops(cfg, B, T)
-    head_flops = 2.0 * B * T * cfg.V * cfg.C
-    head_avg = statistics.mean(head_ms)
-    achieved = head_flops / (head_avg / 1e3) / 1e12
-    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    peak_b = float(pk.get("hbm_gbs"))
+
+    def rate(work, bound, ms):
+        if bound == "tensor":
+            a = work / (ms / 1e3) / 1e12
+            return a, peak_t, "TFLOP/s"
+        a = work / (ms / 1e3) / 1e9
+        return a, peak_b, "GB/s"
+
+    total_ms = sum(v["ms_per_step"] for v in breakdown.values())
+    kernels = []
+    for name, v in sorted(breakdown.items(), key=lambda kv: -kv[1]["ms_per_step"]):
+        a, p, u = rate(v["work"], v["bound"], v["avg_ms"])
+        kernels.append({"step": name, "launches_per_step": v["launches_per_step"], "avg_ms": v["avg_ms"],
+                        "share": v["ms_per_step"] / total_ms, "bound": v["bound"], "achieved": a, "unit": u,
+                        "frac": a / p})
+    dom_avg = statistics.mean(dom_ms)
+    achieved, peak, unit = rate(breakdown[dom]["work"], breakdown[dom]["bound"], dom_avg)
+    traffic = None
+    tr = NCU_TRAFFIC.get(dom)
+    if tr is not None and (B, T) == (16, 1024) and source_digest(tr["sources"]) == tr["digest"]:
+        traffic = tr["bytes"]
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, w, ids_np, tg_np)
@@ -254,10 +377,13 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": "gemm_tc_kernel<EPI_CE> (tied LM head + cross-entropy partials)",
-                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_source": f"{pk_src} bf16 sustained", "avg_launch_ms": head_avg},
+        "roofline": {"kernel": KERNEL_OF_STEP[dom], "step": dom, "bound": breakdown[dom]["bound"],
+                     "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": traffic,
+                     "algorithmic": breakdown[dom]["work"],
+                     "peak_source": f"{pk_src} " + ("bf16 sustained" if unit == "TFLOP/s" else "HBM copy"),
+                     "avg_launch_ms": dom_avg, "launches_timed": len(dom_ms)},
+        "kernels": kernels,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
