@@ -274,7 +274,10 @@ def run_ours(args, rank, world, local_rank):
             lib.gpt_time_step(model.handle, sid, layer, pa.cuda_event, pb.cuda_event)
             model.forward(ids, tg, loss, None, check=False)
             torch.cuda.synchronize()
-            times.append(pa.elapsed_time(pb))
+            if lib.gpt_last_probe_hits(model.handle) == 1:
+                times.append(pa.elapsed_time(pb))
+        if not times:                 # the step did not run in this configuration
+            continue
         work, bound = step_work(name, cfg, B, T)
         breakdown[name] = {"launches_per_step": len(times), "avg_ms": statistics.mean(times),
                            "ms_per_step": sum(times), "work": work, "bound": bound}

@@ -72,6 +72,7 @@ def load(path: str = LIB_PATH):
         "gpt_param_count": (i64, [ctypes.POINTER(GptConfig)]),
         "gpt_time_step": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gpt_last_launch_count": (ctypes.c_int, [vp]),
+        "gpt_last_probe_hits": (ctypes.c_int, [vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),

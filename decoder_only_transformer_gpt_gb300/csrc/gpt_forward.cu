@@ -42,7 +42,7 @@ bool probe_hit(const gpt_model* m, int step, int layer) {
     const int rc_ = (expr);                                                         \
     if (rc_ != GPT_OK) return rc_;                                                  \
     ++m->launches;                                                                  \
-    if (hit_) cudaEventRecord(m->prof_ev1, s);                                      \
+    if (hit_) { cudaEventRecord(m->prof_ev1, s); ++m->probe_hits; }                 \
   } while (0)
 
 int ensure_act_maps(gpt_model* m, int B, int T) {
@@ -108,21 +108,22 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     const gpt_layer_dev& w = m->layers[l];
     GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
     GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_tc(m->tm_qkv, m->y, B, T, c.H, C / c.H, m->err, s), "attention"));
+    // the LayerNorm after each residual add: ln_2 then the next block's ln_1 or ln_f
+    // (pre-norm), ln_1 then ln_2 applied to x itself (post-norm)
+    NextLN mid = pre ? NextLN{w.ln2_g, w.ln2_b} : NextLN{w.ln1_g, w.ln1_b};
+    NextLN out{w.ln2_g, w.ln2_b};
+    if (pre) {
+      out = {nullptr, nullptr};
+      if (l + 1 < L) out = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
+      else if (c.final_ln) out = {m->lnf_g, m->lnf_b};
+    }
     GPT_STEP(GPT_STEP_C_PROJ, l, tc_gemm(m, m->tm_y, w.tm_proj_w, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
-    if (pre)
-      GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
-    else
-      GPT_STEP(GPT_STEP_LN_MID, l, cu(launch_layernorm(m->x, w.ln1_g, w.ln1_b, m->a, 1, m->x, M, C, c.ln_eps, s), "ln"));
+    GPT_STEP(GPT_STEP_LN_MID, l,
+             cu(launch_layernorm(m->x, mid.g, mid.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
     GPT_STEP(GPT_STEP_C_FC, l, tc_gemm(m, m->tm_a, w.tm_fc_w, m->tm_g_out, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
     GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm(m, m->tm_g, w.tm_mp_w, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
-    if (pre) {
-      NextLN n{nullptr, nullptr};
-      if (l + 1 < L) n = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
-      else if (c.final_ln) n = {m->lnf_g, m->lnf_b};
-      GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, n.g, n.b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
-    } else {
-      GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, m->a, 1, m->x, M, C, c.ln_eps, s), "ln"));
-    }
+    GPT_STEP(GPT_STEP_LN_OUT, l,
+             cu(launch_layernorm(m->x, out.g, out.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
   }
   if (!pre && L == 0 && c.final_ln)
     GPT_STEP(GPT_STEP_LN_OUT, -1, cu(launch_layernorm(m->x, m->lnf_g, m->lnf_b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
@@ -242,6 +243,7 @@ int gpt_forward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, in
   if (rc != GPT_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   m->launches = 0;
+  m->probe_hits = 0;
   rc = m->bf16 ? forward_bf16(m, d_ids, d_targets, B, T, d_loss, d_logits, s)
                : forward_f32(m, d_ids, d_targets, B, T, d_loss, d_logits, s);
   m->prof_ev0 = m->prof_ev1 = nullptr;       // a probe covers one forward
@@ -265,6 +267,8 @@ int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_st
 }
 
 int gpt_last_launch_count(const gpt_model* m) { return m ? m->launches : 0; }
+
+int gpt_last_probe_hits(const gpt_model* m) { return m ? m->probe_hits : 0; }
 
 int gpt_status(gpt_model* m, void* stream) {
   if (!m) return GPT_EINVAL;

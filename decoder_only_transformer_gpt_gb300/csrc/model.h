@@ -50,6 +50,7 @@ struct gpt_model {
   int prof_step = -1, prof_layer = -1;
   cudaEvent_t prof_ev0 = nullptr, prof_ev1 = nullptr;
   int launches = 0;
+  int probe_hits = 0;       // launches the armed probe bracketed in the last forward
   int cached_B = -1, cached_T = -1;
   CUtensorMap tm_a, tm_y, tm_g, tm_qkv;            // GEMM A operands and the attention input
   CUtensorMap tm_qkv_out, tm_g_out, tm_x_out;      // GEMM epilogue outputs (TMA store / reduce-add)

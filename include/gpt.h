@@ -90,6 +90,9 @@ typedef struct gpt_model gpt_model;
  * the caller may free its buffers on return. It also allocates the workspace
  * for cfg->max_tokens tokens and builds the TMA descriptors of the weights.
  * On success *out receives the handle; on failure *out is NULL and nothing leaks.
+ * GPT_GB300_NO_PDL=1 in the environment (read once per process) launches the
+ * kernels without Programmatic Dependent Launch overlap; the results are the
+ * same bit for bit.
  */
 int gpt_create(const gpt_config* cfg, const gpt_weights* weights, gpt_model** out);
 
@@ -143,6 +146,11 @@ int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_st
 
 /* Number of kernels the last gpt_forward call launched (0 before the first). */
 int gpt_last_launch_count(const gpt_model* m);
+
+/* Number of launches the probe armed for the last gpt_forward bracketed: 1, or
+ * 0 when that step did not run (the loss steps of a forward without targets, a
+ * block index past the last block). */
+int gpt_last_probe_hits(const gpt_model* m);
 
 /* Synchronise the stream, read and clear the model's device error word. */
 int gpt_status(gpt_model* m, void* stream);

@@ -69,6 +69,18 @@ def test_fp32_variants(gpt_lib, variant):
     _check(cfg, w, ids, tg)
 
 
+@pytest.mark.parametrize("variant", ["post", "erf", "noln_f", "pre"])
+def test_bf16_variants(gpt_lib, variant):
+    """The tensor-core path for each norm / GELU / final-LayerNorm variant."""
+    kw = {"post": dict(norm_mode=POST_NORM, final_ln=0), "erf": dict(gelu=GELU_ERF),
+          "noln_f": dict(final_ln=0), "pre": {}}[variant]
+    cfg = GPTConfig(V=300, C=128, H=2, L=2, ctx=80, ffn=512, dtype=DT_BF16, **kw)
+    rng = np.random.Generator(np.random.PCG64(11))
+    w = make_weights(cfg, rng, affine="random", wstd=0.02)     # GPT-2 initialisation scale
+    ids, tg = make_tokens(cfg.V, 3, 80, rng)
+    _check(cfg, w, ids, tg)
+
+
 def test_minigpt_bf16_parity(gpt_lib):
     wl = workload("minigpt")
     w, ids, tg = generate(wl, affine="random")
