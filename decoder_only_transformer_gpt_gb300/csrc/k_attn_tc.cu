@@ -17,19 +17,24 @@
 // tiles are double-buffered so the tensor core and the softmax never wait for
 // each other:
 //   S(j)  = Q K_j^T   tcgen05.mma M=128 N=128 K=D  -> TMEM S[j % 2] (128 columns each)
-//   O_h  += P(j)[:, 64h:64h+64] U_j[64h:64h+64]     -> TMEM O_h (D columns, h = 0, 1)
+//   O_h  += P(j)[:, 64h:64h+64] U_j[64h:64h+64]     -> TMEM O[item % 2]_h (h = 0, 1)
 // While the softmax turns S(j) into P(j), the tensor core already holds S(j+1)
 // and runs P(j-1) U_{j-1}; S(j+2) is issued as soon as P(j) is handed over.
+// The output accumulators are double-buffered across items, so an item's first
+// P U never waits for the previous item's output to be read.
 // P(j) is written as bf16 into one of two 128-byte-swizzled K-major shared
 // tiles (one 64-key swizzle block per half); U_j is consumed MN-major straight
 // from its TMA tile. Two softmax threads share each query row (= TMEM lane):
 // one owns keys [0, 64) of every key tile, the other keys [64, 128), each with
-// its own running max, running sum and TMEM output accumulator; the two halves
-// are merged once per item. The running max is raised lazily: a half's O and
-// sum are rescaled only when its max grows by more than 2^8.
+// its own running max, running sum and TMEM output accumulator; the scores of a
+// half stay in registers between its max pass and its exponent pass. The running
+// max is raised lazily: a half's O and sum are rescaled only when its max grows
+// by more than 2^8. At the end of an item both threads of a row exchange their
+// (max, sum) and each writes half of the row's D output columns.
 // Warp roles (320 threads, one persistent CTA per SM):
 //   warp 0      TMA producer: Q once per item, then K_j, U_j into a four-stage ring
-//   warp 1      TMEM allocator (512 columns) and MMA issuer
+//   warp 1      TMEM allocator (512 columns) and MMA issuer (the whole warp runs
+//               the loop, one elected lane issues)
 //   warps 2-5   softmax, keys [0, 64) of each tile; warps 6-9 keys [64, 128)
 #include "common.cuh"
 #include "kernels.h"
@@ -51,7 +56,7 @@ constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by 
 constexpr int NS = 4;                   // K/U ring depth (key tiles in flight)
 // TMEM columns
 constexpr uint32_t kColS = 0;           // S[0] at 0, S[1] at 128
-constexpr uint32_t kColO = 256;         // O_0 at 256, O_1 at 320
+constexpr uint32_t kColO = 256;         // O[0] at 256, O[1] at 384; half h of O[k] at + 64 h
 
 template <int D>
 struct AttnCfg {
@@ -62,8 +67,8 @@ struct AttnCfg {
   static constexpr int OFF_K = TILE;                                 // NS stages
   static constexpr int OFF_U = OFF_K + NS * TILE;                    // NS stages
   static constexpr int OFF_P = ((OFF_U + NS * TILE + 1023) / 1024) * 1024;   // P[0], P[1]
-  static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;                 // (max, sum) of the upper halves
-  static constexpr int OFF_BAR = OFF_ML + BQ * 8;
+  static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;                 // (max, sum) of both halves of every row
+  static constexpr int OFF_BAR = OFF_ML + 2 * BQ * 8;
   // at least 120 KB so that two CTAs (2 x 512 TMEM columns) never share an SM
   static constexpr int SMEM = (OFF_BAR + 256 > 120 * 1024) ? OFF_BAR + 256 : 120 * 1024;
   static_assert(D == 32 || D == 64, "head width");
@@ -78,8 +83,8 @@ struct __align__(8) AttnBars {
   uint64_t s_full[2];       // S buffer b holds a new score tile
   uint64_t p_full[2];       // P buffer b holds a tile's probabilities (8 softmax warps)
   uint64_t o_full[2];       // the P U of a step with buffer b has completed
-  uint64_t o_free;          // the item's final O has been read out of TMEM
-  uint64_t ml_full;         // the upper halves wrote their (max, sum) for the merge
+  uint64_t o_free[2];       // output buffer k has been read out of TMEM (8 softmax warps)
+  uint64_t ml_full;         // both halves wrote their (max, sum) for the merge (8 softmax warps)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -96,7 +101,7 @@ __device__ __forceinline__ void issue_s(uint32_t tS, uint64_t q_desc, uint64_t k
   constexpr uint32_t idesc = idesc_bf16_f32(BQ, BKV, false);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k)          // K-major: a K step of 16 bf16 is 32 bytes along the swizzled row
-    tc_mma_bf16(tS, desc_add(q_desc, k * 32), desc_add(k_desc, k * 32), idesc, k > 0 ? 1u : 0u);
+    tc_mma_bf16_warp(tS, desc_add(q_desc, k * 32), desc_add(k_desc, k * 32), idesc, k > 0 ? 1u : 0u);
 }
 
 template <int D>
@@ -109,7 +114,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint64_t p_desc, uint64_t 
     for (int kk = 0; kk < 4; ++kk) {
       // P: keys [64 hf, 64 hf + 64) are one swizzle block of BQ*128 bytes, 32 bytes per K step;
       // U: 16 keys = 16 rows of ROWB bytes
-      tc_mma_bf16(tO + 64 * hf, desc_add(p_desc, hf * (BQ * 128) + kk * 32),
+      tc_mma_bf16_warp(tO + 64 * hf, desc_add(p_desc, hf * (BQ * 128) + kk * 32),
                   desc_add(u_desc, (hf * 64 + kk * 16) * Cfg::ROWB), idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
   }
@@ -173,8 +178,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
       mbar_init(&bars->p_full[i], 8);
       mbar_init(&bars->o_full[i], 1);
     }
-    mbar_init(&bars->o_free, 4);
-    mbar_init(&bars->ml_full, 4);
+    mbar_init(&bars->o_free[0], 8);
+    mbar_init(&bars->o_free[1], 8);
+    mbar_init(&bars->ml_full, 8);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -220,15 +226,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         if (issued & (1u << s)) mbar_wait_drain(&bars->kv_full[s], (last_par >> s) & 1u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (whole warp; one elected lane issues)
+    {
       // base descriptors: Q and K K-major (8-row groups ROWB*8 apart), P K-major
       // 128-byte swizzle, U MN-major (K-direction 8-row groups ROWB*8 apart)
       const uint64_t dq = smem_desc(smem_u32(sQ), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t du0 = smem_desc(smem_u32(sU), Cfg::TILE, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t dp0 = smem_desc(smem_u32(sP), 16, 1024, SWZ_128B);
-      const uint32_t tO = tmem_base + kColO;
       uint32_t kv_it = 0;                            // K/U tiles consumed so far (ring position)
       uint32_t gs = 0;                               // score tiles so far: step g uses buffers g % 2
       uint32_t items_done = 0;
@@ -237,43 +242,46 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const int item = item_of(r, cta, G);
         if (item >= n_items) break;
         const Item w = decode_item(item, BH, H, n_qtiles);
-        if (!mbar_wait(&bars->q_full, static_cast<uint32_t>(r) & 1u, abort_flag, err)) break;
+        if (!mbar_wait_warp(&bars->q_full, static_cast<uint32_t>(r) & 1u, abort_flag, err)) break;
+        const uint32_t ob = items_done & 1u;
+        const uint32_t tO = tmem_base + kColO + 128 * ob;
         // the first two score tiles (the softmax read both buffers' previous tiles before
         // handing over the previous item's last probabilities)
         for (int jj = 0; jj < 2 && jj < w.n; ++jj) {
           const uint32_t t = kv_it + jj;
           const uint32_t b = (gs + jj) & 1u;
-          if (!mbar_wait(&bars->kv_full[t % NS], (t / NS) & 1u, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait_warp(&bars->kv_full[t % NS], (t / NS) & 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t % NS) * Cfg::TILE));
-          tc_commit(&bars->s_full[b]);
+          tc_commit_warp(&bars->s_full[b]);
         }
         for (int j = 0; j < w.n && ok; ++j) {
           const uint32_t g = gs + j;
           const uint32_t b = g & 1u;
           const uint32_t s = (kv_it + j) % NS;
-          if (!mbar_wait(&bars->p_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
-          if (j == 0 && items_done > 0 &&            // the previous item's O has been read out
-              !mbar_wait(&bars->o_free, (items_done - 1) & 1u, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait_warp(&bars->p_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+          // output buffer ob was last used two items ago: its values have been read out
+          if (j == 0 && items_done >= 2 &&
+              !mbar_wait_warp(&bars->o_free[ob], ((items_done >> 1) - 1) & 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           issue_pv<D>(tO, desc_add(dp0, b * P_BYTES), desc_add(du0, s * Cfg::TILE), j > 0);
-          tc_commit(&bars->o_full[b]);
-          tc_commit(&bars->kv_empty[s]);             // K_j and U_j are consumed
+          tc_commit_warp(&bars->o_full[b]);
+          tc_commit_warp(&bars->kv_empty[s]);        // K_j and U_j are consumed
           if (j + 2 < w.n) {                         // S buffer b is free again: the score tile after next
             const uint32_t t2 = kv_it + j + 2;
-            if (!mbar_wait(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
+            if (!mbar_wait_warp(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t2 % NS) * Cfg::TILE));
-            tc_commit(&bars->s_full[b]);
+            tc_commit_warp(&bars->s_full[b]);
           }
         }
         if (!ok) break;
-        tc_commit(&bars->q_empty);                   // every S of this item has read Q
+        tc_commit_warp(&bars->q_empty);              // every S of this item has read Q
         gs += w.n;
         kv_it += w.n;
         ++items_done;
       }
-      tc_commit(&bars->drain);
+      tc_commit_warp(&bars->drain);
       mbar_wait_drain(&bars->drain, 0);
     }
   } else {
@@ -282,10 +290,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
     const int sub = warp & 3;
     const int r_row = sub * 32 + lane;                // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
-    const uint32_t tO0 = tmem_base + kColO + lane_off;            // O of keys [0, 64)
-    const uint32_t tO = tO0 + 64 * hf;                              // this half's O
     uint8_t* prow = sP + hf * (BQ * 128) + (r_row >> 3) * 1024 + (r_row & 7) * 128;
-    float2* sML = reinterpret_cast<float2*>(smem_raw + Cfg::OFF_ML);
+    float2* sML = reinterpret_cast<float2*>(smem_raw + Cfg::OFF_ML);   // [2 halves][BQ rows]
     uint32_t gs = 0;
     uint32_t items_done = 0;
     bool ok = true;
@@ -294,37 +300,39 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
       if (item >= n_items) break;
       const Item w = decode_item(item, BH, H, n_qtiles);
       const int t = w.qt * BQ + r_row;                // query position
+      const uint32_t ob = items_done & 1u;
+      const uint32_t tO0 = tmem_base + kColO + 128 * ob + lane_off;   // O of keys [0, 64)
+      const uint32_t tO = tO0 + 64 * hf;                                // this half's O
       float m_run = -INFINITY;                        // running (lazily raised) max, log2 units
       float l = 0.0f;                                 // running sum of 2^(s - m_run) over this half
       for (int j = 0; j < w.n; ++j) {
         const uint32_t g = gs + j;
         const uint32_t b = g & 1u;
-        if (!mbar_wait(&bars->s_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+        if (!mbar_wait_warp(&bars->s_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tS = tmem_base + kColS + 128 * b + 64 * hf + lane_off;
         const bool diag = (j == w.n - 1);
         const int kb = j * BKV + 64 * hf;             // first key of this half
+        // this half's 64 scores, kept in registers for both passes
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32(tS, va);
+        tmem_ld_32x32b_x32(tS + 32, vb);
+        tmem_ld_wait();
         // pass 1: maximum over this half's allowed keys, eight independent chains
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-        {
-          uint32_t va[32], vb[32];
-          tmem_ld_32x32b_x32(tS, va);
-          tmem_ld_32x32b_x32(tS + 32, vb);
-          tmem_ld_wait();
-          if (diag) {
+        if (diag) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float a = (kb + i <= t) ? __uint_as_float(va[i]) : -INFINITY;
-              const float bv = (kb + 32 + i <= t) ? __uint_as_float(vb[i]) : -INFINITY;
-              mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(a, bv));
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(va[i]), __uint_as_float(vb[i])));
+          for (int i = 0; i < 32; ++i) {
+            const float a = (kb + i <= t) ? __uint_as_float(va[i]) : -INFINITY;
+            const float bv = (kb + 32 + i <= t) ? __uint_as_float(vb[i]) : -INFINITY;
+            mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(a, bv));
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(va[i]), __uint_as_float(vb[i])));
         }
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -333,7 +341,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const bool need = m_new > m_run + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
           if (j > 0) {                                // this half's O must hold all earlier P U
-            if (!mbar_wait(&bars->o_full[(g - 1) & 1u], ((g - 1) >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+            if (!mbar_wait_warp(&bars->o_full[(g - 1) & 1u], ((g - 1) >> 1) & 1u, abort_flag, err)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
           }
           const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
@@ -354,88 +365,81 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         }
         // P buffer b was last read by the P U of step g - 2 (for j < 2 that was the previous
         // item, whose last P U was waited for before its output was read)
-        if (j >= 2 && !mbar_wait(&bars->o_full[b], ((g - 2) >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait_warp(&bars->o_full[b], ((g - 2) >> 1) & 1u, abort_flag, err)) { ok = false; break; }
         // pass 2: probabilities 2^(s*scale - m_run) as bf16 into this half's swizzle block
         const float neg_m = -m_run;
+        float pv[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const uint32_t raw = i < 32 ? va[i] : vb[i - 32];
+          const float e = ex2_approx(fmaf(__uint_as_float(raw), scale_log2, neg_m));
+          pv[i] = (!diag || kb + i <= t) ? e : 0.0f;
+        }
         float ls[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) ls[k] = 0.0f;
-        uint8_t* pdst = prow + b * P_BYTES;
-        {
-          uint32_t va[32], vb[32];
-          tmem_ld_32x32b_x32(tS, va);
-          tmem_ld_32x32b_x32(tS + 32, vb);
-          tmem_ld_wait();
 #pragma unroll
-          for (int qd = 0; qd < 8; ++qd) {
-            float pv[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int col = 8 * qd + k;                     // 0..63 within the half
-              const uint32_t raw = col < 32 ? va[col & 31] : vb[col & 31];
-              const bool allowed = !diag || (kb + col) <= t;
-              pv[k] = allowed ? ex2_approx(fmaf(__uint_as_float(raw), scale_log2, neg_m)) : 0.0f;
-              ls[k] += pv[k];
-            }
-            const int unit = qd ^ (r_row & 7);
-            uint4 wv;
-            wv.x = pack_bf16x2(pv[0], pv[1]);
-            wv.y = pack_bf16x2(pv[2], pv[3]);
-            wv.z = pack_bf16x2(pv[4], pv[5]);
-            wv.w = pack_bf16x2(pv[6], pv[7]);
-            *reinterpret_cast<uint4*>(pdst + unit * 16) = wv;
-          }
-        }
+        for (int i = 0; i < 64; ++i) ls[i & 7] += pv[i];
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        uint8_t* pdst = prow + b * P_BYTES;
+#pragma unroll
+        for (int qd = 0; qd < 8; ++qd) {
+          uint4 wv;
+          wv.x = pack_bf16x2(pv[8 * qd + 0], pv[8 * qd + 1]);
+          wv.y = pack_bf16x2(pv[8 * qd + 2], pv[8 * qd + 3]);
+          wv.z = pack_bf16x2(pv[8 * qd + 4], pv[8 * qd + 5]);
+          wv.w = pack_bf16x2(pv[8 * qd + 6], pv[8 * qd + 7]);
+          *reinterpret_cast<uint4*>(pdst + ((qd ^ (r_row & 7)) << 4)) = wv;
+        }
         fence_proxy_async_smem();               // P stores -> visible to the tensor core
         tc_fence_before();                      // our TMEM reads of S are ordered before the next MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[b]);
       }
       if (!ok) break;
-      // the item's output: merge the two halves, O / l for this row
+      // the item's output: both threads of a row exchange (max, sum); each writes D/2 columns
       const uint32_t glast = gs + w.n - 1;
-      if (!mbar_wait(&bars->o_full[glast & 1u], (glast >> 1) & 1u, abort_flag, err)) break;
+      if (!mbar_wait_warp(&bars->o_full[glast & 1u], (glast >> 1) & 1u, abort_flag, err)) break;
       tc_fence_after();
-      if (hf == 1) {
-        sML[r_row] = make_float2(m_run, l);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ml_full);
+      sML[hf * BQ + r_row] = make_float2(m_run, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ml_full);
+      if (!mbar_wait_warp(&bars->ml_full, items_done & 1u, abort_flag, err)) break;
+      const float2 other = sML[(hf ^ 1) * BQ + r_row];
+      const float m0 = hf == 0 ? m_run : other.x, l0 = hf == 0 ? l : other.y;
+      const float m1 = hf == 0 ? other.x : m_run, l1 = hf == 0 ? other.y : l;
+      const float m = fmaxf(m0, m1);                // finite: key 0 of tile 0 is always allowed
+      const float a0 = ex2_approx(m0 - m);
+      const float a1 = ex2_approx(m1 - m);          // 0 when the upper half never had an allowed key
+      const float inv = 1.0f / (a0 * l0 + a1 * l1);
+      const float w0 = a0 * inv, w1 = a1 * inv;
+      constexpr int DH = D / 2;                      // output columns per thread
+      const int c0 = hf * DH;
+      uint32_t v0[DH], v1[DH];
+      if constexpr (DH == 32) {
+        tmem_ld_32x32b_x32(tO0 + c0, v0);
+        tmem_ld_32x32b_x32(tO0 + 64 + c0, v1);
       } else {
-        if (!mbar_wait(&bars->ml_full, items_done & 1u, abort_flag, err)) break;
-        const float2 ml1 = sML[r_row];
-        const float m = fmaxf(m_run, ml1.x);          // m_run is finite: key 0 of tile 0 is always allowed
-        const float a0 = ex2_approx(m_run - m);
-        const float a1 = ex2_approx(ml1.x - m);       // 0 when the upper half never had an allowed key
-        const float inv = 1.0f / (a0 * l + a1 * ml1.y);
-        const float w0 = a0 * inv, w1 = a1 * inv;
-        uint4* dst = reinterpret_cast<uint4*>(y + ((size_t)w.b * T + (t < T ? t : 0)) * C + w.h * D);
+        tmem_ld_32x32b_x16(tO0 + c0, v0);
+        tmem_ld_32x32b_x16(tO0 + 64 + c0, v1);
+      }
+      tmem_ld_wait();
+      tc_fence_before();                             // output buffer ob may be overwritten after this
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free[ob]);
+      if (t < T) {
+        uint4* dst = reinterpret_cast<uint4*>(y + ((size_t)w.b * T + t) * C + w.h * D + c0);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(tO0 + c * 32, v0);
-          tmem_ld_32x32b_x32(tO0 + 64 + c * 32, v1);
-          tmem_ld_wait();
-          if (c == D / 32 - 1) {                       // both halves read: O may be overwritten
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->o_free);
-          }
-          if (t < T) {
+        for (int q = 0; q < DH / 8; ++q) {
+          float f[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float f[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                f[i] = w0 * __uint_as_float(v0[8 * q + i]) + w1 * __uint_as_float(v1[8 * q + i]);
-              uint4 wv;
-              wv.x = pack_bf16x2(f[0], f[1]);
-              wv.y = pack_bf16x2(f[2], f[3]);
-              wv.z = pack_bf16x2(f[4], f[5]);
-              wv.w = pack_bf16x2(f[6], f[7]);
-              dst[c * 4 + q] = wv;
-            }
-          }
+          for (int i = 0; i < 8; ++i) f[i] = w0 * __uint_as_float(v0[8 * q + i]) + w1 * __uint_as_float(v1[8 * q + i]);
+          uint4 wv;
+          wv.x = pack_bf16x2(f[0], f[1]);
+          wv.y = pack_bf16x2(f[2], f[3]);
+          wv.z = pack_bf16x2(f[4], f[5]);
+          wv.w = pack_bf16x2(f[6], f[7]);
+          dst[q] = wv;
         }
       }
       gs += w.n;
