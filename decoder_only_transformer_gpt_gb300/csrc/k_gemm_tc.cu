@@ -11,7 +11,7 @@
 // accumulators of BN fp32 columns, so the epilogue of tile i overlaps the main
 // loop of tile i+1. Warp roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer (one elected lane)
-//   warp 1      TMEM allocator and MMA issuer (one elected lane)
+//   warp 1      TMEM allocator and MMA issuer (the whole warp runs the loop, one elected lane issues)
 //   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4).., one output row per thread
 #include "common.cuh"
 #include "kernels.h"
@@ -320,8 +320,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (issued & (1u << s)) mbar_wait_drain(&bars->full[s], (last_par >> s) & 1u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (whole warp; one elected lane issues)
+    {
       const uint32_t idesc = idesc_bf16_f32(BM, BN, false);
       // base descriptors of stage 0 (K-major, 128-byte swizzle, 8-row groups 1024 bytes apart);
       // the start address is the low field, so other stages and K steps are plain adds
@@ -333,26 +333,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
+        if (!mbar_wait_warp(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&bars->full[stage], phase, abort_flag, args.err)) { ok = false; break; }
+          if (!mbar_wait_warp(&bars->full[stage], phase, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = da0 + static_cast<uint64_t>((stage * A_BYTES) >> 4);
           const uint64_t db = db0 + static_cast<uint64_t>((stage * B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          tc_commit(&bars->empty[stage]);           // frees the stage once these MMAs finish
+            tc_mma_bf16_warp(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          tc_commit_warp(&bars->empty[stage]);           // frees the stage once these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&bars->tfull[acc]);               // accumulator ready for the epilogue
+        tc_commit_warp(&bars->tfull[acc]);               // accumulator ready for the epilogue
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      tc_commit(&bars->drain);                      // all issued MMAs have completed after this
+      tc_commit_warp(&bars->drain);                      // all issued MMAs have completed after this
       mbar_wait_drain(&bars->drain, 0);
     }
   } else {
