@@ -19,9 +19,10 @@
 //   S(j)  = Q K_j^T   tcgen05.mma M=128 N=128 K=D  -> TMEM S[j % 2] (128 columns each)
 //   O_h  += P(j)[:, 64h:64h+64] U_j[64h:64h+64]     -> TMEM O[item % 2]_h (h = 0, 1)
 // While the softmax turns S(j) into P(j), the tensor core already holds S(j+1)
-// and runs P(j-1) U_{j-1}; S(j+2) is issued as soon as P(j) is handed over.
-// The output accumulators are double-buffered across items, so an item's first
-// P U never waits for the previous item's output to be read.
+// and runs P(j-1) U_{j-1}; S(j+2) is issued as soon as P(j) is handed over,
+// ahead of P(j) U_j. The output accumulators and the query tile are
+// double-buffered across items, so an item's first score tile and first P U
+// never wait for the previous item's output or for its own Q load.
 // P(j) is written as bf16 into one of two 128-byte-swizzled K-major shared
 // tiles (one 64-key swizzle block per half); U_j is consumed MN-major straight
 // from its TMA tile. Two softmax threads share each query row (= TMEM lane):
@@ -32,7 +33,7 @@
 // by more than 2^8. At the end of an item both threads of a row exchange their
 // (max, sum) and each writes half of the row's D output columns.
 // Warp roles (320 threads, one persistent CTA per SM):
-//   warp 0      TMA producer: Q once per item, then K_j, U_j into a four-stage ring
+//   warp 0      TMA producer: Q once per item (two buffers), then K_j, U_j into a four-stage ring
 //   warp 1      TMEM allocator (512 columns) and MMA issuer (the whole warp runs
 //               the loop, one elected lane issues)
 //   warps 2-5   softmax, keys [0, 64) of each tile; warps 6-9 keys [64, 128)
@@ -63,8 +64,8 @@ struct AttnCfg {
   static constexpr int ROWB = D * 2;                               // bytes per row of a Q/K/U tile
   static constexpr uint32_t SWZ = (ROWB == 128) ? SWZ_128B : SWZ_64B;
   static constexpr int TILE = BQ * ROWB;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = TILE;                                 // NS stages
+  static constexpr int OFF_Q = 0;                                    // Q[0], Q[1]
+  static constexpr int OFF_K = 2 * TILE;                             // NS stages
   static constexpr int OFF_U = OFF_K + NS * TILE;                    // NS stages
   static constexpr int OFF_P = ((OFF_U + NS * TILE + 1023) / 1024) * 1024;   // P[0], P[1]
   static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;                 // (max, sum) of both halves of every row
@@ -76,8 +77,8 @@ struct AttnCfg {
 };
 
 struct __align__(8) AttnBars {
-  uint64_t q_full;
-  uint64_t q_empty;
+  uint64_t q_full[2];       // Q buffer r % 2 holds item r's query tile
+  uint64_t q_empty[2];      // every S of the item that used Q buffer k has been computed
   uint64_t kv_full[NS];
   uint64_t kv_empty[NS];
   uint64_t s_full[2];       // S buffer b holds a new score tile
@@ -167,8 +168,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
   const int cta = static_cast<int>(blockIdx.x);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
     for (int i = 0; i < NS; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
@@ -205,9 +208,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const int item = item_of(r, cta, G);
         if (item >= n_items) break;
         const Item w = decode_item(item, BH, H, n_qtiles);
-        if (r > 0 && !mbar_wait(&bars->q_empty, static_cast<uint32_t>(r - 1) & 1u, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&bars->q_full, Cfg::TILE);
-        tma_load_3d(sQ, &tm, &bars->q_full, w.h * D, w.qt * BQ, w.b);
+        const int qb = r & 1;                        // Q buffer of this item; its previous user was item r - 2
+        if (r >= 2 && !mbar_wait(&bars->q_empty[qb], static_cast<uint32_t>((r >> 1) - 1) & 1u, abort_flag, err)) break;
+        mbar_arrive_expect_tx(&bars->q_full[qb], Cfg::TILE);
+        tma_load_3d(sQ + qb * Cfg::TILE, &tm, &bars->q_full[qb], w.h * D, w.qt * BQ, w.b);
         ++q_loads;
         for (int j = 0; j < w.n; ++j, ++kv_it) {
           const int s = kv_it % NS;
@@ -221,7 +225,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         }
       }
       // never leave with copies in flight into this CTA's shared memory
-      if (q_loads > 0) mbar_wait_drain(&bars->q_full, (q_loads - 1) & 1u);
+      for (uint32_t k = q_loads > 2 ? q_loads - 2 : 0; k < q_loads; ++k)
+        mbar_wait_drain(&bars->q_full[k & 1u], (k >> 1) & 1u);
       for (int s = 0; s < NS; ++s)
         if (issued & (1u << s)) mbar_wait_drain(&bars->kv_full[s], (last_par >> s) & 1u);
     }
@@ -230,7 +235,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
     {
       // base descriptors: Q and K K-major (8-row groups ROWB*8 apart), P K-major
       // 128-byte swizzle, U MN-major (K-direction 8-row groups ROWB*8 apart)
-      const uint64_t dq = smem_desc(smem_u32(sQ), 16, 8 * Cfg::ROWB, Cfg::SWZ);
+      const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t du0 = smem_desc(smem_u32(sU), Cfg::TILE, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t dp0 = smem_desc(smem_u32(sP), 16, 1024, SWZ_128B);
@@ -242,7 +247,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const int item = item_of(r, cta, G);
         if (item >= n_items) break;
         const Item w = decode_item(item, BH, H, n_qtiles);
-        if (!mbar_wait_warp(&bars->q_full, static_cast<uint32_t>(r) & 1u, abort_flag, err)) break;
+        const int qb = r & 1;
+        if (!mbar_wait_warp(&bars->q_full[qb], static_cast<uint32_t>(r >> 1) & 1u, abort_flag, err)) break;
+        const uint64_t dq = desc_add(dq0, qb * Cfg::TILE);
         const uint32_t ob = items_done & 1u;
         const uint32_t tO = tmem_base + kColO + 128 * ob;
         // the first two score tiles (the softmax read both buffers' previous tiles before
@@ -260,6 +267,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
           const uint32_t b = g & 1u;
           const uint32_t s = (kv_it + j) % NS;
           if (!mbar_wait_warp(&bars->p_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          // S buffer b is free again (the softmax has read S(j)): the score tile after next
+          // goes first, so the softmax never waits behind this step's P U
+          if (j + 2 < w.n) {
+            const uint32_t t2 = kv_it + j + 2;
+            if (!mbar_wait_warp(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t2 % NS) * Cfg::TILE));
+            tc_commit_warp(&bars->s_full[b]);
+          }
           // output buffer ob was last used two items ago: its values have been read out
           if (j == 0 && items_done >= 2 &&
               !mbar_wait_warp(&bars->o_free[ob], ((items_done >> 1) - 1) & 1u, abort_flag, err)) { ok = false; break; }
@@ -267,16 +284,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
           issue_pv<D>(tO, desc_add(dp0, b * P_BYTES), desc_add(du0, s * Cfg::TILE), j > 0);
           tc_commit_warp(&bars->o_full[b]);
           tc_commit_warp(&bars->kv_empty[s]);        // K_j and U_j are consumed
-          if (j + 2 < w.n) {                         // S buffer b is free again: the score tile after next
-            const uint32_t t2 = kv_it + j + 2;
-            if (!mbar_wait_warp(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t2 % NS) * Cfg::TILE));
-            tc_commit_warp(&bars->s_full[b]);
-          }
         }
         if (!ok) break;
-        tc_commit_warp(&bars->q_empty);              // every S of this item has read Q
+        tc_commit_warp(&bars->q_empty[qb]);          // every S of this item has read its Q
         gs += w.n;
         kv_it += w.n;
         ++items_done;
