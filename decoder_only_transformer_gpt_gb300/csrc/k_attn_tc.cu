@@ -14,23 +14,24 @@
 // A work item is one (b, h) and one 128-row query tile; the kernel is
 // persistent (one CTA per SM walks its items, heaviest first, snake-dealt) and
 // keeps its barriers, TMEM and K/U ring across items. Inside an item the score
-// tiles are double-buffered so the tensor core and the softmax never wait for
-// each other:
+// tiles are double-buffered so the tensor core and the softmax overlap:
 //   S(j)  = Q K_j^T   tcgen05.mma M=128 N=128 K=D  -> TMEM S[j % 2] (128 columns each)
-//   O_h  += P(j)[:, 64h:64h+64] U_j[64h:64h+64]     -> TMEM O[item % 2]_h (h = 0, 1)
-// While the softmax turns S(j) into P(j), the tensor core already holds S(j+1)
-// and runs P(j-1) U_{j-1}; S(j+2) is issued as soon as P(j) is handed over,
-// ahead of P(j) U_j. The output accumulators and the query tile are
-// double-buffered across items, so an item's first score tile and first P U
-// never wait for the previous item's output or for its own Q load.
-// P(j) is written as bf16 into one of two 128-byte-swizzled K-major shared
-// tiles (one 64-key swizzle block per half); U_j is consumed MN-major straight
-// from its TMA tile. Two softmax threads share each query row (= TMEM lane):
-// one owns keys [0, 64) of every key tile, the other keys [64, 128), each with
-// its own running max, running sum and TMEM output accumulator; the scores of a
-// half stay in registers between its max pass and its exponent pass. The running
-// max is raised lazily: a half's O and sum are rescaled only when its max grows
-// by more than 2^8. At the end of an item both threads of a row exchange their
+//   O_h  += P(j)_h U_j[64h:64h+64]                 -> TMEM O[item % 2]_h (h = 0, 1)
+// The softmax reads its 64 scores of S(j) into registers and writes P(j) back
+// as bf16 pairs over the first 32 columns of the same 64 (row = lane), so the
+// P U MMA takes its A operand straight from tensor memory: probabilities never
+// pass through shared memory. While the softmax turns S(j) into P(j), the
+// tensor core already holds S(j+1); once P(j) is handed over it runs P(j) U_j
+// and then S(j+2) into the same buffer (one thread's MMAs execute in issue
+// order, so S(j+2) overwrites P(j) only after P(j) U_j has read it). The output
+// accumulators and the query tile are double-buffered across items, so an
+// item's first score tile and first P U never wait for the previous item's
+// output or for its own Q load. U_j is consumed MN-major straight from its TMA
+// tile. Two softmax threads share each query row (= TMEM lane): one owns keys
+// [0, 64) of every key tile, the other keys [64, 128), each with its own
+// running max, running sum and TMEM output accumulator. The running max is
+// raised lazily: a half's O and sum are rescaled only when its max grows by
+// more than 2^8. At the end of an item both threads of a row exchange their
 // (max, sum) and each writes half of the row's D output columns.
 // Warp roles (320 threads, one persistent CTA per SM):
 //   warp 0      TMA producer: Q once per item (two buffers), then K_j, U_j into a four-stage ring
@@ -51,7 +52,6 @@ constexpr int BQ = kAttnBQ;       // query rows per tile
 constexpr int BKV = 128;          // keys per tile
 constexpr int THREADS = 320;
 constexpr int TMEM_COLS = 512;
-constexpr int P_BYTES = BQ * BKV * 2;   // two 128-byte-swizzled blocks of 64 keys
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by more than this
 constexpr int NS = 4;                   // K/U ring depth (key tiles in flight)
@@ -67,8 +67,7 @@ struct AttnCfg {
   static constexpr int OFF_Q = 0;                                    // Q[0], Q[1]
   static constexpr int OFF_K = 2 * TILE;                             // NS stages
   static constexpr int OFF_U = OFF_K + NS * TILE;                    // NS stages
-  static constexpr int OFF_P = ((OFF_U + NS * TILE + 1023) / 1024) * 1024;   // P[0], P[1]
-  static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;                 // (max, sum) of both halves of every row
+  static constexpr int OFF_ML = OFF_U + NS * TILE;                  // (max, sum) of both halves of every row
   static constexpr int OFF_BAR = OFF_ML + 2 * BQ * 8;
   // at least 120 KB so that two CTAs (2 x 512 TMEM columns) never share an SM
   static constexpr int SMEM = (OFF_BAR + 256 > 120 * 1024) ? OFF_BAR + 256 : 120 * 1024;
@@ -105,18 +104,20 @@ __device__ __forceinline__ void issue_s(uint32_t tS, uint64_t q_desc, uint64_t k
     tc_mma_bf16_warp(tS, desc_add(q_desc, k * 32), desc_add(k_desc, k * 32), idesc, k > 0 ? 1u : 0u);
 }
 
+// O_h += P(j)_h U_h for both key halves h: P(j) lies in TMEM over the first 32
+// columns of each 64-column half of its score buffer (two bf16 per column, row =
+// lane), U_j is MN-major in shared memory (D contiguous per key).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint64_t p_desc, uint64_t u_desc, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint64_t u_desc, bool accumulate) {
   using Cfg = AttnCfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(BQ, D, true);     // U is MN-major (D contiguous)
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      // P: keys [64 hf, 64 hf + 64) are one swizzle block of BQ*128 bytes, 32 bytes per K step;
-      // U: 16 keys = 16 rows of ROWB bytes
-      tc_mma_bf16_warp(tO + 64 * hf, desc_add(p_desc, hf * (BQ * 128) + kk * 32),
-                  desc_add(u_desc, (hf * 64 + kk * 16) * Cfg::ROWB), idesc, (accumulate || kk > 0) ? 1u : 0u);
+      // a K step of 16 keys is 8 TMEM columns of P and 16 rows of ROWB bytes of U
+      tc_mma_bf16_ts_warp(tO + 64 * hf, tP + 64 * hf + 8 * kk, desc_add(u_desc, (hf * 64 + kk * 16) * Cfg::ROWB),
+                          idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
   }
 }
@@ -158,7 +159,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
   uint8_t* sQ = smem_raw + Cfg::OFF_Q;
   uint8_t* sK = smem_raw + Cfg::OFF_K;
   uint8_t* sU = smem_raw + Cfg::OFF_U;
-  uint8_t* sP = smem_raw + Cfg::OFF_P;
   volatile int* abort_flag = &bars->abort_flag;
 
   const int BH = B * H;
@@ -238,7 +238,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
       const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t du0 = smem_desc(smem_u32(sU), Cfg::TILE, 8 * Cfg::ROWB, Cfg::SWZ);
-      const uint64_t dp0 = smem_desc(smem_u32(sP), 16, 1024, SWZ_128B);
       uint32_t kv_it = 0;                            // K/U tiles consumed so far (ring position)
       uint32_t gs = 0;                               // score tiles so far: step g uses buffers g % 2
       uint32_t items_done = 0;
@@ -267,9 +266,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
           const uint32_t b = g & 1u;
           const uint32_t s = (kv_it + j) % NS;
           if (!mbar_wait_warp(&bars->p_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+          // output buffer ob was last used two items ago: its values have been read out
+          if (j == 0 && items_done >= 2 &&
+              !mbar_wait_warp(&bars->o_free[ob], ((items_done >> 1) - 1) & 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
-          // S buffer b is free again (the softmax has read S(j)): the score tile after next
-          // goes first, so the softmax never waits behind this step's P U
+          issue_pv<D>(tO, tmem_base + kColS + 128 * b, desc_add(du0, s * Cfg::TILE), j > 0);
+          tc_commit_warp(&bars->o_full[b]);
+          tc_commit_warp(&bars->kv_empty[s]);        // K_j and U_j are consumed
+          // the score tile after next into buffer b: issued after P(j) U_j, which reads
+          // P(j) out of the same columns (one thread's MMAs run in issue order)
           if (j + 2 < w.n) {
             const uint32_t t2 = kv_it + j + 2;
             if (!mbar_wait_warp(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
@@ -277,13 +282,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
             issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t2 % NS) * Cfg::TILE));
             tc_commit_warp(&bars->s_full[b]);
           }
-          // output buffer ob was last used two items ago: its values have been read out
-          if (j == 0 && items_done >= 2 &&
-              !mbar_wait_warp(&bars->o_free[ob], ((items_done >> 1) - 1) & 1u, abort_flag, err)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv<D>(tO, desc_add(dp0, b * P_BYTES), desc_add(du0, s * Cfg::TILE), j > 0);
-          tc_commit_warp(&bars->o_full[b]);
-          tc_commit_warp(&bars->kv_empty[s]);        // K_j and U_j are consumed
         }
         if (!ok) break;
         tc_commit_warp(&bars->q_empty[qb]);          // every S of this item has read its Q
@@ -300,7 +298,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
     const int sub = warp & 3;
     const int r_row = sub * 32 + lane;                // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
-    uint8_t* prow = sP + hf * (BQ * 128) + (r_row >> 3) * 1024 + (r_row & 7) * 128;
     float2* sML = reinterpret_cast<float2*>(smem_raw + Cfg::OFF_ML);   // [2 halves][BQ rows]
     uint32_t gs = 0;
     uint32_t items_done = 0;
@@ -373,10 +370,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
             tmem_st_wait();
           }
         }
-        // P buffer b was last read by the P U of step g - 2 (for j < 2 that was the previous
-        // item, whose last P U was waited for before its output was read)
-        if (j >= 2 && !mbar_wait_warp(&bars->o_full[b], ((g - 2) >> 1) & 1u, abort_flag, err)) { ok = false; break; }
-        // pass 2: probabilities 2^(s*scale - m_run) as bf16 into this half's swizzle block
+        // pass 2: probabilities 2^(s*scale - m_run)
         const float neg_m = -m_run;
         float pv[64];
 #pragma unroll
@@ -391,18 +385,13 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
 #pragma unroll
         for (int i = 0; i < 64; ++i) ls[i & 7] += pv[i];
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        uint8_t* pdst = prow + b * P_BYTES;
+        // P(j) as bf16 pairs over the first 32 columns of this half (its scores are in registers)
+        uint32_t pk[32];
 #pragma unroll
-        for (int qd = 0; qd < 8; ++qd) {
-          uint4 wv;
-          wv.x = pack_bf16x2(pv[8 * qd + 0], pv[8 * qd + 1]);
-          wv.y = pack_bf16x2(pv[8 * qd + 2], pv[8 * qd + 3]);
-          wv.z = pack_bf16x2(pv[8 * qd + 4], pv[8 * qd + 5]);
-          wv.w = pack_bf16x2(pv[8 * qd + 6], pv[8 * qd + 7]);
-          *reinterpret_cast<uint4*>(pdst + ((qd ^ (r_row & 7)) << 4)) = wv;
-        }
-        fence_proxy_async_smem();               // P stores -> visible to the tensor core
-        tc_fence_before();                      // our TMEM reads of S are ordered before the next MMA
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
+        tmem_st_32x32b_x32(tS, pk);
+        tmem_st_wait();
+        tc_fence_before();                      // our TMEM reads of S and writes of P precede the next MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[b]);
       }
