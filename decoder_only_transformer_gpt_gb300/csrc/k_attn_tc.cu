@@ -320,10 +320,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const uint32_t tS = tmem_base + kColS + 128 * b + 64 * hf + lane_off;
         const bool diag = (j == w.n - 1);
         const int kb = j * BKV + 64 * hf;             // first key of this half
-        // this half's 64 scores, kept in registers for both passes
-        uint32_t va[32], vb[32];
-        tmem_ld_32x32b_x32(tS, va);
-        tmem_ld_32x32b_x32(tS + 32, vb);
+        // this half's 64 scores, kept in registers for both passes (one 64-column TMEM load)
+        uint32_t sv[64];
+        tmem_ld_32x32b_x64(tS, sv);
         tmem_ld_wait();
         // pass 1: maximum over this half's allowed keys, eight independent chains
         float mx8[8];
@@ -332,14 +331,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         if (diag) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float a = (kb + i <= t) ? __uint_as_float(va[i]) : -INFINITY;
-            const float bv = (kb + 32 + i <= t) ? __uint_as_float(vb[i]) : -INFINITY;
+            const float a = (kb + i <= t) ? __uint_as_float(sv[i]) : -INFINITY;
+            const float bv = (kb + 32 + i <= t) ? __uint_as_float(sv[32 + i]) : -INFINITY;
             mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(a, bv));
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(va[i]), __uint_as_float(vb[i])));
+            mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[32 + i])));
         }
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -375,7 +374,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         float pv[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const uint32_t raw = i < 32 ? va[i] : vb[i - 32];
+          const uint32_t raw = sv[i];
           const float e = ex2_approx(fmaf(__uint_as_float(raw), scale_log2, neg_m));
           pv[i] = (!diag || kb + i <= t) ? e : 0.0f;
         }

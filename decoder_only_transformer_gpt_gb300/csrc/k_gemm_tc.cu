@@ -77,8 +77,7 @@ __device__ __forceinline__ float gelu_f(float x, int erf_form) {
 // ---------------------------------------------------------------- epilogues
 
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32], int grow,
-                                               int n0) {
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t* r, int grow, int n0) {
   const bool full = (n0 + 32 <= a.N);
   float v[32];
 #pragma unroll
@@ -150,8 +149,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
 // Cross-entropy epilogue for one 32-column chunk: fold the chunk into the
 // row's running (max m, sum s of exp(z - m)) for this tile, capture the
 // target's logit, and store logits if asked.
-__device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t (&r)[32], int grow, int n0,
-                                         int tgt, float& m, float& s) {
+__device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, int grow, int n0, int tgt,
+                                         float& m, float& s) {
   float z[32];
   float cm = -INFINITY;
 #pragma unroll
@@ -202,15 +201,11 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const uint32_t
 // CW == 64, fp32 bits when CW == 32. sbias: the chunk's bias in shared memory
 // (zeros past N), or nullptr.
 template <int EPI, int CW>
-__device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t (&r0)[32], const uint32_t (&r1)[32],
-                                             const float* sbias, uint32_t (&w)[32]) {
+__device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t* r, const float* sbias,
+                                             uint32_t (&w)[32]) {
   float v[CW];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r0[i]);
-  if (CW == 64) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[(32 + i) % CW] = __uint_as_float(r1[i]);
-  }
+  for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
   if (sbias != nullptr) {
     const float4* b4 = reinterpret_cast<const float4*>(sbias);     // same address in every lane: broadcast
 #pragma unroll
@@ -381,21 +376,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int grow = mb * BM + row;
       const bool row_ok = grow < args.M;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      // the accumulator is read 64 columns per tcgen05.ld (see tmem_ld_32x32b_x64)
       if (EPI == EPI_CE) {
         const int tgt = row_ok ? __ldg(args.targets + grow) : -1;
         float m = -INFINITY, s = 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
+        for (int c2 = 0; c2 < BN / 64; ++c2) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x64(tbase + c2 * 64, r);
           tmem_ld_wait();
-          if (c == BN / 32 - 1) {                     // accumulator fully read: hand it back early
+          if (c2 == BN / 64 - 1) {                    // accumulator fully read: hand it back early
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[acc]);
           }
-          const int n0 = nb * BN + c * 32;
-          if (row_ok && n0 < args.N) ce_chunk(args, r, grow, n0, tgt, m, s);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int n0 = nb * BN + c2 * 64 + h * 32;
+            if (row_ok && n0 < args.N) ce_chunk(args, r + h * 32, grow, n0, tgt, m, s);
+          }
         }
         if (row_ok) {
           args.pmax[(size_t)nb * args.M + grow] = m;
@@ -405,46 +404,52 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         constexpr int CW = (EPI == EPI_BIAS_RESID) ? 32 : 64;    // columns per 128-byte staged row
         const int m0 = mb * BM + sub * 32;
 #pragma unroll 1
-        for (int c = 0; c < BN / CW; ++c) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(tbase + c * CW, r0);
-          if (CW == 64) tmem_ld_32x32b_x32(tbase + c * CW + 32, r1);
+        for (int c2 = 0; c2 < BN / 64; ++c2) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x64(tbase + c2 * 64, r);
           tmem_ld_wait();
-          if (c == BN / CW - 1) {
+          if (c2 == BN / 64 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[acc]);
           }
-          const int n0 = nb * BN + c * CW;
-          if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
-          uint32_t w[32];
-          finish_chunk<EPI, CW>(args, r0, r1, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
-          uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
-          ++n_staged;
-          if (lane == 0) bulk_wait_read<EPI_NBUF - 1>();   // the store that last used this box has read it
-          __syncwarp();
-          stage_row(buf, lane, w);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (EPI == EPI_BIAS_RESID) tma_reduce_add_2d(&tmC, buf, n0, m0);   // x += tile, in L2
-            else tma_store_2d(&tmC, buf, n0, m0);
-            bulk_commit();
+#pragma unroll
+          for (int h = 0; h < 64 / CW; ++h) {
+            const int c = c2 * (64 / CW) + h;            // chunk of CW columns within the tile
+            const int n0 = nb * BN + c * CW;
+            if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
+            uint32_t w[32];
+            finish_chunk<EPI, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
+            uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
+            ++n_staged;
+            if (lane == 0) bulk_wait_read<EPI_NBUF - 1>();   // the store that last used this box has read it
+            __syncwarp();
+            stage_row(buf, lane, w);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (EPI == EPI_BIAS_RESID) tma_reduce_add_2d(&tmC, buf, n0, m0);   // x += tile, in L2
+              else tma_store_2d(&tmC, buf, n0, m0);
+              bulk_commit();
+            }
           }
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
+        for (int c2 = 0; c2 < BN / 64; ++c2) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x64(tbase + c2 * 64, r);
           tmem_ld_wait();
-          if (c == BN / 32 - 1) {
+          if (c2 == BN / 64 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[acc]);
           }
-          const int n0 = nb * BN + c * 32;
-          if (row_ok && n0 < args.N) epilogue_chunk<EPI>(args, r, grow, n0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int n0 = nb * BN + c2 * 64 + h * 32;
+            if (row_ok && n0 < args.N) epilogue_chunk<EPI>(args, r + h * 32, grow, n0);
+          }
         }
       }
       acc ^= 1;

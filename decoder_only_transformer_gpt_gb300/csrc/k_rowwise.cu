@@ -208,6 +208,7 @@ cudaError_t ln_dispatch(const float* x, const float* g, const float* b, OT* out,
 // block also writes the sum of its rows' nll for the mean (fixed order).
 constexpr int kCeRows = 32;
 constexpr int kCeWarps = 8;
+constexpr int kCeGroup = 16;          // tiles per warp whose partials are loaded together
 
 __global__ void __launch_bounds__(kCeRows * kCeWarps)
 ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum,
@@ -222,14 +223,26 @@ ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum
   const int m = blockIdx.x * kCeRows + lane;
   float mx = -INFINITY, s = 0.0f;
   if (m < M) {
-    for (int t = warp; t < NB; t += kCeWarps) {
-      const float pm = __ldg(pmax + (size_t)t * M + m);
-      const float ps = __ldg(psum + (size_t)t * M + m);
-      if (pm > mx) {
-        s = s * expf(mx - pm) + ps;              // mx = -inf on the first tile: scale 0
-        mx = pm;
-      } else {
-        s += ps * expf(pm - mx);
+    // this warp's tiles t = warp, warp + 8, ...: kCeGroup of them loaded at once,
+    // then folded into the running (max, sum) with one rescale per group
+    for (int t0 = warp; t0 < NB; t0 += kCeGroup * kCeWarps) {
+      float pm[kCeGroup], ps[kCeGroup];
+#pragma unroll
+      for (int k = 0; k < kCeGroup; ++k) {
+        const int t = t0 + k * kCeWarps;
+        pm[k] = t < NB ? __ldg(pmax + (size_t)t * M + m) : -INFINITY;
+        ps[k] = t < NB ? __ldg(psum + (size_t)t * M + m) : 0.0f;
+      }
+      float gm = mx;
+#pragma unroll
+      for (int k = 0; k < kCeGroup; ++k) gm = fmaxf(gm, pm[k]);
+      if (gm != -INFINITY) {
+        float acc = (mx == -INFINITY) ? 0.0f : s * expf(mx - gm);
+#pragma unroll
+        for (int k = 0; k < kCeGroup; ++k)
+          if (pm[k] != -INFINITY) acc += ps[k] * expf(pm[k] - gm);
+        s = acc;
+        mx = gm;
       }
     }
   }
@@ -261,21 +274,25 @@ ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum
   }
 }
 
-// loss = (sum of the partial sums) / M in a fixed order: each thread sums a
-// strided slice in fp64, then a shared-memory tree in fp64. One block.
-__global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ part, int n, int M, float* loss) {
-  __shared__ double red[1024];
+// loss = (sum of the partial sums) / M in a fixed order: each lane of one warp
+// sums a strided slice in fp64 (four loads in flight), then a shuffle tree in fp64.
+__global__ void __launch_bounds__(32) mean_kernel(const float* __restrict__ part, int n, int M, float* loss) {
   pdl_wait();
   pdl_trigger();
+  const int lane = threadIdx.x;
   double s = 0.0;
-  for (int i = threadIdx.x; i < n; i += 1024) s += static_cast<double>(part[i]);
-  red[threadIdx.x] = s;
-  __syncthreads();
-  for (int w = 512; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
+  int i = lane;
+  for (; i + 96 < n; i += 128) {
+    const float a = part[i], b = part[i + 32], c = part[i + 64], d = part[i + 96];
+    s += static_cast<double>(a);
+    s += static_cast<double>(b);
+    s += static_cast<double>(c);
+    s += static_cast<double>(d);
   }
-  if (threadIdx.x == 0) *loss = static_cast<float>(red[0] / static_cast<double>(M));
+  for (; i < n; i += 32) s += static_cast<double>(part[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) *loss = static_cast<float>(s / static_cast<double>(M));
 }
 
 }  // namespace
@@ -316,7 +333,7 @@ int ce_combine_blocks(int M) { return (M + kCeRows - 1) / kCeRows; }
 
 cudaError_t launch_mean(const float* part, int n, int M, float* loss, cudaStream_t s) {
   if (M <= 0 || n <= 0) return cudaSuccess;
-  return launch_k(mean_kernel, dim3(1), dim3(1024), 0, s, part, n, M, loss);
+  return launch_k(mean_kernel, dim3(1), dim3(32), 0, s, part, n, M, loss);
 }
 
 }  // namespace gptgb
