@@ -333,15 +333,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
           for (int i = 0; i < 32; ++i) {
             const float a = (kb + i <= t) ? __uint_as_float(sv[i]) : -INFINITY;
             const float bv = (kb + 32 + i <= t) ? __uint_as_float(sv[32 + i]) : -INFINITY;
-            mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(a, bv));
+            mx8[i & 7] = fmax3(mx8[i & 7], a, bv);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[32 + i])));
+            mx8[i & 7] = fmax3(mx8[i & 7], __uint_as_float(sv[i]), __uint_as_float(sv[32 + i]));
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         // a fully masked half (all its keys after t) leaves mx = -inf: nothing to raise
         const float m_new = fmaxf(m_run, mx * scale_log2);
         const bool need = m_new > m_run + kRescaleLog2;

@@ -68,10 +68,16 @@ __device__ __forceinline__ void tile_coords(int tile, int MB, int NB, int m_fast
 }
 
 
+// GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated as
+// u = x (c0 + c1 x^2), h = x / 2, h + h tanh(u): five ALU instructions and one
+// tanh (the ALU count matters: it runs beside the tensor core's main loop).
 __device__ __forceinline__ float gelu_f(float x, int erf_form) {
   if (erf_form) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
-  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.0f + tanh_approx(u));
+  constexpr float c0 = 0.7978845608028654f;             // sqrt(2/pi)
+  constexpr float c1 = 0.7978845608028654f * 0.044715f;
+  const float u = x * fmaf(x * x, c1, c0);
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_approx(u), h);
 }
 
 // ---------------------------------------------------------------- epilogues
@@ -152,12 +158,14 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
 __device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, int grow, int n0, int tgt,
                                          float& m, float& s) {
   float z[32];
-  float cm = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
-    cm = fmaxf(cm, z[i]);
-  }
+  for (int i = 0; i < 32; ++i) z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
+  float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c4[k] = fmax3(c4[k], z[i + 2 * k], z[i + 2 * k + 1]);
+  const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
   if (cm != -INFINITY) {
     const float nm = fmaxf(m, cm);
     const float nml = nm * kLog2e;
