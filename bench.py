@@ -49,14 +49,14 @@ STEP_KINDS = [("embed", 0, False), ("c_attn", 1, True), ("attention", 2, True), 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the same
 # launch configuration, valid only while the kernel's sources hash to the digest recorded with it.
 NCU_TRAFFIC = {
-    "attention": {"bytes": 76.324608e6 + 6.569472e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
+    "attention": {"bytes": 75.940864e6 + 6.589184e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                  "digest": "8c31ccb209d8b5c5d1df6f69fb2bcaa646363b12"},
-    "head": {"bytes": 102.534656e6 + 18.057728e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+                  "digest": "1c1aff9e9f550641087cf6825bbe918751ada5ea"},
+    "head": {"bytes": 102.54848e6 + 17.579776e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "83834d9049d502883ec01d1e1aa2b3039e73f6d3"},
+             "digest": "93867db28a7d1e43baf70de122f9c90028bc21af"},
 }
 
 
