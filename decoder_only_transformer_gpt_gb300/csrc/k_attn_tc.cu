@@ -14,27 +14,29 @@
 // A work item is one (b, h) and one 128-row query tile; the kernel is
 // persistent (one CTA per SM walks its items, heaviest first, snake-dealt) and
 // keeps its barriers, TMEM and K/U ring across items. Inside an item the score
-// tiles are double-buffered so the tensor core and the softmax overlap:
-//   S(j)  = Q K_j^T   tcgen05.mma M=128 N=128 K=D  -> TMEM S[j % 2] (128 columns each)
-//   O_h  += P(j)_h U_j[64h:64h+64]                 -> TMEM O[item % 2]_h (h = 0, 1)
+// tiles are triple-buffered so the tensor core and the softmax overlap:
+//   S(j)  = Q K_j^T   tcgen05.mma M=128 N=128 K=D  -> TMEM S[j % 3] (128 columns each)
+//   O_h  += P(j)_h U_j[64h:64h+64]                 -> TMEM O_h (h = 0, 1)
 // The softmax reads its 64 scores of S(j) into registers and writes P(j) back
 // as bf16 pairs over the first 32 columns of the same 64 (row = lane), so the
 // P U MMA takes its A operand straight from tensor memory: probabilities never
 // pass through shared memory. While the softmax turns S(j) into P(j), the
-// tensor core already holds S(j+1); once P(j) is handed over it runs P(j) U_j
-// and then S(j+2) into the same buffer (one thread's MMAs execute in issue
-// order, so S(j+2) overwrites P(j) only after P(j) U_j has read it). The output
-// accumulators and the query tile are double-buffered across items, so an
-// item's first score tile and first P U never wait for the previous item's
-// output or for its own Q load. U_j is consumed MN-major straight from its TMA
-// tile. Two softmax threads share each query row (= TMEM lane): one owns keys
-// [0, 64) of every key tile, the other keys [64, 128), each with its own
-// running max, running sum and TMEM output accumulator. The running max is
-// raised lazily: a half's O and sum are rescaled only when its max grows by
-// more than 2^8. At the end of an item both threads of a row exchange their
-// (max, sum) and each writes half of the row's D output columns.
+// tensor core already holds S(j+1) and S(j+2); once P(j) is handed over it runs
+// P(j) U_j and then S(j+3) into the same buffer (one thread's MMAs execute in
+// issue order, so S(j+3) overwrites P(j) only after P(j) U_j has read it), which
+// leaves two softmax steps for that chain. The query tile is double-buffered
+// across items, so an item's first score tiles never wait for its Q load; the
+// next item's first P U waits only for the previous item's output to be read,
+// which the same softmax warps do before they produce that P. U_j is consumed
+// MN-major straight from its TMA tile. Two softmax threads share each query row
+// (= TMEM lane): one owns keys [0, 64) of every key tile, the other keys
+// [64, 128), each with its own running max, running sum and TMEM output
+// accumulator. The running max is raised lazily: a half's O and sum are
+// rescaled only when its max grows by more than 2^8. At the end of an item both
+// threads of a row exchange their (max, sum) and each writes half of the row's
+// D output columns.
 // Warp roles (320 threads, one persistent CTA per SM):
-//   warp 0      TMA producer: Q once per item (two buffers), then K_j, U_j into a four-stage ring
+//   warp 0      TMA producer: Q once per item (two buffers), then K_j, U_j into a five-stage ring
 //   warp 1      TMEM allocator (512 columns) and MMA issuer (the whole warp runs
 //               the loop, one elected lane issues)
 //   warps 2-5   softmax, keys [0, 64) of each tile; warps 6-9 keys [64, 128)
@@ -54,10 +56,11 @@ constexpr int THREADS = 320;
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by more than this
-constexpr int NS = 4;                   // K/U ring depth (key tiles in flight)
+constexpr int NS = 5;                   // K/U ring depth (key tiles in flight)
+constexpr uint32_t NSB = 3;             // score buffers: S(j+3) is issued while the softmax works on S(j+1)
 // TMEM columns
-constexpr uint32_t kColS = 0;           // S[0] at 0, S[1] at 128
-constexpr uint32_t kColO = 256;         // O[0] at 256, O[1] at 384; half h of O[k] at + 64 h
+constexpr uint32_t kColS = 0;           // S[k] at 128 k, k < NSB
+constexpr uint32_t kColO = 128 * NSB;   // O (half h at + 64 h): 384..511
 
 template <int D>
 struct AttnCfg {
@@ -80,10 +83,10 @@ struct __align__(8) AttnBars {
   uint64_t q_empty[2];      // every S of the item that used Q buffer k has been computed
   uint64_t kv_full[NS];
   uint64_t kv_empty[NS];
-  uint64_t s_full[2];       // S buffer b holds a new score tile
-  uint64_t p_full[2];       // P buffer b holds a tile's probabilities (8 softmax warps)
-  uint64_t o_full[2];       // the P U of a step with buffer b has completed
-  uint64_t o_free[2];       // output buffer k has been read out of TMEM (8 softmax warps)
+  uint64_t s_full[NSB];     // score buffer b holds a new score tile
+  uint64_t p_full[NSB];     // buffer b holds a tile's probabilities (8 softmax warps)
+  uint64_t o_full[NSB];     // the P U of a step with buffer b has completed
+  uint64_t o_free;          // the output accumulator has been read out of TMEM (8 softmax warps)
   uint64_t ml_full;         // both halves wrote their (max, sum) for the merge (8 softmax warps)
   uint64_t drain;
   uint32_t tmem_base;
@@ -176,13 +179,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (uint32_t i = 0; i < NSB; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 8);
       mbar_init(&bars->o_full[i], 1);
     }
-    mbar_init(&bars->o_free[0], 8);
-    mbar_init(&bars->o_free[1], 8);
+    mbar_init(&bars->o_free, 8);
     mbar_init(&bars->ml_full, 8);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -249,13 +251,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const int qb = r & 1;
         if (!mbar_wait_warp(&bars->q_full[qb], static_cast<uint32_t>(r >> 1) & 1u, abort_flag, err)) break;
         const uint64_t dq = desc_add(dq0, qb * Cfg::TILE);
-        const uint32_t ob = items_done & 1u;
-        const uint32_t tO = tmem_base + kColO + 128 * ob;
+        const uint32_t tO = tmem_base + kColO;
         // the first two score tiles (the softmax read both buffers' previous tiles before
         // handing over the previous item's last probabilities)
-        for (int jj = 0; jj < 2 && jj < w.n; ++jj) {
+        for (int jj = 0; jj < static_cast<int>(NSB) && jj < w.n; ++jj) {
           const uint32_t t = kv_it + jj;
-          const uint32_t b = (gs + jj) & 1u;
+          const uint32_t b = (gs + jj) % NSB;
           if (!mbar_wait_warp(&bars->kv_full[t % NS], (t / NS) & 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t % NS) * Cfg::TILE));
@@ -263,20 +264,20 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         }
         for (int j = 0; j < w.n && ok; ++j) {
           const uint32_t g = gs + j;
-          const uint32_t b = g & 1u;
+          const uint32_t b = g % NSB;
           const uint32_t s = (kv_it + j) % NS;
-          if (!mbar_wait_warp(&bars->p_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
-          // output buffer ob was last used two items ago: its values have been read out
-          if (j == 0 && items_done >= 2 &&
-              !mbar_wait_warp(&bars->o_free[ob], ((items_done >> 1) - 1) & 1u, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait_warp(&bars->p_full[b], (g / NSB) & 1u, abort_flag, err)) { ok = false; break; }
+          // the previous item's output has been read out of the accumulator
+          if (j == 0 && items_done >= 1 &&
+              !mbar_wait_warp(&bars->o_free, (items_done - 1) & 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           issue_pv<D>(tO, tmem_base + kColS + 128 * b, desc_add(du0, s * Cfg::TILE), j > 0);
           tc_commit_warp(&bars->o_full[b]);
           tc_commit_warp(&bars->kv_empty[s]);        // K_j and U_j are consumed
           // the score tile after next into buffer b: issued after P(j) U_j, which reads
           // P(j) out of the same columns (one thread's MMAs run in issue order)
-          if (j + 2 < w.n) {
-            const uint32_t t2 = kv_it + j + 2;
+          if (j + static_cast<int>(NSB) < w.n) {
+            const uint32_t t2 = kv_it + j + NSB;
             if (!mbar_wait_warp(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t2 % NS) * Cfg::TILE));
@@ -307,15 +308,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
       if (item >= n_items) break;
       const Item w = decode_item(item, BH, H, n_qtiles);
       const int t = w.qt * BQ + r_row;                // query position
-      const uint32_t ob = items_done & 1u;
-      const uint32_t tO0 = tmem_base + kColO + 128 * ob + lane_off;   // O of keys [0, 64)
+      const uint32_t tO0 = tmem_base + kColO + lane_off;              // O of keys [0, 64)
       const uint32_t tO = tO0 + 64 * hf;                                // this half's O
       float m_run = -INFINITY;                        // running (lazily raised) max, log2 units
       float l = 0.0f;                                 // running sum of 2^(s - m_run) over this half
       for (int j = 0; j < w.n; ++j) {
         const uint32_t g = gs + j;
-        const uint32_t b = g & 1u;
-        if (!mbar_wait_warp(&bars->s_full[b], (g >> 1) & 1u, abort_flag, err)) { ok = false; break; }
+        const uint32_t b = g % NSB;
+        if (!mbar_wait_warp(&bars->s_full[b], (g / NSB) & 1u, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tS = tmem_base + kColS + 128 * b + 64 * hf + lane_off;
         const bool diag = (j == w.n - 1);
@@ -346,7 +346,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const bool need = m_new > m_run + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
           if (j > 0) {                                // this half's O must hold all earlier P U
-            if (!mbar_wait_warp(&bars->o_full[(g - 1) & 1u], ((g - 1) >> 1) & 1u, abort_flag, err)) {
+            if (!mbar_wait_warp(&bars->o_full[(g - 1) % NSB], ((g - 1) / NSB) & 1u, abort_flag, err)) {
               ok = false;
               break;
             }
@@ -396,7 +396,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
       if (!ok) break;
       // the item's output: both threads of a row exchange (max, sum); each writes D/2 columns
       const uint32_t glast = gs + w.n - 1;
-      if (!mbar_wait_warp(&bars->o_full[glast & 1u], (glast >> 1) & 1u, abort_flag, err)) break;
+      if (!mbar_wait_warp(&bars->o_full[glast % NSB], (glast / NSB) & 1u, abort_flag, err)) break;
       tc_fence_after();
       sML[hf * BQ + r_row] = make_float2(m_run, l);
       __syncwarp();
@@ -421,9 +421,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         tmem_ld_32x32b_x16(tO0 + 64 + c0, v1);
       }
       tmem_ld_wait();
-      tc_fence_before();                             // output buffer ob may be overwritten after this
+      tc_fence_before();                             // the accumulator may be overwritten after this
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_free[ob]);
+      if (lane == 0) mbar_arrive(&bars->o_free);
       if (t < T) {
         uint4* dst = reinterpret_cast<uint4*>(y + ((size_t)w.b * T + t) * C + w.h * D + c0);
 #pragma unroll
