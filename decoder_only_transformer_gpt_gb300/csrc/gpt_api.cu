@@ -227,11 +227,13 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
   Carve ws;
   const size_t o_x = ws.take(Mx * C * 4), o_a = ws.take(Mx * C * es), o_qkv = ws.take(Mx * 3 * C * es),
                o_y = ws.take(Mx * C * es), o_g = ws.take(Mx * F * es);
-  size_t o_pmax = 0, o_psum = 0, o_ztgt = 0, o_logits = 0;
+  size_t o_pmax = 0, o_psum = 0, o_ztgt = 0, o_logits = 0, o_skp = 0, o_skf = 0;
   if (m->bf16) {
     o_pmax = ws.take(NB * Mx * 4);
     o_psum = ws.take(NB * Mx * 4);
     o_ztgt = ws.take(Mx * 4);
+    o_skp = ws.take(gemm_sk_part_floats(m->num_sms) * 4);
+    o_skf = ws.take(gemm_sk_flag_ints(m->num_sms) * 4);
   } else {
     o_logits = ws.take(Mx * V * 4);
   }
@@ -248,6 +250,12 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
     m->pmax = reinterpret_cast<float*>(m->ws + o_pmax);
     m->psum = reinterpret_cast<float*>(m->ws + o_psum);
     m->ztgt = reinterpret_cast<float*>(m->ws + o_ztgt);
+    m->sk_part = reinterpret_cast<float*>(m->ws + o_skp);
+    m->sk_flag = reinterpret_cast<int*>(m->ws + o_skf);
+    if (cudaMemset(m->sk_flag, 0, gemm_sk_flag_ints(m->num_sms) * 4) != cudaSuccess) {
+      free_model(m);
+      return GPT_ECUDA;
+    }
   } else {
     m->logits_ws = reinterpret_cast<float*>(m->ws + o_logits);
   }

@@ -75,6 +75,8 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   a.gelu_erf = m->cfg.gelu;
   a.err = m->err;
   a.m_fastest = (N > M) ? 1 : 0;        // keep the larger operand's tiles shared by co-running CTAs
+  a.sk_part = m->sk_part;               // used where whole tiles would leave the last wave part-idle
+  a.sk_flag = m->sk_flag;
   GPT_CUDA(launch_gemm_tc(tmA, tmB, tmC, a, epi, m->num_sms, s));
   return GPT_OK;
 }
@@ -276,6 +278,11 @@ int gpt_status(gpt_model* m, void* stream) {
   GPT_CUDA(cudaMemcpyAsync(m->h_pinned, m->err, sizeof(int), cudaMemcpyDeviceToHost, s));
   GPT_CUDA(cudaMemsetAsync(m->err, 0, sizeof(int), s));
   GPT_CUDA(cudaStreamSynchronize(s));
+  if (m->h_pinned[0] != 0 && m->sk_flag != nullptr) {
+    // a launch that gave up may have left stream-K flags set
+    GPT_CUDA(cudaMemsetAsync(m->sk_flag, 0, gemm_sk_flag_ints(m->num_sms) * sizeof(int), s));
+    GPT_CUDA(cudaStreamSynchronize(s));
+  }
   return map_device_error(m->h_pinned[0]);
 }
 

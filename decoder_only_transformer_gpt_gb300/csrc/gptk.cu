@@ -67,7 +67,27 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
   a.bias = bias; a.out = out; a.ldo = N;
   a.err = err;
   a.m_fastest = N > M ? 1 : 0;
-  GPT_CUDA(launch_gemm_tc(tmA, tmB, tmC, a, epilogue, num_sms(), s));
+  const int grid = num_sms();
+  uint8_t* skws = nullptr;                 // stream-K partial tiles + flags, on the stream
+  if (gemm_tc_stream_k(M, N, K, epilogue, grid)) {
+    const size_t pbytes = gemm_sk_part_floats(grid) * sizeof(float);
+    const size_t fbytes = gemm_sk_flag_ints(grid) * sizeof(int);
+    GPT_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&skws), pbytes + fbytes, s));
+    a.sk_part = reinterpret_cast<float*>(skws);
+    a.sk_flag = reinterpret_cast<int*>(skws + pbytes);
+    const cudaError_t e = cudaMemsetAsync(a.sk_flag, 0, fbytes, s);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(skws, s);
+      set_detail("cudaMemsetAsync", e);
+      return GPT_ECUDA;
+    }
+  }
+  const cudaError_t e = launch_gemm_tc(tmA, tmB, tmC, a, epilogue, grid, s);
+  if (skws) cudaFreeAsync(skws, s);
+  if (e != cudaSuccess) {
+    set_detail("launch_gemm_tc", e);
+    return GPT_ECUDA;
+  }
   return GPT_OK;
 }
 

@@ -235,9 +235,62 @@ __device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t* 
   }
 }
 
+// ---------------------------------------------------------------- work list
+
+// A CTA's work as a sequence of segments (tile, K blocks [kb0, kb1)).
+//
+// Whole tiles: tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//
+// Stream-K (tiles not a whole number of waves): the first S tiles, S = one wave
+// plus the remainder, form a region whose tiles x KB (tile, K block) units are
+// dealt in equal contiguous shares, one per CTA; each share is at least KB units,
+// so a tile is split between at most two CTAs: the one holding its first K blocks
+// (a prefix: the CTA's last segment of the region) and the next CTA (a suffix:
+// its first segment). The remaining tiles are whole waves, dealt as above. The
+// region comes first so that a split tile's fixup overlaps later whole tiles, and
+// it is a small contiguous range of tiles so that co-running CTAs share operands
+// in L2.
+struct SegIter {
+  int KB;
+  long long k, kend;          // stream-K units still to deal
+  int t, stride, count;       // whole tiles still to deal
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
+    if (k < kend) {
+      tile = static_cast<int>(k / KB);
+      kb0 = static_cast<int>(k - static_cast<long long>(tile) * KB);
+      const long long left = kend - k;
+      kb1 = (KB - kb0 < left) ? KB : kb0 + static_cast<int>(left);
+      k += kb1 - kb0;
+      return true;
+    }
+    if (t >= count) return false;
+    tile = t;
+    kb0 = 0;
+    kb1 = KB;
+    t += stride;
+    return true;
+  }
+};
+
+__device__ __forceinline__ SegIter make_seg_iter(bool sk, int num_tiles, int KB) {
+  const int G = gridDim.x;
+  const int S = !sk ? 0 : (num_tiles >= 2 * G ? G + num_tiles % G : num_tiles);
+  SegIter it;
+  it.KB = KB;
+  const long long units = static_cast<long long>(S) * KB;
+  it.k = units * blockIdx.x / G;
+  it.kend = units * (blockIdx.x + 1) / G;
+  it.t = S + blockIdx.x;
+  it.stride = G;
+  it.count = num_tiles;
+  return it;
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <int EPI>
+// SK: whether the launch splits tiles (stream-K). Whole-tile launches use their
+// own instantiation, whose loops have no segment bookkeeping.
+template <int EPI, bool SK>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -259,6 +312,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int NB = (args.N + BN - 1) / BN;
   const int KB = (args.K + BK - 1) / BK;
   const int num_tiles = MB * NB;
+  constexpr bool sk = SK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&bars->full[s], 1); mbar_init(&bars->empty[s], 1); }
@@ -290,20 +344,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // The weights (B) do not depend on the previous kernel: the first tile's
       // first stages of B are requested before waiting for that kernel to finish.
       int pre = 0;
-      if (static_cast<int>(blockIdx.x) < num_tiles) {
-        int mb0, nb0;
-        tile_coords(blockIdx.x, MB, NB, args.m_fastest, mb0, nb0);
-        pre = KB < STAGES ? KB : STAGES;
-        for (int kb = 0; kb < pre; ++kb) {
-          mbar_arrive_expect_tx(&bars->full[kb], STAGE_BYTES);
-          tma_load_2d(sB + kb * B_BYTES, &tmB, &bars->full[kb], kb * BK, nb0 * BN);
+      SegIter it = make_seg_iter(sk, num_tiles, KB);
+      {
+        SegIter it0 = it;
+        int tile0, kb00, kb10;
+        if (it0.next(tile0, kb00, kb10)) {
+          int mb0, nb0;
+          tile_coords(tile0, MB, NB, args.m_fastest, mb0, nb0);
+          pre = (kb10 - kb00) < STAGES ? (kb10 - kb00) : STAGES;
+          for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(&bars->full[i], STAGE_BYTES);
+            tma_load_2d(sB + i * B_BYTES, &tmB, &bars->full[i], (kb00 + i) * BK, nb0 * BN);
+          }
         }
       }
       pdl_wait();                     // A, written by the previous kernel, is now visible
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         int mb, nb;
         tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (pre > 0) {                // stage armed and its B requested above
             --pre;
             tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
@@ -335,18 +395,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      SegIter it = make_seg_iter(sk, num_tiles, KB);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         if (!mbar_wait_warp(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_warp(&bars->full[stage], phase, abort_flag, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = da0 + static_cast<uint64_t>((stage * A_BYTES) >> 4);
           const uint64_t db = db0 + static_cast<uint64_t>((stage * B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_bf16_warp(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_bf16_warp(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           tc_commit_warp(&bars->empty[stage]);           // frees the stage once these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -368,10 +430,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     pdl_wait();                                      // outputs may be read-modified-written below
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    SegIter it = make_seg_iter(sk, num_tiles, KB);
+    int tile, kb0, kb1;
+    while (it.next(tile, kb0, kb1)) {
       int mb, nb;
       tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
-      if (kTmaOut && args.bias != nullptr) {
+      // stream-K: a suffix (kb0 > 0) hands its fp32 partial to the CTA before, in
+      // slot blockIdx.x; a prefix (kb1 < KB) takes the next CTA's from slot blockIdx.x + 1
+      const bool writer = kb0 > 0;
+      const bool owner = kb0 == 0 && kb1 < KB;
+      if (kTmaOut && args.bias != nullptr && !writer) {
         // this tile's BN bias values into the warp's shared copy, while the main loop runs
         const int nbase = nb * BN + lane * (BN / 32);
 #pragma unroll
@@ -384,6 +452,51 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int grow = mb * BM + row;
       const bool row_ok = grow < args.M;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (SK && kTmaOut && writer) {
+        // this warp's 32 rows of the partial tile, then its flag. Layout of a slot:
+        // [warp][64-column chunk][float4 q][lane], so that each store (and the
+        // owner's matching load) covers 512 contiguous bytes
+        float4* pw = reinterpret_cast<float4*>(args.sk_part) + ((size_t)blockIdx.x * 4 + sub) * (BN / 64) * 16 * 32 + lane;
+#pragma unroll 1
+        for (int c2 = 0; c2 < BN / 64; ++c2) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x64(tbase + c2 * 64, r);
+          tmem_ld_wait();
+          if (c2 == BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+          }
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            pw[(c2 * 16 + q) * 32] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                                 __uint_as_float(r[4 * q + 3]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(args.sk_flag + blockIdx.x * 4 + sub, 1);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
+      const float4* ppart = nullptr;                  // owner: the other CTA's partial rows
+      if (SK && kTmaOut && owner) {
+        // wait (bounded) for the writer's flag, then clear it for the next launch
+        int* flag = args.sk_flag + (blockIdx.x + 1) * 4 + sub;
+        bool seen = ld_acquire_gpu(flag) != 0;
+        if (!seen) {
+          const long long t0 = clock64();
+          while (!(seen = (ld_acquire_gpu(flag) != 0))) {
+            if (*abort_flag || clock64() - t0 > kWaitLimitCycles) break;
+          }
+        }
+        if (!__all_sync(0xffffffffu, seen)) {
+          if (lane == 0) { record_error(args.err, GPT_DEV_ETIMEOUT); *abort_flag = 1; }
+        } else if (lane == 0) {
+          *flag = 0;
+        }
+        ppart = reinterpret_cast<const float4*>(args.sk_part) + ((size_t)(blockIdx.x + 1) * 4 + sub) * (BN / 64) * 16 * 32 + lane;
+      }
       // the accumulator is read 64 columns per tcgen05.ld (see tmem_ld_32x32b_x64)
       if (EPI == EPI_CE) {
         const int tgt = row_ok ? __ldg(args.targets + grow) : -1;
@@ -420,6 +533,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+          }
+          if (SK && ppart != nullptr) {               // finish a split tile: + the suffix's K blocks
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float4 p4 = ppart[(c2 * 16 + q) * 32];
+              r[4 * q + 0] = __float_as_uint(__uint_as_float(r[4 * q + 0]) + p4.x);
+              r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + p4.y);
+              r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + p4.z);
+              r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + p4.w);
+            }
           }
 #pragma unroll
           for (int h = 0; h < 64 / CW; ++h) {
@@ -475,27 +598,49 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <int EPI>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
-                       int grid_limit, cudaStream_t s) {
+template <int EPI, bool SK>
+cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                        int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, SK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<EPI>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  return launch_k(gemm_tc_kernel<EPI, SK>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
+}
+
+template <int EPI>
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                       int grid_limit, cudaStream_t s) {
   const int MB = (a.M + BM - 1) / BM;
   const int NB = (a.N + BN - 1) / BN;
   const int tiles = MB * NB;
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
-  return launch_k(gemm_tc_kernel<EPI>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
+  constexpr bool kSplit = EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID;
+  if (kSplit && a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
+    return launch_inst<EPI, kSplit>(tmA, tmB, tmC, a, grid, s);
+  return launch_inst<EPI, false>(tmA, tmB, tmC, a, grid, s);
 }
 
 }  // namespace
 
 int gemm_tc_bn() { return BN; }
+
+// Stream-K only where whole tiles would leave a partly idle last wave, and only
+// for long K (at least kSplitMinKB K blocks): with shorter tiles the idle part of
+// the last wave is smaller than the cost of splitting (measured on GB300).
+constexpr int kSplitMinKB = 24;
+bool gemm_tc_stream_k(int M, int N, int K, int epi, int grid_limit) {
+  if (epi != EPI_BIAS_OUT && epi != EPI_BIAS_GELU_OUT && epi != EPI_BIAS_RESID) return false;
+  const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int KB = (K + BK - 1) / BK;
+  return KB >= kSplitMinKB && grid_limit > 0 && tiles > grid_limit && tiles % grid_limit != 0;
+}
+size_t gemm_sk_part_floats(int grid) { return static_cast<size_t>(grid + 1) * BM * BN; }
+size_t gemm_sk_flag_ints(int grid) { return static_cast<size_t>(grid + 1) * 4; }
 int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,

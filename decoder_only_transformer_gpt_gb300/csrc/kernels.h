@@ -37,7 +37,17 @@ struct GemmArgs {
   float* logits;            // EPI_CE: [M, ldo] fp32 or nullptr
   int* err;                 // device error word
   int m_fastest;            // tile order: 1 = consecutive tiles walk M
+  // Stream-K (EPI_BIAS_OUT, EPI_BIAS_GELU_OUT, EPI_BIAS_RESID): each CTA takes an equal
+  // range of (tile, K block) units; a tile split between two CTAs is finished by the
+  // CTA holding its first K blocks after adding the other's fp32 partial.
+  float* sk_part;           // [grid + 1][BM x 256] fp32 partial tiles, or nullptr: whole tiles per CTA
+  int* sk_flag;             // [grid + 1][4] per-warp "partial written" flags, zero between launches
 };
+// Floats of stream-K partial workspace for a grid of `grid` CTAs, and ints of flags.
+size_t gemm_sk_part_floats(int grid);
+size_t gemm_sk_flag_ints(int grid);
+// Whether launch_gemm_tc splits tiles across CTAs (given a workspace) for this shape.
+bool gemm_tc_stream_k(int M, int N, int K, int epi, int grid_limit);
 
 // ---- tensor-core (bf16) path
 constexpr int kGemmBM = 128;

@@ -38,6 +38,8 @@ struct gpt_model {
   float* nll = nullptr;     // [Mx]
   float* block_sums = nullptr;  // [ce_combine_blocks(Mx)] per-block sums of nll
   float* logits_ws = nullptr;   // fp32 path: [Mx, V]
+  float* sk_part = nullptr;     // bf16 path: stream-K partial tiles of the block projections
+  int* sk_flag = nullptr;       // and their flags (zero between launches)
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;

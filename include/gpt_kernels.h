@@ -32,7 +32,11 @@ enum {
  * out[M,N] = epilogue(A[M,K] . W[N,K]^T + bias[N]).
  * A and W are row-major in dtype (nn.Linear orientation, §25.5); bias fp32
  * [N] or NULL; out row-major with row stride N. K and N must be multiples of
- * 8 on the bf16 path (16-byte TMA row strides).
+ * 8 on the bf16 path (16-byte TMA row strides). Where the bf16 tiles would not
+ * fill whole waves of the GPU and K >= 1536, epilogues 0-2 split tiles along K
+ * between two CTAs (stream-K, fixed summation order: results do not depend on
+ * timing); their fp32 partial tiles and flags are allocated on the stream
+ * (stream-ordered allocator) and freed there after the launch.
  */
 int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_t M, int32_t N,
               int32_t K, int32_t epilogue, int32_t dtype, void* stream);

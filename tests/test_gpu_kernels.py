@@ -64,6 +64,31 @@ def test_gemm_tc_many_tiles_per_cta(gpt_lib, M, N, K):
     _gemm_case(gpt_lib, M, N, K, 0, seed=M)
 
 
+@pytest.mark.parametrize("M,N,K", [(6500, 768, 3072), (4000, 2304, 1544), (5000, 2304, 1536)])
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_gemm_tc_stream_k(gpt_lib, M, N, K, epi):
+    # more tiles than SMs, not a whole number of waves, K >= 1536: tiles are split
+    # along K between CTAs. With 152 SMs: 153 tiles (151 splits), 288 tiles with a
+    # ragged last K block, and 360 tiles (a 208-tile split region, then a whole wave).
+    _gemm_case(gpt_lib, M, N, K, epi, seed=K + epi)
+
+
+def test_gemm_tc_stream_k_deterministic(gpt_lib):
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(5)
+    M, N, K = 6500, 768, 3072
+    A = dev_bf16(rand_bf16(rng, (M, K)))
+    W = dev_bf16(rand_bf16(rng, (N, K), 0.5))
+    b = dev_f32(rng.standard_normal(N).astype(np.float32))
+    outs = []
+    for _ in range(3):
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        binding.gemm(A, W, b, out, binding.EPI_BIAS)
+        binding.status()
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
 def _attn_case(B, T, H, D, seed=0, qk_scale=1.5):
     from decoder_only_transformer_gpt_gb300 import binding
     rng = np.random.default_rng(seed)
