@@ -368,21 +368,24 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
             tmem_st_wait();
           }
         }
-        // pass 2: probabilities 2^(s*scale - m_run)
-        const float neg_m = -m_run;
+        // pass 2: probabilities 2^(s*scale - m_run), two keys per f32x2 instruction
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
         float pv[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint32_t raw = sv[i];
-          const float e = ex2_approx(fmaf(__uint_as_float(raw), scale_log2, neg_m));
-          pv[i] = (!diag || kb + i <= t) ? e : 0.0f;
+        for (int i = 0; i < 64; i += 2) {
+          const float2 x = fma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
+          const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
+          pv[i] = (!diag || kb + i <= t) ? e0 : 0.0f;
+          pv[i + 1] = (!diag || kb + i + 1 <= t) ? e1 : 0.0f;
         }
-        float ls[8];
+        float2 ls[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ls[k] = 0.0f;
+        for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) ls[i & 7] += pv[i];
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        for (int i = 0; i < 64; i += 2) ls[(i >> 1) & 3] = add2_rn(ls[(i >> 1) & 3], make_float2(pv[i], pv[i + 1]));
+        const float2 l2 = add2_rn(add2_rn(ls[0], ls[1]), add2_rn(ls[2], ls[3]));
+        l += l2.x + l2.y;
         // P(j) as bf16 pairs over the first 32 columns of this half (its scores are in registers)
         uint32_t pk[32];
 #pragma unroll
