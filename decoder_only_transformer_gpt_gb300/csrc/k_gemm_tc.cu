@@ -158,8 +158,13 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
 __device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, int grow, int n0, int tgt,
                                          float& m, float& s) {
   float z[32];
+  if (n0 + 32 <= a.N) {                              // warp-uniform: only the last tile is ragged
 #pragma unroll
-  for (int i = 0; i < 32; ++i) z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
+    for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
+  }
   float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int i = 0; i < 32; i += 8)
@@ -169,10 +174,16 @@ __device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, i
   if (cm != -INFINITY) {
     const float nm = fmaxf(m, cm);
     const float nml = nm * kLog2e;
-    float acc = 0.0f;
+    // exp(z - nm) = 2^(z log2e - nm log2e), two logits per f32x2 instruction
+    const float2 l2e = make_float2(kLog2e, kLog2e), nm2 = make_float2(-nml, -nml);
+    float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc += ex2_approx(fmaf(z[i], kLog2e, -nml));
-    s = s * ex2_approx((m - nm) * kLog2e) + acc;   // m = -inf on the first chunk: scale 0
+    for (int i = 0; i < 32; i += 2) {
+      const float2 x = fma2_rn(make_float2(z[i], z[i + 1]), l2e, nm2);
+      acc2[(i >> 1) & 1] = add2_rn(acc2[(i >> 1) & 1], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+    }
+    const float2 a2 = add2_rn(acc2[0], acc2[1]);
+    s = s * ex2_approx((m - nm) * kLog2e) + (a2.x + a2.y);   // m = -inf on the first chunk: scale 0
     m = nm;
   }
   if (static_cast<unsigned>(tgt - n0) < 32u) {
