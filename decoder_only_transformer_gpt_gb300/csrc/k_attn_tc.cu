@@ -375,9 +375,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
           const float2 x = fma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
-          const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
-          pv[i] = (!diag || kb + i <= t) ? e0 : 0.0f;
-          pv[i + 1] = (!diag || kb + i + 1 <= t) ? e1 : 0.0f;
+          pv[i] = ex2_approx(x.x);
+          pv[i + 1] = ex2_approx(x.y);
+        }
+        if (diag) {                                   // keys after t get probability 0
+#pragma unroll
+          for (int i = 0; i < 64; ++i) pv[i] = (kb + i <= t) ? pv[i] : 0.0f;
         }
         float2 ls[4];
 #pragma unroll
