@@ -222,20 +222,42 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const uint32_t
 template <int EPI, int CW>
 __device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t* r, const float* sbias,
                                              uint32_t (&w)[32]) {
-  float v[CW];
+  // element pairs go through the packed f32x2 instructions
+  float2 v2[CW / 2];
 #pragma unroll
-  for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < CW / 2; ++i) v2[i] = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
   if (sbias != nullptr) {
     const float4* b4 = reinterpret_cast<const float4*>(sbias);     // same address in every lane: broadcast
 #pragma unroll
     for (int q = 0; q < CW / 4; ++q) {
       const float4 bb = b4[q];
-      v[4 * q + 0] += bb.x; v[4 * q + 1] += bb.y; v[4 * q + 2] += bb.z; v[4 * q + 3] += bb.w;
+      v2[2 * q] = add2_rn(v2[2 * q], make_float2(bb.x, bb.y));
+      v2[2 * q + 1] = add2_rn(v2[2 * q + 1], make_float2(bb.z, bb.w));
     }
   }
   if (EPI == EPI_BIAS_GELU_OUT) {
+    if (a.gelu_erf) {
 #pragma unroll
-    for (int i = 0; i < CW; ++i) v[i] = gelu_f(v[i], a.gelu_erf);
+      for (int i = 0; i < CW / 2; ++i) v2[i] = make_float2(gelu_f(v2[i].x, 1), gelu_f(v2[i].y, 1));
+    } else {
+      // 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), as h + h tanh(u) with h = x / 2
+      constexpr float c0 = 0.7978845608028654f;
+      constexpr float c1 = 0.7978845608028654f * 0.044715f;
+      const float2 c0v = make_float2(c0, c0), c1v = make_float2(c1, c1), half = make_float2(0.5f, 0.5f);
+#pragma unroll
+      for (int i = 0; i < CW / 2; ++i) {
+        const float2 x = v2[i];
+        const float2 u = mul2_rn(x, fma2_rn(mul2_rn(x, x), c1v, c0v));
+        const float2 h = mul2_rn(x, half);
+        v2[i] = fma2_rn(h, make_float2(tanh_approx(u.x), tanh_approx(u.y)), h);
+      }
+    }
+  }
+  float v[CW];
+#pragma unroll
+  for (int i = 0; i < CW / 2; ++i) {
+    v[2 * i] = v2[i].x;
+    v[2 * i + 1] = v2[i].y;
   }
   if (CW == 64) {
 #pragma unroll
