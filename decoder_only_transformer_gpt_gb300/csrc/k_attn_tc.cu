@@ -56,6 +56,7 @@ constexpr int THREADS = 320;
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by more than this
+constexpr float kSumLimit = 65536.0f;   // off-diagonal tiles: recompute against the exact max past this sum
 constexpr int NS = 5;                   // K/U ring depth (key tiles in flight)
 constexpr uint32_t NSB = 3;             // score buffers: S(j+3) is issued while the softmax works on S(j+1)
 // TMEM columns
@@ -320,36 +321,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         const uint32_t tS = tmem_base + kColS + 128 * b + 64 * hf + lane_off;
         const bool diag = (j == w.n - 1);
         const int kb = j * BKV + 64 * hf;             // first key of this half
-        // this half's 64 scores, kept in registers for both passes (one 64-column TMEM load)
-        uint32_t sv[64];
-        tmem_ld_32x32b_x64(tS, sv);
-        tmem_ld_wait();
-        // pass 1: maximum over this half's allowed keys, eight independent chains
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = (kb + i <= t) ? __uint_as_float(sv[i]) : -INFINITY;
-            const float bv = (kb + 32 + i <= t) ? __uint_as_float(sv[32 + i]) : -INFINITY;
-            mx8[i & 7] = fmax3(mx8[i & 7], a, bv);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx8[i & 7] = fmax3(mx8[i & 7], __uint_as_float(sv[i]), __uint_as_float(sv[32 + i]));
-        }
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-        // a fully masked half (all its keys after t) leaves mx = -inf: nothing to raise
-        const float m_new = fmaxf(m_run, mx * scale_log2);
-        const bool need = m_new > m_run + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
+        // Raise this half's running max to m_new where `need`: scale its sum and output by
+        // 2^(m_run - m_new) (the output once every earlier P U has landed). Warp-uniform.
+        auto raise_max = [&](bool need, float m_new) -> bool {
           if (j > 0) {                                // this half's O must hold all earlier P U
-            if (!mbar_wait_warp(&bars->o_full[(g - 1) % NSB], ((g - 1) / NSB) & 1u, abort_flag, err)) {
-              ok = false;
-              break;
-            }
+            if (!mbar_wait_warp(&bars->o_full[(g - 1) % NSB], ((g - 1) / NSB) & 1u, abort_flag, err)) return false;
             tc_fence_after();
           }
           const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
@@ -367,28 +343,77 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
             }
             tmem_st_wait();
           }
-        }
-        // pass 2: probabilities 2^(s*scale - m_run), two keys per f32x2 instruction
+          return true;
+        };
+        // Exact maximum of this half's allowed keys, eight independent chains.
+        auto tile_max = [&](const uint32_t (&v)[64]) -> float {
+          float mx8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = (!diag || kb + i <= t) ? __uint_as_float(v[i]) : -INFINITY;
+            const float bv = (!diag || kb + 32 + i <= t) ? __uint_as_float(v[32 + i]) : -INFINITY;
+            mx8[i & 7] = fmax3(mx8[i & 7], a, bv);
+          }
+          return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        };
+        // pv = 2^(s*scale - m_run), two keys per f32x2 instruction; returns their sum
         const float2 sc2 = make_float2(scale_log2, scale_log2);
-        const float2 nm2 = make_float2(-m_run, -m_run);
+        auto probs = [&](const uint32_t (&v)[64], float (&p)[64]) -> float {
+          const float2 nm2 = make_float2(-m_run, -m_run);
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            const float2 x = fma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc2, nm2);
+            p[i] = ex2_approx(x.x);
+            p[i + 1] = ex2_approx(x.y);
+          }
+          if (diag) {                                 // keys after t get probability 0
+#pragma unroll
+            for (int i = 0; i < 64; ++i) p[i] = (kb + i <= t) ? p[i] : 0.0f;
+          }
+          float2 ls[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) ls[(i >> 1) & 3] = add2_rn(ls[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
+          const float2 l2 = add2_rn(add2_rn(ls[0], ls[1]), add2_rn(ls[2], ls[3]));
+          return l2.x + l2.y;
+        };
+        // this half's 64 scores (one 64-column TMEM load)
+        uint32_t sv[64];
+        tmem_ld_32x32b_x64(tS, sv);
+        tmem_ld_wait();
         float pv[64];
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float2 x = fma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
-          pv[i] = ex2_approx(x.x);
-          pv[i + 1] = ex2_approx(x.y);
+        float lt;                                     // this tile's sum of probabilities
+        if (!diag) {
+          // Off the diagonal no maximum pass: the probabilities are taken against the running
+          // max (for an item's first tile, against this row's first score), and only a tile
+          // whose sum passes 2^16 (every probability is at most its sum, and an overflow shows
+          // as an infinite sum) is recomputed against its exact maximum.
+          if (j == 0) m_run = __uint_as_float(sv[0]) * scale_log2;
+          lt = probs(sv, pv);
+          if (__any_sync(0xffffffffu, !(lt <= kSumLimit))) {
+            tmem_ld_32x32b_x64(tS, sv);               // the scores again (their registers were reused)
+            tmem_ld_wait();
+            const float m_new = fmaxf(m_run, tile_max(sv) * scale_log2);
+            if (!raise_max(m_new > m_run + kRescaleLog2, m_new)) { ok = false; break; }
+            tmem_ld_32x32b_x64(tS, sv);
+            tmem_ld_wait();
+            lt = probs(sv, pv);
+          }
+        } else {
+          // the diagonal tile: exact maximum first (a fully masked half leaves -inf: nothing to raise)
+          const float m_new = fmaxf(m_run, tile_max(sv) * scale_log2);
+          const bool need = m_new > m_run + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            if (!raise_max(need, m_new)) { ok = false; break; }
+            tmem_ld_32x32b_x64(tS, sv);               // read the scores again rather than hold them
+            tmem_ld_wait();
+          }
+          lt = probs(sv, pv);
         }
-        if (diag) {                                   // keys after t get probability 0
-#pragma unroll
-          for (int i = 0; i < 64; ++i) pv[i] = (kb + i <= t) ? pv[i] : 0.0f;
-        }
-        float2 ls[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) ls[(i >> 1) & 3] = add2_rn(ls[(i >> 1) & 3], make_float2(pv[i], pv[i + 1]));
-        const float2 l2 = add2_rn(add2_rn(ls[0], ls[1]), add2_rn(ls[2], ls[3]));
-        l += l2.x + l2.y;
+        l += lt;
         // P(j) as bf16 pairs over the first 32 columns of this half (its scores are in registers)
         uint32_t pk[32];
 #pragma unroll

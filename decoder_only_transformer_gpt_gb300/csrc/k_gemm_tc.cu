@@ -152,29 +152,47 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
   }
 }
 
-// Cross-entropy epilogue for one 32-column chunk: fold the chunk into the
-// row's running (max m, sum s of exp(z - m)) for this tile, capture the
-// target's logit, and store logits if asked.
-__device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, int grow, int n0, int tgt,
-                                         float& m, float& s) {
-  float z[32];
-  if (n0 + 32 <= a.N) {                              // warp-uniform: only the last tile is ragged
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
-  }
+// Fold 32 logits (-inf for none) into a row's (reference m, sum s of exp(z - m)) against
+// the exact maximum of the chunk and m; m = -inf with s = 0 before the first.
+constexpr float kCeChunkSumLimit = 18446744073709551616.0f;    // 2^64
+__device__ __forceinline__ float ce_fold_exact(const float (&z)[32], float& m, float s) {
   float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int i = 0; i < 32; i += 8)
 #pragma unroll
     for (int k = 0; k < 4; ++k) c4[k] = fmax3(c4[k], z[i + 2 * k], z[i + 2 * k + 1]);
   const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
-  if (cm != -INFINITY) {
-    const float nm = fmaxf(m, cm);
-    const float nml = nm * kLog2e;
-    // exp(z - nm) = 2^(z log2e - nm log2e), two logits per f32x2 instruction
+  if (cm == -INFINITY) return s;
+  const float nm = fmaxf(m, cm);
+  const float nml = nm * kLog2e;
+  const float2 l2e = make_float2(kLog2e, kLog2e), nm2 = make_float2(-nml, -nml);
+  float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 x = fma2_rn(make_float2(z[i], z[i + 1]), l2e, nm2);
+    acc2[(i >> 1) & 1] = add2_rn(acc2[(i >> 1) & 1], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+  }
+  const float2 a2 = add2_rn(acc2[0], acc2[1]);
+  const float out = s * ex2_approx((m - nm) * kLog2e) + (a2.x + a2.y);   // m = -inf: scale 0
+  m = nm;
+  return out;
+}
+
+// Cross-entropy epilogue for one 32-column chunk: fold the chunk into the
+// row's running (reference m, sum s of exp(z - m)) for this tile, capture the
+// target's logit, and store logits if asked.
+__device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, int grow, int n0, int tgt,
+                                         float& m, float& s) {
+  float z[32];
+  const bool whole = n0 + 32 <= a.N;                 // warp-uniform: only the last tile is ragged
+  if (whole) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]);
+    // s = sum exp(z - m) needs m only as a reference, not the maximum: a row's first logit
+    // of the tile starts it, and a chunk is summed against the current reference in one
+    // pass; only a chunk whose sum passes 2^64 (or overflows) is redone below against its max.
+    if (m == -INFINITY) m = z[0];
+    const float nml = m * kLog2e;
     const float2 l2e = make_float2(kLog2e, kLog2e), nm2 = make_float2(-nml, -nml);
     float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
@@ -183,8 +201,16 @@ __device__ __forceinline__ void ce_chunk(const GemmArgs& a, const uint32_t* r, i
       acc2[(i >> 1) & 1] = add2_rn(acc2[(i >> 1) & 1], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
     }
     const float2 a2 = add2_rn(acc2[0], acc2[1]);
-    s = s * ex2_approx((m - nm) * kLog2e) + (a2.x + a2.y);   // m = -inf on the first chunk: scale 0
-    m = nm;
+    const float cs = a2.x + a2.y;
+    if (cs <= kCeChunkSumLimit) {
+      s += cs;
+    } else {
+      s = ce_fold_exact(z, m, s);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = (n0 + i < a.N) ? __uint_as_float(r[i]) : -INFINITY;
+    s = ce_fold_exact(z, m, s);
   }
   if (static_cast<unsigned>(tgt - n0) < 32u) {
     float zt = 0.0f;

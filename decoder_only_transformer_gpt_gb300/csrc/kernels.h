@@ -31,8 +31,9 @@ struct GemmArgs {
   int ldo;
   int gelu_erf;             // 0 tanh form, 1 erf form
   const int32_t* targets;   // EPI_CE: [M]
-  float* pmax;              // EPI_CE: [NB, M] tile maxima of the logits
-  float* psum;              // EPI_CE: [NB, M] sum of exp(z - tile max)
+  float* pmax;              // EPI_CE: [NB, M] per tile a reference logit m: one of the row's logits
+                            //         in the tile, at most 64 ln 2 below their maximum
+  float* psum;              // EPI_CE: [NB, M] sum over the tile of exp(z - m)
   float* ztgt;              // EPI_CE: [M] the target's logit
   float* logits;            // EPI_CE: [M, ldo] fp32 or nullptr
   int* err;                 // device error word

@@ -89,12 +89,14 @@ def test_gemm_tc_stream_k_deterministic(gpt_lib):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
-def _attn_case(B, T, H, D, seed=0, qk_scale=1.5):
+def _attn_case(B, T, H, D, seed=0, qk_scale=1.5, boost_keys=None):
     from decoder_only_transformer_gpt_gb300 import binding
     rng = np.random.default_rng(seed)
     C = H * D
     qkv = rand_bf16(rng, (B, T, 3 * C))
     qkv[..., :2 * C] = qkv[..., :2 * C] * qk_scale          # peaky softmax (power of two keeps bf16 exact)
+    if boost_keys is not None:                               # keys whose scores jump (x 8, still bf16-exact)
+        qkv[:, boost_keys, C:2 * C] *= 8.0
     y = torch.empty((B, T, C), dtype=torch.bfloat16, device="cuda")
     binding.attention(dev_bf16(qkv), y, H)
     binding.status()
@@ -110,6 +112,14 @@ def _attn_case(B, T, H, D, seed=0, qk_scale=1.5):
                                      (2, 777, 2, 64), (1, 1024, 2, 64), (2, 300, 3, 32)])
 def test_attention_tc(gpt_lib, B, T, H, D):
     _attn_case(B, T, H, D, qk_scale=2.0)
+
+
+@pytest.mark.parametrize("D", [64, 32])
+def test_attention_tc_late_max(gpt_lib, D):
+    # keys 256..383 score 8x higher: queries 384..511 meet their running maximum's jump in an
+    # off-diagonal key tile after two earlier ones (the raise-and-recompute path with a
+    # rescale of the output), queries 256..383 on their diagonal tile
+    _attn_case(2, 512, 2, D, seed=11, qk_scale=1.0, boost_keys=slice(256, 384))
 
 
 @pytest.mark.parametrize("C,M", [(768, 37), (128, 300), (16, 5), (2048, 9)])
