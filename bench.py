@@ -49,14 +49,18 @@ STEP_KINDS = [("embed", 0, False), ("c_attn", 1, True), ("attention", 2, True), 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the same
 # launch configuration, valid only while the kernel's sources hash to the digest recorded with it.
 NCU_TRAFFIC = {
-    "attention": {"bytes": 75.940864e6 + 6.589184e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
+    "attention": {"bytes": 75.961344e6 + 6.167040e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                  "digest": "1c1aff9e9f550641087cf6825bbe918751ada5ea"},
-    "head": {"bytes": 102.54848e6 + 17.579776e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+                  "digest": "42a0a54118b079c59411ffb054c71c4fbf5d5995"},
+    "head": {"bytes": 102.546432e6 + 17.707008e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "93867db28a7d1e43baf70de122f9c90028bc21af"},
+             "digest": "2b4ddb1cbd737796727556269c4b582bb97632cb"},
+    "mlp_proj": {"bytes": 163.247872e6 + 25.978880e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+                 "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
+                             "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
+                 "digest": "2b4ddb1cbd737796727556269c4b582bb97632cb"},
 }
 
 
