@@ -1,6 +1,6 @@
 """Throughput of the GPT-2-small forward pass + mean next-token cross-entropy on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--model gpt2_small|gpt2_xl]
 
 One step = one full forward + loss (embedding, 12 blocks, ln_f, tied head with
 the fused cross-entropy, mean) over a batch of B x T synthetic tokens of the
@@ -12,6 +12,10 @@ tokens / max-over-ranks time ("weak" scaling).
 
 --impl reference times the fp64 oracle on the host cores, one bounded sample
 (one sequence prefix) per step, in the same metric and unit.
+
+--model gpt2_xl runs the same path at the GPT-2 XL shape (48 blocks, C = 1600,
+25 heads, FFN 6400; 1.56 B parameters) as a second workload; the default is
+GPT-2 small, the configuration the throughput target is stated on.
 """
 import argparse
 import json
@@ -29,6 +33,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GPT-2 small fwd+CE tokens/sec on 1 GB300; % of BF16 tensor-core peak"
 WORKLOAD = "gpt2_small_b16_t1024"
+MODELS = {   # --model: (workload, metric, workload name at B=16, T=1024)
+    "gpt2_small": ("gpt2_sweep", METRIC, WORKLOAD),
+    "gpt2_xl": ("gpt2_xl", "GPT-2 XL fwd+CE tokens/sec on 1 GB300; % of BF16 tensor-core peak",
+                "gpt2_xl_b16_t1024"),
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -216,7 +225,8 @@ def run_reference(args, rank, world):
     from workloads import workload
     from workloads.generate import generate
     import oracle
-    wl = workload("gpt2_sweep")
+    wl_name, metric, wl_label = MODELS[args.model]
+    wl = workload(wl_name)
     w, ids, tg = generate(wl, B=16, T=1024)
     T = 128
     for _ in range(args.warmup):
@@ -227,10 +237,10 @@ def run_reference(args, rank, world):
         oracle.forward(wl.cfg, w, ids[r:r + 1, :T], tg[r:r + 1, :T])
     dt = time.perf_counter() - t0
     value = args.steps * T / dt
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "B": 16, "T": 1024, "sample_per_step": f"1 x {T} tokens"},
+            "config": {"workload": wl_label, "B": 16, "T": 1024, "sample_per_step": f"1 x {T} tokens"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"1 sequence x {T} tokens per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -246,7 +256,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wl = workload("gpt2_sweep")
+    wl_name, metric, wl_label = MODELS[args.model]
+    wl = workload(wl_name)
     B, T = args.batch, args.seq
     w, ids_np, tg_np = generate(wl, B=B, T=T)
     cfg = wl.cfg
@@ -364,18 +375,21 @@ def run_ours(args, rank, world, local_rank):
     achieved, peak, unit = rate(breakdown[dom]["work"], breakdown[dom]["bound"], dom_avg)
     traffic = None
     tr = NCU_TRAFFIC.get(dom)
-    if tr is not None and (B, T) == (16, 1024) and source_digest(tr["sources"]) == tr["digest"]:
+    if (tr is not None and args.model == "gpt2_small" and (B, T) == (16, 1024)
+            and source_digest(tr["sources"]) == tr["digest"]):
         traffic = tr["bytes"]
+    n_params = cfg.L * (12 * cfg.C * cfg.C + 13 * cfg.C) + (cfg.V + cfg.ctx + 2) * cfg.C   # ffn = 4C
+    weight_mb = 2e-6 * n_params                                                          # bf16
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, w, ids_np, tg_np)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if (B, T) == (16, 1024) else f"gpt2_small_b{B}_t{T}", "B": B, "T": T,
+        "config": {"workload": wl_label if (B, T) == (16, 1024) else f"{args.model}_b{B}_t{T}", "B": B, "T": T,
                    "V": cfg.V, "C": cfg.C, "H": cfg.H, "L": cfg.L, "ids": "zipf(1.1) seed 4",
-                   "l2": "inputs larger than L2 (weights 249 MB + activations per step > 129 MB)",
+                   "l2": f"inputs larger than L2 (weights {weight_mb:.0f} MB + activations per step > 129 MB)",
                    "parallelism": f"replicas x{world}"},
         "tflops": flops * args.steps * world / (ms_max / 1e3) / 1e12,
         "frac_of_peak": flops / (ms_max / args.steps / 1e3) / 1e12 / float(pk["bf16_tflops"]),
@@ -406,6 +420,7 @@ def main():
     ap.add_argument("--batch", type=int, default=16)
     ap.add_argument("--seq", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--model", choices=sorted(MODELS), default="gpt2_small")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

@@ -64,12 +64,13 @@ def test_gemm_tc_many_tiles_per_cta(gpt_lib, M, N, K):
     _gemm_case(gpt_lib, M, N, K, 0, seed=M)
 
 
-@pytest.mark.parametrize("M,N,K", [(6500, 768, 3072), (4000, 2304, 1544), (5000, 2304, 1536)])
+@pytest.mark.parametrize("M,N,K", [(6500, 768, 3072), (4000, 2304, 1544), (5000, 2304, 1536), (4000, 1600, 1600)])
 @pytest.mark.parametrize("epi", [0, 1, 2])
 def test_gemm_tc_stream_k(gpt_lib, M, N, K, epi):
     # more tiles than SMs, not a whole number of waves, K >= 1536: tiles are split
     # along K between CTAs. With 152 SMs: 153 tiles (151 splits), 288 tiles with a
-    # ragged last K block, and 360 tiles (a 208-tile split region, then a whole wave).
+    # ragged last K block, 360 tiles (a 208-tile split region, then a whole wave), and
+    # 224 tiles whose last column tile is ragged (N = 1600, the GPT-2 XL width).
     _gemm_case(gpt_lib, M, N, K, epi, seed=K + epi)
 
 

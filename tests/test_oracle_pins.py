@@ -65,6 +65,19 @@ def test_param_count_gpt1_about_117m():
     assert abs(n / 1e6 - g["value_millions"]) / g["value_millions"] < 0.01, g["cite"]
 
 
+def test_param_count_gpt2_xl_about_1_5b():
+    # the page rounds 1,557,611,200 (tied head, ctx 1024) to "1.5B"; its FFN width is 4C
+    g = GOLDEN["gpt2_xl_shape"]
+    cfg = workload("gpt2_xl").cfg
+    assert (cfg.V, cfg.C, cfg.H, cfg.L, cfg.ffn) == (g["V"], g["C"], g["H"], g["L"], g["ffn"]), g["cite"]
+    assert cfg.ffn == 4 * cfg.C and cfg.C // cfg.H == 64
+    n = go.param_count(cfg)
+    assert n == 48 * (12 * 1600 ** 2 + 13 * 1600) + 50257 * 1600 + 1024 * 1600 + 2 * 1600 == 1_557_611_200
+    assert abs(n / 1e9 - g["value_billions"]) / g["value_billions"] < 0.05, g["cite"]
+    e = GOLDEN["gpt2_xl_embedding_params_approx"]
+    assert abs(e["V"] * e["C"] / 1e6 - e["value_millions"]) / e["value_millions"] < 0.01, e["cite"]
+
+
 def test_kv_values_per_token():
     g = GOLDEN["kv_values_per_token"]
     assert 2 * g["L"] * g["H"] * g["D"] == g["value"]

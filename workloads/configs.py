@@ -61,6 +61,7 @@ class Workload:
 
 
 GPT2_SMALL = GPTConfig(V=50257, C=768, H=12, L=12, ctx=1024, ffn=3072)
+GPT2_XL = GPTConfig(V=50257, C=1600, H=25, L=48, ctx=1024, ffn=6400)
 
 WORKLOADS = {
     # toy GPT-2 from the chapter-25 experiment; fp32 parity mode
@@ -77,6 +78,9 @@ WORKLOADS = {
     "gpt2_sweep": Workload("gpt2_sweep", GPT2_SMALL, B=16, T=1024, seed=4, ids="zipf",
                            targets="shifted", scale_cproj=True,
                            extra_shapes=((1, 1024), (16, 1024), (32, 1024), (16, 777))),
+    # the same path at the GPT-2 XL shape (48 blocks, C = 1600, 25 heads of 64)
+    "gpt2_xl": Workload("gpt2_xl", GPT2_XL, B=16, T=1024, seed=6, ids="zipf", targets="shifted",
+                        scale_cproj=True),
 }
 
 
