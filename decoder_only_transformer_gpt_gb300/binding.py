@@ -73,6 +73,9 @@ def load(path: str = LIB_PATH):
         "gpt_time_step": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gpt_last_launch_count": (ctypes.c_int, [vp]),
         "gpt_last_probe_hits": (ctypes.c_int, [vp]),
+        "gpt_kv_reserve": (ctypes.c_int, [vp, i32]),
+        "gpt_prefill": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
+        "gpt_decode_step": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
@@ -173,6 +176,20 @@ class GPTModel:
         """The host-buffer entry with raw (e.g. pinned) host pointers."""
         _check(self.lib.gpt_forward_host(self.handle, ids_ptr, tg_ptr, B, T, loss_ptr, None, _stream(stream)),
                "gpt_forward_host")
+
+    def kv_reserve(self, max_batch: int) -> None:
+        """Allocate the key/value cache for up to max_batch sequences of ctx tokens."""
+        _check(self.lib.gpt_kv_reserve(self.handle, max_batch), "gpt_kv_reserve")
+
+    def prefill(self, ids, logits=None, stream=None) -> None:
+        """Forward over prompts ids [B, T] (device int32) that fills the cache; logits [B, V] of the last tokens."""
+        B, T = ids.shape
+        _check(self.lib.gpt_prefill(self.handle, _ptr(ids), B, T, _ptr(logits), _stream(stream)), "gpt_prefill")
+
+    def decode_step(self, ids, pos: int, logits, stream=None) -> None:
+        """Append ids [B] (device int32) at position pos; logits [B, V] of the next token."""
+        _check(self.lib.gpt_decode_step(self.handle, _ptr(ids), ids.shape[0], pos, _ptr(logits), _stream(stream)),
+               "gpt_decode_step")
 
     def status(self, stream=None):
         _check(self.lib.gpt_status(self.handle, _stream(stream)), "gpt_status")

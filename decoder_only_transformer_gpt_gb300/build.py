@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgpt_gb300.so")
 
-SOURCES = ["k_gemm_tc.cu", "k_attn_tc.cu", "k_rowwise.cu", "k_simt.cu", "tmap.cu", "gpt_api.cu",
+SOURCES = ["k_gemm_tc.cu", "k_attn_tc.cu", "k_rowwise.cu", "k_simt.cu", "k_decode.cu", "tmap.cu", "gpt_api.cu",
            "gpt_forward.cu", "gptk.cu", "gptk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,

@@ -97,6 +97,7 @@ void free_model(gpt_model* m) {
   cudaFree(m->wbuf);
   cudaFree(m->ws);
   cudaFree(m->stage_logits);
+  cudaFree(m->kv);
   cudaFreeHost(m->h_pinned);
   delete m;
 }
@@ -268,6 +269,20 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
   if (cudaMemset(m->err, 0, sizeof(int)) != cudaSuccess) { free_model(m); return GPT_ECUDA; }
   if (cudaMallocHost(&m->h_pinned, 64) != cudaSuccess) { free_model(m); return GPT_ENOMEM; }
   *out = m;
+  return GPT_OK;
+}
+
+int gpt_kv_reserve(gpt_model* m, int32_t max_batch) {
+  if (!m || max_batch < 1) return GPT_EINVAL;
+  if (!m->bf16) return GPT_ECONFIG;
+  if (max_batch <= m->kv_batch) return GPT_OK;
+  const size_t bytes = static_cast<size_t>(m->cfg.L) * max_batch * m->cfg.ctx * 2 * m->cfg.C * 2;
+  uint8_t* p = nullptr;
+  if (bytes > 0 && cudaMalloc(&p, bytes) != cudaSuccess) return GPT_ENOMEM;
+  cudaDeviceSynchronize();                  // no launch may still use the old cache
+  cudaFree(m->kv);
+  m->kv = p;
+  m->kv_batch = max_batch;
   return GPT_OK;
 }
 

@@ -81,6 +81,11 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   return GPT_OK;
 }
 
+// Layer l's key/value cache: [kv_batch][ctx][2C] bf16.
+void* kv_layer(gpt_model* m, int l) {
+  return m->kv + static_cast<size_t>(l) * m->kv_batch * m->cfg.ctx * 2 * m->cfg.C * 2;
+}
+
 // The LayerNorm that follows the residual add of a block (or ln_f / nothing).
 // Pre-norm: a = LN(x). Post-norm: x = LN(x) and a = copy of it.
 struct NextLN { const float* g; const float* b; };
@@ -109,6 +114,11 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
   for (int l = 0; l < L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
     GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
+    if (m->kv_fill) {                       // prefill: keep every token's key and value
+      ++m->launches;
+      rc = cu(launch_kv_store(m->qkv, kv_layer(m, l), B, T, C, c.ctx, s), "kv_store");
+      if (rc != GPT_OK) return rc;
+    }
     GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_tc(m->tm_qkv, m->y, B, T, c.H, C / c.H, m->err, s), "attention"));
     // the LayerNorm after each residual add: ln_2 then the next block's ln_1 or ln_f
     // (pre-norm), ln_1 then ln_2 applied to x itself (post-norm)
@@ -225,6 +235,53 @@ int check_shape(const gpt_model* m, int B, int T) {
   return GPT_OK;
 }
 
+// One decode step (bf16): B new tokens at position pos, every projection a
+// matrix-vector product over the B rows, attention over the cached rows.
+int decode_bf16(gpt_model* m, const int32_t* ids, int B, int pos, float* d_logits, cudaStream_t s) {
+  const gpt_config& c = m->cfg;
+  const int C = c.C, F = c.ffn, L = c.L, D = C / c.H;
+  const bool pre = c.norm_mode == 0;
+#define GPT_DEC(expr, what)                       \
+  do {                                            \
+    const int rc_ = cu((expr), what);             \
+    if (rc_ != GPT_OK) return rc_;                \
+    ++m->launches;                                \
+  } while (0)
+  {
+    int out_mode = 1;
+    const float* g = nullptr;
+    const float* b = nullptr;
+    if (pre) {
+      if (L > 0) { out_mode = 2; g = m->layers[0].ln1_g; b = m->layers[0].ln1_b; }
+      else if (c.final_ln) { out_mode = 2; g = m->lnf_g; b = m->lnf_b; }
+    }
+    GPT_DEC(launch_embed(ids, m->wte, m->wpe, 1, m->x, m->a, out_mode, 1, g, b, B, 1, C, c.V, c.ln_eps, m->err, s, pos),
+            "embed");
+  }
+  for (int l = 0; l < L; ++l) {
+    const gpt_layer_dev& w = m->layers[l];
+    GPT_DEC(launch_gemv(m->a, C, w.attn_w, w.attn_b, m->qkv, 3 * C, B, 3 * C, C, EPI_BIAS_OUT, c.gelu, s), "c_attn");
+    GPT_DEC(launch_attention_decode(m->qkv, kv_layer(m, l), m->y, B, c.H, D, c.ctx, pos, s), "attention");
+    NextLN mid = pre ? NextLN{w.ln2_g, w.ln2_b} : NextLN{w.ln1_g, w.ln1_b};
+    NextLN out{w.ln2_g, w.ln2_b};
+    if (pre) {
+      out = {nullptr, nullptr};
+      if (l + 1 < L) out = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
+      else if (c.final_ln) out = {m->lnf_g, m->lnf_b};
+    }
+    GPT_DEC(launch_gemv(m->y, C, w.proj_w, w.proj_b, m->x, C, B, C, C, EPI_BIAS_RESID, c.gelu, s), "c_proj");
+    GPT_DEC(launch_layernorm(m->x, mid.g, mid.b, m->a, 1, pre ? nullptr : m->x, B, C, c.ln_eps, s), "ln");
+    GPT_DEC(launch_gemv(m->a, C, w.fc_w, w.fc_b, m->g, F, B, F, C, EPI_BIAS_GELU_OUT, c.gelu, s), "c_fc");
+    GPT_DEC(launch_gemv(m->g, F, w.mp_w, w.mp_b, m->x, C, B, C, F, EPI_BIAS_RESID, c.gelu, s), "mlp_proj");
+    GPT_DEC(launch_layernorm(m->x, out.g, out.b, m->a, 1, pre ? nullptr : m->x, B, C, c.ln_eps, s), "ln");
+  }
+  if (!pre && L == 0 && c.final_ln)
+    GPT_DEC(launch_layernorm(m->x, m->lnf_g, m->lnf_b, m->a, 1, nullptr, B, C, c.ln_eps, s), "ln");
+  GPT_DEC(launch_gemv(m->a, C, m->wte, nullptr, d_logits, c.V, B, c.V, C, EPI_F32, c.gelu, s), "head");
+#undef GPT_DEC
+  return GPT_OK;
+}
+
 int map_device_error(int code) {
   switch (code) {
     case GPT_DEV_OK: return GPT_OK;
@@ -251,6 +308,39 @@ int gpt_forward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, in
   m->prof_ev0 = m->prof_ev1 = nullptr;       // a probe covers one forward
   m->prof_step = m->prof_layer = -1;
   return rc;
+}
+
+int gpt_prefill(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t T, float* d_logits, void* stream) {
+  if (!m || !d_ids) return GPT_EINVAL;
+  if (!m->bf16) return GPT_ECONFIG;
+  int rc = check_shape(m, B, T);
+  if (rc != GPT_OK) return rc;
+  if (B > m->kv_batch) return GPT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  m->launches = 0;
+  m->probe_hits = 0;
+  m->kv_fill = true;
+  rc = forward_bf16(m, d_ids, nullptr, B, T, nullptr, nullptr, s);
+  m->kv_fill = false;
+  m->prof_ev0 = m->prof_ev1 = nullptr;
+  m->prof_step = m->prof_layer = -1;
+  if (rc != GPT_OK || !d_logits) return rc;
+  // the head on each sequence's last row only (rows T-1, 2T-1, ... of the final activations)
+  const gpt_config& c = m->cfg;
+  rc = cu(launch_gemv(static_cast<const uint8_t*>(m->a) + static_cast<size_t>(T - 1) * c.C * 2, T * c.C, m->wte,
+                      nullptr, d_logits, c.V, B, c.V, c.C, EPI_F32, c.gelu, s),
+          "head");
+  if (rc == GPT_OK) ++m->launches;
+  return rc;
+}
+
+int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, float* d_logits, void* stream) {
+  if (!m || !d_ids || !d_logits) return GPT_EINVAL;
+  if (!m->bf16) return GPT_ECONFIG;
+  if (B < 1 || B > m->kv_batch || B > m->cfg.max_tokens) return GPT_EINVAL;
+  if (pos < 0 || pos >= m->cfg.ctx) return GPT_ESEQ;
+  m->launches = 0;
+  return decode_bf16(m, d_ids, B, pos, d_logits, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_stop) {

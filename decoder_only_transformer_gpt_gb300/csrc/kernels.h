@@ -66,9 +66,10 @@ cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T
                                 int* err, cudaStream_t s);
 
 // ---- row-wise kernels (both paths)
+// Row m is token m of its sequence at position pos0 + m % T.
 cudaError_t launch_embed(const int32_t* ids, const void* wte, const void* wpe, int wdt, float* x,
                          void* out, int out_mode, int odt, const float* g, const float* b,
-                         int M, int T, int C, int V, float eps, int* err, cudaStream_t s);
+                         int M, int T, int C, int V, float eps, int* err, cudaStream_t s, int pos0 = 0);
 cudaError_t launch_layernorm(const float* x, const float* g, const float* b, void* out, int odt,
                              float* out_f32, int M, int C, float eps, cudaStream_t s);
 // nll per row from the head's partials; block_sums (nullable) receives one sum of
@@ -98,5 +99,18 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t r
                   uint32_t box_cols, uint32_t box_rows);
 // qkv viewed as [B][T][3C] bf16 with a box of 128 rows x D columns (one batch).
 bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int D);
+
+// ---- incremental decoding (bf16)
+constexpr int kGemvMaxRows = 16;       // rows per matrix-vector launch
+// out[r, :] = epilogue(a[r, :] W^T (+ bias)) for r < M (any M; a: bf16 rows of stride lda,
+// W: bf16 [N, K] with K % 8 == 0; epi as for the GEMMs: bf16 out, bf16 GELU out, fp32 +=, fp32 out).
+cudaError_t launch_gemv(const void* a, int lda, const void* W, const float* bias, void* out, int ldo, int M, int N,
+                        int K, int epi, int gelu_erf, cudaStream_t s);
+// The new tokens' attention at position pos: stores each one's key and value (from qkv [B, 3C])
+// in the layer's cache [batch][ctx][2C] at pos, then y[b] = softmax over keys 0..pos.
+cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y, int B, int H, int D, int ctx, int pos,
+                                    cudaStream_t s);
+// cache[b][t][0:2C] = qkv[b, t][C:3C] for a prompt of T tokens.
+cudaError_t launch_kv_store(const void* qkv, void* cache_layer, int B, int T, int C, int ctx, cudaStream_t s);
 
 }  // namespace gptgb

@@ -40,6 +40,10 @@ struct gpt_model {
   float* logits_ws = nullptr;   // fp32 path: [Mx, V]
   float* sk_part = nullptr;     // bf16 path: stream-K partial tiles of the block projections
   int* sk_flag = nullptr;       // and their flags (zero between launches)
+  // key/value cache for incremental decoding: per layer [kv_batch][ctx][2C] bf16
+  uint8_t* kv = nullptr;
+  int kv_batch = 0;
+  bool kv_fill = false;         // the next bf16 forward also stores keys and values (prefill)
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;

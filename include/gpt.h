@@ -152,6 +152,40 @@ int gpt_last_launch_count(const gpt_model* m);
  * block index past the last block). */
 int gpt_last_probe_hits(const gpt_model* m);
 
+/*
+ * Incremental decoding with a key/value cache ("预训练一个 Mini GPT", the
+ * sections on the KV cache and on prefill and decode: the keys and values of
+ * every processed token are kept, so a new token costs one projection of its
+ * own row per layer plus attention over the cached rows). bf16 models only
+ * (GPT_ECONFIG otherwise).
+ *
+ * gpt_kv_reserve: allocate (or grow) the model-owned cache for up to
+ * max_batch sequences of ctx tokens: L x max_batch x ctx x 2C bf16
+ * (604 MB for GPT-2 small at 16 sequences). Synchronous; GPT_ENOMEM on failure.
+ */
+int gpt_kv_reserve(gpt_model* m, int32_t max_batch);
+
+/*
+ * Prefill: the forward pass over prompts d_ids [B, T] (device int32, all of
+ * length T) that also stores every token's key and value in the cache (rows
+ * 0..T-1 of sequences 0..B-1), and writes the logits of each sequence's last
+ * token to d_logits [B, V] (device fp32; NULL: not computed). Requires
+ * B <= the reserved batch (GPT_EINVAL), T <= ctx (GPT_ESEQ), B*T <= max_tokens.
+ * Stream-ordered and asynchronous like gpt_forward.
+ */
+int gpt_prefill(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t T, float* d_logits, void* stream);
+
+/*
+ * One decode step: token d_ids[b] (device int32 [B]) is appended to sequence
+ * b at position pos (its key and value go to cache row pos; rows 0..pos-1
+ * must hold that sequence's earlier tokens, from gpt_prefill and earlier
+ * steps), and d_logits [B, V] (device fp32) receives the next-token logits,
+ * equal to row pos of a full forward over the sequence. Requires
+ * 0 <= pos < ctx (GPT_ESEQ) and B <= the reserved batch (GPT_EINVAL).
+ * Stream-ordered and asynchronous; bad ids are reported by gpt_status().
+ */
+int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, float* d_logits, void* stream);
+
 /* Synchronise the stream, read and clear the model's device error word. */
 int gpt_status(gpt_model* m, void* stream);
 
