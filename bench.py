@@ -411,6 +411,73 @@ def run_ours(args, rank, world, local_rank):
     model.close()
 
 
+def run_decode(args, rank, world, local_rank):
+    """--decode: tokens/s of incremental decoding with the key/value cache (a second measurement,
+    not the default line). B sequences are prefilled with a prompt of --prompt tokens; then --steps
+    decode steps (one new token per sequence each) are timed with CUDA events. Decode streams
+    every weight and each sequence's cached keys and values once per step, so the roofline is
+    HBM bandwidth: algorithmic bytes per step = weights (bf16) + B x L x (pos + 1) x 2C x 2 bytes
+    of cache + the B x V fp32 logits written, averaged over the timed positions."""
+    import torch
+    from decoder_only_transformer_gpt_gb300 import binding
+    from workloads import workload
+    from workloads.generate import generate
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl_name, _, wl_label = MODELS[args.model]
+    wl = workload(wl_name)
+    cfg = wl.cfg
+    B, T0 = args.batch, args.prompt
+    n_new = args.warmup + args.steps
+    if T0 + n_new > cfg.ctx:
+        raise SystemExit(f"--prompt {T0} + {n_new} decode steps exceed ctx {cfg.ctx}")
+    w, ids_np, _ = generate(wl, B=B, T=T0 + n_new)
+    model = binding.GPTModel(cfg, w, B * T0)
+    model.kv_reserve(B)
+    ids = torch.from_numpy(ids_np).to(dev)
+    cols = [ids[:, t].contiguous() for t in range(T0 + n_new)]
+    logits = torch.empty((B, cfg.V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    model.prefill(ids[:, :T0].contiguous(), logits)
+    for k in range(args.warmup):
+        model.decode_step(cols[T0 + k], T0 + k, logits)
+    model.status()
+    launches = model.lib.gpt_last_launch_count(model.handle)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    torch.cuda.synchronize()
+    start.record(stream)
+    p0 = T0 + args.warmup
+    for k in range(args.steps):
+        model.decode_step(cols[p0 + k], p0 + k, logits)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    model.status()
+    ms = start.elapsed_time(stop)
+    n_params = cfg.L * (12 * cfg.C * cfg.C + 13 * cfg.C) + (cfg.V + cfg.ctx + 2) * cfg.C
+    mean_pos = p0 + (args.steps - 1) / 2.0
+    step_bytes = 2.0 * n_params + B * cfg.L * (mean_pos + 1) * 2 * cfg.C * 2 + B * cfg.V * 4
+    pk, pk_src = peaks()
+    achieved = step_bytes * args.steps / (ms / 1e3) / 1e9
+    line = {
+        "metric": f"{wl_label.split('_b')[0]} decode tokens/sec (KV cache) on 1 GB300", "value": B * args.steps / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.model}_decode_b{B}_prompt{T0}", "B": B, "prompt": T0,
+                   "positions": [p0, p0 + args.steps - 1],
+                   "l2": f"weights {2e-6 * n_params:.0f} MB read per step, larger than L2"},
+        "clocks": clk, "gpu_launches": launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                     "frac": achieved / float(pk["hbm_gbs"]), "traffic": None, "algorithmic_bytes_per_step": step_bytes,
+                     "peak_source": f"{pk_src} HBM copy"},
+    }
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,6 +488,8 @@ def main():
     ap.add_argument("--seq", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--model", choices=sorted(MODELS), default="gpt2_small")
+    ap.add_argument("--decode", action="store_true", help="time incremental decoding instead of the forward")
+    ap.add_argument("--prompt", type=int, default=512, help="--decode: prompt length before the timed steps")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
@@ -436,7 +505,11 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     from decoder_only_transformer_gpt_gb300 import build
     build.build()
-    run_ours(args, rank, world, local_rank)
+    if args.decode:
+        if rank == 0:
+            run_decode(args, rank, world, local_rank)
+    else:
+        run_ours(args, rank, world, local_rank)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -98,6 +98,9 @@ void free_model(gpt_model* m) {
   cudaFree(m->ws);
   cudaFree(m->stage_logits);
   cudaFree(m->kv);
+  cudaFree(m->dec_pos);
+  if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   cudaFreeHost(m->h_pinned);
   delete m;
 }
@@ -277,12 +280,17 @@ int gpt_kv_reserve(gpt_model* m, int32_t max_batch) {
   if (!m->bf16) return GPT_ECONFIG;
   if (max_batch <= m->kv_batch) return GPT_OK;
   const size_t bytes = static_cast<size_t>(m->cfg.L) * max_batch * m->cfg.ctx * 2 * m->cfg.C * 2;
+  if (!m->dec_pos && cudaMalloc(&m->dec_pos, sizeof(int)) != cudaSuccess) return GPT_ENOMEM;
   uint8_t* p = nullptr;
   if (bytes > 0 && cudaMalloc(&p, bytes) != cudaSuccess) return GPT_ENOMEM;
   cudaDeviceSynchronize();                  // no launch may still use the old cache
   cudaFree(m->kv);
   m->kv = p;
   m->kv_batch = max_batch;
+  if (m->dec_exec) {                        // the captured step holds the old cache's address
+    cudaGraphExecDestroy(m->dec_exec);
+    m->dec_exec = nullptr;
+  }
   return GPT_OK;
 }
 

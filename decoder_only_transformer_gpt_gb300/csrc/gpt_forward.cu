@@ -20,6 +20,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 using namespace gptgb;
 
 namespace {
@@ -235,9 +237,19 @@ int check_shape(const gpt_model* m, int B, int T) {
   return GPT_OK;
 }
 
-// One decode step (bf16): B new tokens at position pos, every projection a
+// Decode steps are captured once into a CUDA graph and replayed (GPT_GB300_NO_GRAPH=1: launched
+// directly each step); the results are the same either way.
+bool decode_graphs_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GPT_GB300_NO_GRAPH");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
+
+// One decode step (bf16): B new tokens at position *pos_dev, every projection a
 // matrix-vector product over the B rows, attention over the cached rows.
-int decode_bf16(gpt_model* m, const int32_t* ids, int B, int pos, float* d_logits, cudaStream_t s) {
+int decode_bf16(gpt_model* m, const int32_t* ids, int B, const int* pos_dev, float* d_logits, cudaStream_t s) {
   const gpt_config& c = m->cfg;
   const int C = c.C, F = c.ffn, L = c.L, D = C / c.H;
   const bool pre = c.norm_mode == 0;
@@ -255,13 +267,14 @@ int decode_bf16(gpt_model* m, const int32_t* ids, int B, int pos, float* d_logit
       if (L > 0) { out_mode = 2; g = m->layers[0].ln1_g; b = m->layers[0].ln1_b; }
       else if (c.final_ln) { out_mode = 2; g = m->lnf_g; b = m->lnf_b; }
     }
-    GPT_DEC(launch_embed(ids, m->wte, m->wpe, 1, m->x, m->a, out_mode, 1, g, b, B, 1, C, c.V, c.ln_eps, m->err, s, pos),
+    GPT_DEC(launch_embed(ids, m->wte, m->wpe, 1, m->x, m->a, out_mode, 1, g, b, B, 1, C, c.V, c.ln_eps, m->err, s, 0,
+                         pos_dev),
             "embed");
   }
   for (int l = 0; l < L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
     GPT_DEC(launch_gemv(m->a, C, w.attn_w, w.attn_b, m->qkv, 3 * C, B, 3 * C, C, EPI_BIAS_OUT, c.gelu, s), "c_attn");
-    GPT_DEC(launch_attention_decode(m->qkv, kv_layer(m, l), m->y, B, c.H, D, c.ctx, pos, s), "attention");
+    GPT_DEC(launch_attention_decode(m->qkv, kv_layer(m, l), m->y, B, c.H, D, c.ctx, pos_dev, s), "attention");
     NextLN mid = pre ? NextLN{w.ln2_g, w.ln2_b} : NextLN{w.ln1_g, w.ln1_b};
     NextLN out{w.ln2_g, w.ln2_b};
     if (pre) {
@@ -339,8 +352,41 @@ int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, 
   if (!m->bf16) return GPT_ECONFIG;
   if (B < 1 || B > m->kv_batch || B > m->cfg.max_tokens) return GPT_EINVAL;
   if (pos < 0 || pos >= m->cfg.ctx) return GPT_ESEQ;
-  m->launches = 0;
-  return decode_bf16(m, d_ids, B, pos, d_logits, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the step reads its ids and position from model memory, so one captured graph serves every step
+  GPT_CUDA(cudaMemcpyAsync(m->stage_ids, d_ids, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+  GPT_CUDA(launch_set_int(m->dec_pos, pos, s));
+  if (!decode_graphs_enabled()) {
+    m->launches = 1;
+    return decode_bf16(m, m->stage_ids, B, m->dec_pos, d_logits, s);
+  }
+  if (!m->dec_exec || m->dec_B != B || m->dec_logits != d_logits) {
+    if (m->dec_exec) {
+      GPT_CUDA(cudaStreamSynchronize(s));    // the old graph may still be running
+      GPT_CUDA(cudaGraphExecDestroy(m->dec_exec));
+      m->dec_exec = nullptr;
+    }
+    if (!m->cap_stream) GPT_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+    GPT_CUDA(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    m->launches = 0;
+    const int rc = decode_bf16(m, m->stage_ids, B, m->dec_pos, d_logits, m->cap_stream);
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
+    if (rc != GPT_OK) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    GPT_CUDA(e);
+    const cudaError_t ei = cudaGraphInstantiate(&m->dec_exec, g, 0);
+    cudaGraphDestroy(g);
+    GPT_CUDA(ei);
+    m->dec_B = B;
+    m->dec_logits = d_logits;
+    m->dec_launches = m->launches;
+  }
+  GPT_CUDA(cudaGraphLaunch(m->dec_exec, s));
+  m->launches = m->dec_launches + 1;
+  return GPT_OK;
 }
 
 int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_stop) {

@@ -54,43 +54,81 @@ __device__ __forceinline__ float gelu_dec(float x, int erf_form) {
 }
 
 // out[r, n] = epilogue(sum_k a[r, k] W[n, k] (+ bias[n])) for rows r < M <= MR.
-// One warp per column n: lane i reads W[n, 8i + 256j .. +8] (the warp covers
-// 512 contiguous bytes per step) and the same columns of every row of a
-// (L1-resident: all warps of the grid read the same few rows). K % 8 == 0.
-template <int EPI, int MR>
+// SPLIT warps share a column n: the 16-byte chunks c of W's row n (K / 8 of
+// them) are dealt c = part * 32 + lane + i * 32 * SPLIT, so every warp load
+// covers 512 contiguous bytes, and up to four loads per lane are in flight
+// before the arithmetic. The rows of a are L1-resident (all warps of the grid
+// read the same few rows). The SPLIT partial sums meet in shared memory in a
+// fixed order. K % 8 == 0.
+template <int EPI, int MR, int SPLIT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* __restrict__ W,
             const float* __restrict__ bias, void* out, int ldo, int M, int N, int K, int gelu_erf) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float red[kGemvWarps][MR];
   const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
-  if (n >= N) return;
-  const __nv_bfloat16* wr = W + (size_t)n * K;
+  const int warp = threadIdx.x >> 5;
+  const int part = warp % SPLIT;
+  const int n = blockIdx.x * (kGemvWarps / SPLIT) + warp / SPLIT;
+  const bool live = n < N;                                   // the block's barrier below needs every warp
+  const __nv_bfloat16* wr = W + (size_t)(live ? n : 0) * K;
+  const int chunks = K / 8;
   float acc[MR];
 #pragma unroll
   for (int r = 0; r < MR; ++r) acc[r] = 0.0f;
-  for (int k = lane * 8; k < K; k += 256) {
-    float wf[8];
-    unpack8(ld_stream_u4(wr + k), wf);
+  constexpr int U = 4;                                       // loads in flight per lane
+  for (int c0 = part * 32 + lane; live && c0 < chunks; c0 += U * 32 * SPLIT) {
+    uint4 wv[U];
 #pragma unroll
-    for (int r = 0; r < MR; ++r) {
-      if (r < M) {
-        float af[8];
-        unpack8(*reinterpret_cast<const uint4*>(a + (size_t)r * lda + k), af);
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 32 * SPLIT;
+      wv[u] = c < chunks ? ld_stream_u4(wr + 8 * c) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[r] = fmaf(af[i], wf[i], acc[r]);
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 32 * SPLIT;
+      if (c >= chunks) break;
+      float wf[8];
+      unpack8(wv[u], wf);
+#pragma unroll
+      for (int r = 0; r < MR; ++r) {
+        if (r < M) {
+          float af[8];
+          unpack8(*reinterpret_cast<const uint4*>(a + (size_t)r * lda + 8 * c), af);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[r] = fmaf(af[i], wf[i], acc[r]);
+        }
       }
     }
   }
-  float mine = 0.0f;                           // lane r keeps row r's total
 #pragma unroll
   for (int r = 0; r < MR; ++r) {
     float v = acc[r];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == r) mine = v;
+    acc[r] = v;
   }
+  if (SPLIT > 1) {
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < MR; ++r) red[warp][r] = acc[r];
+    }
+    __syncthreads();
+    if (part != 0) return;
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+      float v = 0.0f;
+#pragma unroll
+      for (int q = 0; q < SPLIT; ++q) v += red[warp + q][r];
+      acc[r] = v;
+    }
+  }
+  if (!live) return;
+  float mine = 0.0f;                                         // lane r keeps row r's total
+#pragma unroll
+  for (int r = 0; r < MR; ++r)
+    if (lane == r) mine = acc[r];
   if (lane >= M) return;
   const int r = lane;
   if (bias != nullptr) mine += __ldg(bias + n);
@@ -112,9 +150,10 @@ gemv_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* _
 template <int D>
 __global__ void __launch_bounds__(kAttnDecThreads)
 attn_decode_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* cache, __nv_bfloat16* __restrict__ y,
-                   int H, int C, int ctx, int pos, float scale_log2) {
+                   int H, int C, int ctx, const int* __restrict__ pos_dev, float scale_log2) {
   pdl_wait();
   pdl_trigger();
+  const int pos = *pos_dev;
   __shared__ float s_m[kAttnDecThreads];
   __shared__ float s_l[kAttnDecThreads];
   __shared__ float s_o[D][kAttnDecThreads + 1];
@@ -205,17 +244,36 @@ kv_store_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict
   }
 }
 
-template <int EPI>
-cudaError_t gemv_dispatch(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, const float* bias, void* out,
-                          int ldo, int M, int N, int K, int gelu_erf, cudaStream_t s) {
-  const dim3 grid((N + kGemvWarps - 1) / kGemvWarps), block(kGemvWarps * 32);
-#define GPT_GEMV(MRV) return launch_k(gemv_kernel<EPI, MRV>, grid, block, 0, s, a, lda, W, bias, out, ldo, M, N, K, gelu_erf)
+__global__ void set_int_kernel(int* p, int v) { *p = v; }
+
+template <int EPI, int SPLIT>
+cudaError_t gemv_rows(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, const float* bias, void* out,
+                      int ldo, int M, int N, int K, int gelu_erf, cudaStream_t s) {
+  const dim3 grid((N + kGemvWarps / SPLIT - 1) / (kGemvWarps / SPLIT)), block(kGemvWarps * 32);
+#define GPT_GEMV(MRV) \
+  return launch_k(gemv_kernel<EPI, MRV, SPLIT>, grid, block, 0, s, a, lda, W, bias, out, ldo, M, N, K, gelu_erf)
   if (M <= 1) GPT_GEMV(1);
   if (M <= 2) GPT_GEMV(2);
   if (M <= 4) GPT_GEMV(4);
   if (M <= 8) GPT_GEMV(8);
   GPT_GEMV(16);
 #undef GPT_GEMV
+}
+
+// Warps per column: enough warps in the grid (about 2048) to keep loads in flight on
+// every SM when N is small, but not more than the 512-byte rows of a weight row.
+template <int EPI>
+cudaError_t gemv_dispatch(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, const float* bias, void* out,
+                          int ldo, int M, int N, int K, int gelu_erf, cudaStream_t s) {
+  const int rows512 = (K / 8 + 31) / 32;
+  int split = 1;
+  while (split < 8 && N * split < 2048 && split * 2 <= rows512) split *= 2;
+  switch (split) {
+    case 1: return gemv_rows<EPI, 1>(a, lda, W, bias, out, ldo, M, N, K, gelu_erf, s);
+    case 2: return gemv_rows<EPI, 2>(a, lda, W, bias, out, ldo, M, N, K, gelu_erf, s);
+    case 4: return gemv_rows<EPI, 4>(a, lda, W, bias, out, ldo, M, N, K, gelu_erf, s);
+    default: return gemv_rows<EPI, 8>(a, lda, W, bias, out, ldo, M, N, K, gelu_erf, s);
+  }
 }
 
 }  // namespace
@@ -247,22 +305,27 @@ cudaError_t launch_gemv(const void* a, int lda, const void* W, const float* bias
   return cudaSuccess;
 }
 
-cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y, int B, int H, int D, int ctx, int pos,
-                                    cudaStream_t s) {
+cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y, int B, int H, int D, int ctx,
+                                    const int* pos_dev, cudaStream_t s) {
   if (B <= 0) return cudaSuccess;
-  if (pos < 0 || pos >= ctx) return cudaErrorInvalidValue;
+  if (pos_dev == nullptr) return cudaErrorInvalidValue;
   const int C = H * D;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   const auto* q = reinterpret_cast<const __nv_bfloat16*>(qkv);
   auto* c = reinterpret_cast<__nv_bfloat16*>(cache_layer);
   auto* yo = reinterpret_cast<__nv_bfloat16*>(y);
   if (D == 64)
-    return launch_k(attn_decode_kernel<64>, dim3(B * H), dim3(kAttnDecThreads), 0, s, q, c, yo, H, C, ctx, pos,
+    return launch_k(attn_decode_kernel<64>, dim3(B * H), dim3(kAttnDecThreads), 0, s, q, c, yo, H, C, ctx, pos_dev,
                     scale_log2);
   if (D == 32)
-    return launch_k(attn_decode_kernel<32>, dim3(B * H), dim3(kAttnDecThreads), 0, s, q, c, yo, H, C, ctx, pos,
+    return launch_k(attn_decode_kernel<32>, dim3(B * H), dim3(kAttnDecThreads), 0, s, q, c, yo, H, C, ctx, pos_dev,
                     scale_log2);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
+  set_int_kernel<<<1, 1, 0, s>>>(p, v);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_store(const void* qkv, void* cache_layer, int B, int T, int C, int ctx, cudaStream_t s) {

@@ -110,7 +110,8 @@ template <int NV, typename WT, typename OT>
 __global__ void __launch_bounds__(kRowThreads)
 embed_kernel(const int32_t* __restrict__ ids, const WT* __restrict__ wte, const WT* __restrict__ wpe,
              float* __restrict__ x, OT* __restrict__ out, int out_mode, const float* __restrict__ g,
-             const float* __restrict__ b, int M, int T, int C, int V, float eps, int* err, int pos0) {
+             const float* __restrict__ b, int M, int T, int C, int V, float eps, int* err, int pos0,
+             const int* __restrict__ pos_dev) {
   pdl_wait();
   pdl_trigger();
   const int warp = (blockIdx.x * kRowThreads + threadIdx.x) >> 5;
@@ -121,7 +122,7 @@ embed_kernel(const int32_t* __restrict__ ids, const WT* __restrict__ wte, const 
     if (lane == 0) record_error(err, GPT_DEV_ETOKEN);
     id = 0;                                   // keep the row defined; the call reports the error
   }
-  const int t = pos0 + warp % T;
+  const int t = (pos_dev != nullptr ? *pos_dev : pos0) + warp % T;
   const WT* erow = wte + (size_t)id * C;
   const WT* prow = wpe + (size_t)t * C;
   float* xrow = x + (size_t)warp * C;
@@ -164,11 +165,11 @@ layernorm_kernel(const float* x, const float* __restrict__ g, const float* __res
 template <typename WT, typename OT>
 cudaError_t embed_dispatch(const int32_t* ids, const WT* wte, const WT* wpe, float* x, OT* out, int out_mode,
                            const float* g, const float* b, int M, int T, int C, int V, float eps, int* err,
-                           cudaStream_t s, int pos0) {
+                           cudaStream_t s, int pos0, const int* pos_dev) {
   const int blocks = (M + 7) / 8;
   const int nv = (C + 255) / 256;
   cudaError_t e = cudaSuccess;
-#define GPT_EMB(NVV) e = launch_k(embed_kernel<NVV, WT, OT>, dim3(blocks), dim3(kRowThreads), 0, s, ids, wte, wpe, x, out, out_mode, g, b, M, T, C, V, eps, err, pos0)
+#define GPT_EMB(NVV) e = launch_k(embed_kernel<NVV, WT, OT>, dim3(blocks), dim3(kRowThreads), 0, s, ids, wte, wpe, x, out, out_mode, g, b, M, T, C, V, eps, err, pos0, pos_dev)
   switch (nv) {
     case 1: GPT_EMB(1); break;
     case 2: GPT_EMB(2); break;
@@ -299,20 +300,20 @@ __global__ void __launch_bounds__(32) mean_kernel(const float* __restrict__ part
 
 cudaError_t launch_embed(const int32_t* ids, const void* wte, const void* wpe, int wdt, float* x, void* out,
                          int out_mode, int odt, const float* g, const float* b, int M, int T, int C, int V,
-                         float eps, int* err, cudaStream_t s, int pos0) {
+                         float eps, int* err, cudaStream_t s, int pos0, const int* pos_dev) {
   if (M <= 0) return cudaSuccess;
   if (wdt == 1) {
     const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(wte);
     const __nv_bfloat16* P = reinterpret_cast<const __nv_bfloat16*>(wpe);
     if (odt == 1)
-      return embed_dispatch(ids, E, P, x, reinterpret_cast<__nv_bfloat16*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0);
-    return embed_dispatch(ids, E, P, x, reinterpret_cast<float*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0);
+      return embed_dispatch(ids, E, P, x, reinterpret_cast<__nv_bfloat16*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0, pos_dev);
+    return embed_dispatch(ids, E, P, x, reinterpret_cast<float*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0, pos_dev);
   }
   const float* E = reinterpret_cast<const float*>(wte);
   const float* P = reinterpret_cast<const float*>(wpe);
   if (odt == 1)
-    return embed_dispatch(ids, E, P, x, reinterpret_cast<__nv_bfloat16*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0);
-  return embed_dispatch(ids, E, P, x, reinterpret_cast<float*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0);
+    return embed_dispatch(ids, E, P, x, reinterpret_cast<__nv_bfloat16*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0, pos_dev);
+  return embed_dispatch(ids, E, P, x, reinterpret_cast<float*>(out), out_mode, g, b, M, T, C, V, eps, err, s, pos0, pos_dev);
 }
 
 cudaError_t launch_layernorm(const float* x, const float* g, const float* b, void* out, int odt, float* out_f32,

@@ -66,10 +66,11 @@ cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T
                                 int* err, cudaStream_t s);
 
 // ---- row-wise kernels (both paths)
-// Row m is token m of its sequence at position pos0 + m % T.
+// Row m is token m of its sequence at position pos0 + m % T (pos0 read from pos_dev when non-null).
 cudaError_t launch_embed(const int32_t* ids, const void* wte, const void* wpe, int wdt, float* x,
                          void* out, int out_mode, int odt, const float* g, const float* b,
-                         int M, int T, int C, int V, float eps, int* err, cudaStream_t s, int pos0 = 0);
+                         int M, int T, int C, int V, float eps, int* err, cudaStream_t s, int pos0 = 0,
+                         const int* pos_dev = nullptr);
 cudaError_t launch_layernorm(const float* x, const float* g, const float* b, void* out, int odt,
                              float* out_f32, int M, int C, float eps, cudaStream_t s);
 // nll per row from the head's partials; block_sums (nullable) receives one sum of
@@ -106,10 +107,13 @@ constexpr int kGemvMaxRows = 16;       // rows per matrix-vector launch
 // W: bf16 [N, K] with K % 8 == 0; epi as for the GEMMs: bf16 out, bf16 GELU out, fp32 +=, fp32 out).
 cudaError_t launch_gemv(const void* a, int lda, const void* W, const float* bias, void* out, int ldo, int M, int N,
                         int K, int epi, int gelu_erf, cudaStream_t s);
-// The new tokens' attention at position pos: stores each one's key and value (from qkv [B, 3C])
-// in the layer's cache [batch][ctx][2C] at pos, then y[b] = softmax over keys 0..pos.
-cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y, int B, int H, int D, int ctx, int pos,
-                                    cudaStream_t s);
+// The new tokens' attention at position pos = *pos_dev (0 <= pos < ctx, checked by the caller):
+// stores each one's key and value (from qkv [B, 3C]) in the layer's cache [batch][ctx][2C] at pos,
+// then y[b] = softmax over keys 0..pos.
+cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y, int B, int H, int D, int ctx,
+                                    const int* pos_dev, cudaStream_t s);
+// *p = v (the decode position, written on the stream before a captured decode step runs).
+cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
 // cache[b][t][0:2C] = qkv[b, t][C:3C] for a prompt of T tokens.
 cudaError_t launch_kv_store(const void* qkv, void* cache_layer, int B, int T, int C, int ctx, cudaStream_t s);
 

@@ -44,6 +44,12 @@ struct gpt_model {
   uint8_t* kv = nullptr;
   int kv_batch = 0;
   bool kv_fill = false;         // the next bf16 forward also stores keys and values (prefill)
+  int* dec_pos = nullptr;       // device int: the position of the decode step being run
+  cudaStream_t cap_stream = nullptr;   // where a decode step is captured into a CUDA graph
+  cudaGraphExec_t dec_exec = nullptr;  // the captured decode step, for dec_B rows into dec_logits
+  int dec_B = 0;
+  float* dec_logits = nullptr;
+  int dec_launches = 0;
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;

@@ -162,6 +162,7 @@ int gpt_last_probe_hits(const gpt_model* m);
  * gpt_kv_reserve: allocate (or grow) the model-owned cache for up to
  * max_batch sequences of ctx tokens: L x max_batch x ctx x 2C bf16
  * (604 MB for GPT-2 small at 16 sequences). Synchronous; GPT_ENOMEM on failure.
+ * Growing the cache discards the rows it held.
  */
 int gpt_kv_reserve(gpt_model* m, int32_t max_batch);
 
@@ -183,6 +184,9 @@ int gpt_prefill(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t T, float*
  * equal to row pos of a full forward over the sequence. Requires
  * 0 <= pos < ctx (GPT_ESEQ) and B <= the reserved batch (GPT_EINVAL).
  * Stream-ordered and asynchronous; bad ids are reported by gpt_status().
+ * The step's kernels are captured into a CUDA graph on the first call for a
+ * given (B, d_logits) and replayed afterwards (the ids and the position are
+ * read from model memory); GPT_GB300_NO_GRAPH=1 launches them directly.
  */
 int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, float* d_logits, void* stream);
 
