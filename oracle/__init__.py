@@ -9,11 +9,11 @@ the ``workloads`` package.
 from .gpt_oracle import (
     param_count, linear, layernorm, gelu, embed, attention_probs,
     causal_self_attention, block_pre_norm, block_post_norm, forward_hidden,
-    lm_head, cross_entropy_rows, cross_entropy, forward,
+    lm_head, cross_entropy_rows, cross_entropy, forward, sample_next,
 )
 
 __all__ = [
     "param_count", "linear", "layernorm", "gelu", "embed", "attention_probs",
     "causal_self_attention", "block_pre_norm", "block_post_norm", "forward_hidden",
-    "lm_head", "cross_entropy_rows", "cross_entropy", "forward",
+    "lm_head", "cross_entropy_rows", "cross_entropy", "forward", "sample_next",
 ]

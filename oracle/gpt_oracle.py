@@ -205,3 +205,52 @@ def forward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets=None):
     logits = lm_head(forward_hidden(cfg, w, ids), w["wte"])
     loss = None if targets is None else cross_entropy(logits, targets)
     return loss, logits
+
+
+def sample_next(logits: np.ndarray, temperature: float, top_k: int, top_p: float, u: float):
+    """Next token of one row of logits: (index, kept probabilities in index order).
+
+    "预训练一个 Mini GPT", 第7步 文本生成: probabilities are softmax(logits / T)
+    and the token is drawn from them (the draw takes the first index whose
+    cumulative probability, in index order, exceeds the uniform number u);
+    temperature 0 is greedy decoding (the most probable token; here the lowest
+    index among equal maxima). "02 GPT 架构", 8.1-8.3: top-k keeps the k most
+    probable tokens; top-p sorts by probability from high to low and keeps the
+    smallest leading set whose probabilities add up to p. Readings: top-k is
+    applied first, top-p to the renormalised top-k distribution; equal
+    probabilities are ordered by index (lower first); the kept set is
+    renormalised before the draw; top_k <= 0 or >= V and top_p <= 0 or >= 1
+    mean no filter.
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    V = z.shape[0]
+    if temperature <= 0:
+        return int(np.argmax(z)), None            # argmax returns the first maximum
+    z = z / temperature
+    p = np.exp(z - z.max())
+    p = p / p.sum()
+    # rank tokens by probability, high to low, lower index first among equals
+    order = sorted(range(V), key=lambda i: (-p[i], i))
+    keep = np.zeros(V, dtype=bool)
+    kcount = V if (top_k <= 0 or top_k >= V) else top_k
+    for i in order[:kcount]:
+        keep[i] = True
+    if 0 < top_p < 1:
+        mass = sum(p[i] for i in order[:kcount])
+        acc = 0.0
+        nucleus = np.zeros(V, dtype=bool)
+        for i in order[:kcount]:
+            nucleus[i] = True
+            acc += p[i]
+            if acc >= top_p * mass:
+                break
+        keep = nucleus
+    q = np.where(keep, p, 0.0)
+    q = q / q.sum()
+    cdf = 0.0
+    for i in range(V):
+        cdf += q[i]
+        if cdf > u:
+            return i, q
+    last = int(np.nonzero(keep)[0][-1])           # u at the very top: the last kept token
+    return last, q

@@ -427,3 +427,48 @@ def test_planted_mistakes_are_caught(mistake, monkeypatch):
     elif mistake == "head_bias":
         monkeypatch.setattr(go, "lm_head", lambda h, wte: orig_head(h, wte) + 0.01)
     assert not _pins_pass(), f"planted mistake {mistake} went unnoticed"
+
+
+# ---- next-token sampling ("预训练一个 Mini GPT" 第7步; "02 GPT 架构" 8.1-8.3)
+
+def test_sample_greedy_is_argmax():
+    rng = np.random.default_rng(3)
+    z = rng.standard_normal(1000)
+    for u in (0.0, 0.5, 0.999):
+        assert go.sample_next(z, 0.0, 0, 1.0, u)[0] == int(np.argmax(z))
+        assert go.sample_next(z, 1.3, 1, 1.0, u)[0] == int(np.argmax(z))      # top-k = 1
+        assert go.sample_next(z, 0.7, 0, 1e-9, u)[0] == int(np.argmax(z))     # a nucleus of one token
+
+
+def test_sample_plain_is_inverse_cdf():
+    # no filter: the draw is the inverse CDF of softmax(z / T) in index order (np.random.choice's rule)
+    rng = np.random.default_rng(4)
+    z = rng.standard_normal(300) * 2
+    T = 0.8
+    p = np.exp(z / T - np.max(z / T))
+    p /= p.sum()
+    cdf = np.cumsum(p)
+    for u in rng.random(50):
+        assert go.sample_next(z, T, 0, 1.0, u)[0] == int(np.searchsorted(cdf, u, side="right"))
+
+
+def test_sample_worked_nucleus_and_top_k():
+    # p = (0.5, 0.3, 0.2): top-p 0.75 keeps tokens 0 and 1 (0.5 < 0.75 <= 0.8), renormalised to
+    # (0.625, 0.375); top-k 2 keeps the same two
+    z = np.log(np.array([0.5, 0.3, 0.2]))
+    for kw in (dict(top_k=0, top_p=0.75), dict(top_k=2, top_p=1.0)):
+        i0, q = go.sample_next(z, 1.0, kw["top_k"], kw["top_p"], 0.6)
+        assert i0 == 0 and np.allclose(q, [0.625, 0.375, 0.0])
+        assert go.sample_next(z, 1.0, kw["top_k"], kw["top_p"], 0.7)[0] == 1
+    # top-p 0.85 needs all three (0.8 < 0.85)
+    assert go.sample_next(z, 1.0, 0, 0.85, 0.95)[0] == 2
+
+
+def test_sample_ties_and_temperature():
+    z = np.array([2.0, 2.0, 1.0])
+    assert go.sample_next(z, 1.0, 1, 1.0, 0.99)[0] == 0          # equal maxima: the lower index
+    assert go.sample_next(z, 0.0, 0, 1.0, 0.99)[0] == 0
+    # a very high temperature flattens the distribution: CDF (0.25, 0.5, 0.75, 1)
+    z4 = np.array([0.3, -1.0, 2.0, 0.5])
+    assert go.sample_next(z4, 1e9, 0, 1.0, 0.5)[0] == 2
+    assert go.sample_next(z4, 1e9, 0, 1.0, 0.49)[0] == 1
