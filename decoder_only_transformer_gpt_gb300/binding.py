@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH):
         "gpt_kv_reserve": (ctypes.c_int, [vp, i32]),
         "gpt_prefill": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
         "gpt_decode_step": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
+        "gpt_sample": (ctypes.c_int, [vp, i32, i32, ctypes.c_float, i32, ctypes.c_float, vp, vp, vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
@@ -207,6 +208,14 @@ class GPTModel:
 
 
 # ---------------------------------------------------------------- per-step entries
+
+def sample(logits, uniform, ids_out, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0, stream=None):
+    """Next-token ids [B] from logits [B, V] (device tensors); uniform [B] in [0, 1) from the caller."""
+    lib = load()
+    B, V = logits.shape
+    _check(lib.gpt_sample(_ptr(logits), B, V, temperature, top_k, top_p, _ptr(uniform), _ptr(ids_out),
+                          _stream(stream)), "gpt_sample")
+
 
 def gemm(A, W, bias, out, epilogue: int, stream=None):
     lib = load()

@@ -389,6 +389,15 @@ int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, 
   return GPT_OK;
 }
 
+int gpt_sample(const float* d_logits, int32_t B, int32_t V, float temperature, int32_t top_k, float top_p,
+               const float* d_uniform, int32_t* d_ids, void* stream) {
+  if (!d_logits || !d_ids || B < 1 || V < 1 || V > kSampleMaxV) return GPT_EINVAL;
+  if (temperature > 0.0f && !d_uniform) return GPT_EINVAL;
+  GPT_CUDA(launch_sample(d_logits, B, V, temperature, top_k, top_p, d_uniform, d_ids,
+                         reinterpret_cast<cudaStream_t>(stream)));
+  return GPT_OK;
+}
+
 int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_stop) {
   if (!m) return GPT_EINVAL;
   if (!ev_start) {

@@ -246,6 +246,226 @@ kv_store_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict
 
 __global__ void set_int_kernel(int* p, int v) { *p = v; }
 
+// ---------------------------------------------------------------- sampling
+
+constexpr int kSampThreads = 1024;
+
+// Block-wide sum (fixed order: lanes, then warps), result in every thread.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();                                   // scratch free from the previous use
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+  for (int w = 0; w < kSampThreads / 32; ++w) t += scratch[w];
+  return t;
+}
+
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float t = -INFINITY;
+  for (int w = 0; w < kSampThreads / 32; ++w) t = fmaxf(t, scratch[w]);
+  return t;
+}
+
+// Exclusive prefix sum over threads (thread order = index order: each thread owns a
+// contiguous chunk of the row), and the total.
+__device__ __forceinline__ int block_scan_int(int v, int* scan, int& total) {
+  __syncthreads();
+  scan[threadIdx.x] = v;
+  __syncthreads();
+  for (int off = 1; off < kSampThreads; off <<= 1) {   // Hillis-Steele
+    const int add = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+    __syncthreads();
+    scan[threadIdx.x] += add;
+    __syncthreads();
+  }
+  total = scan[kSampThreads - 1];
+  return scan[threadIdx.x] - v;
+}
+
+__device__ __forceinline__ float block_scan_float(float v, float* scan, float& total) {
+  __syncthreads();
+  scan[threadIdx.x] = v;
+  __syncthreads();
+  for (int off = 1; off < kSampThreads; off <<= 1) {
+    const float add = threadIdx.x >= off ? scan[threadIdx.x - off] : 0.0f;
+    __syncthreads();
+    scan[threadIdx.x] += add;
+    __syncthreads();
+  }
+  total = scan[kSampThreads - 1];
+  return scan[threadIdx.x] - v;
+}
+
+// One row per block: temperature, top-k, top-p and the inverse-CDF draw in index
+// order ("预训练一个 Mini GPT" 第7步; "02 GPT 架构" 8.1-8.3). The probabilities of
+// the row live in shared memory; thread t owns indices [t * chunk, (t + 1) * chunk),
+// so per-thread counts and sums scanned over threads follow index order. Ranking
+// among equal probabilities is by index, lower first.
+__global__ void __launch_bounds__(kSampThreads)
+sample_kernel(const float* __restrict__ logits, int V, float temperature, int top_k, float top_p,
+              const float* __restrict__ uniform, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float sp[];                      // [V] probabilities, then scratch
+  float* red = sp + V;                               // [32]
+  float* fscan = red + 32;                           // [kSampThreads]
+  int* iscan = reinterpret_cast<int*>(fscan + kSampThreads);
+  const float* z = logits + (size_t)blockIdx.x * V;
+  const int chunk = (V + kSampThreads - 1) / kSampThreads;
+  const int i0 = threadIdx.x * chunk;
+  const int i1 = min(V, i0 + chunk);
+  if (temperature <= 0.0f) {                         // greedy: the first maximum
+    float best = -INFINITY;
+    int bi = V;
+    for (int i = i0; i < i1; ++i)
+      if (z[i] > best) { best = z[i]; bi = i; }
+    const float gm = block_max(best, red);
+    int cand = (best == gm) ? bi : V;                // the lowest index holding the maximum
+    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) iscan[threadIdx.x >> 5] = cand;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int r = V;
+      for (int w = 0; w < kSampThreads / 32; ++w) r = min(r, iscan[w]);
+      out[blockIdx.x] = r;
+    }
+    return;
+  }
+  const float inv_t = 1.0f / temperature;
+  float lm = -INFINITY;
+  for (int i = i0; i < i1; ++i) {
+    const float v = z[i] * inv_t;
+    sp[i] = v;
+    lm = fmaxf(lm, v);
+  }
+  const float zmax = block_max(lm, red);
+  float ls = 0.0f;
+  for (int i = i0; i < i1; ++i) {
+    const float e = expf(sp[i] - zmax);
+    sp[i] = e;                                       // unnormalised: every filter is scale-free
+    ls += e;
+  }
+  float mass = block_sum(ls, red);
+  // ---- top-k: the k-th largest value by a radix select on the bits (p >= 0: bit order = value order)
+  if (top_k > 0 && top_k < V) {
+    unsigned prefix = 0u, mask = 0u;
+    int remaining = top_k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      __syncthreads();
+      for (int d = threadIdx.x; d < 256; d += kSampThreads) iscan[d] = 0;
+      __syncthreads();
+      for (int i = i0; i < i1; ++i) {
+        const unsigned b = __float_as_uint(sp[i]);
+        if ((b & mask) == prefix) atomicAdd(&iscan[(b >> shift) & 0xffu], 1);
+      }
+      __syncthreads();
+      int d = 255, above = 0;
+      while (d > 0 && above + iscan[d] < remaining) { above += iscan[d]; --d; }
+      remaining -= above;                            // elements still needed among digit d
+      prefix |= static_cast<unsigned>(d) << shift;
+      mask |= 0xffu << shift;
+    }
+    // keep bits > prefix, and the first `remaining` elements equal to it in index order
+    int ties = 0;
+    for (int i = i0; i < i1; ++i) ties += __float_as_uint(sp[i]) == prefix;
+    int total_ties;
+    int rank = block_scan_int(ties, iscan, total_ties);
+    float kept = 0.0f;
+    for (int i = i0; i < i1; ++i) {
+      const unsigned b = __float_as_uint(sp[i]);
+      bool keep = b > prefix;
+      if (b == prefix) keep = rank++ < remaining;
+      if (!keep) sp[i] = 0.0f;
+      kept += sp[i];
+    }
+    mass = block_sum(kept, red);
+  }
+  // ---- top-p: the smallest leading set (by value, then index) whose mass reaches top_p of the total
+  if (top_p > 0.0f && top_p < 1.0f) {
+    const float target = top_p * mass;
+    unsigned v = 0u;                                 // largest v with mass(p >= v) >= target
+    for (int bit = 30; bit >= 0; --bit) {
+      const unsigned cand = v | (1u << bit);
+      float part = 0.0f;
+      for (int i = i0; i < i1; ++i)
+        if (__float_as_uint(sp[i]) >= cand) part += sp[i];
+      if (block_sum(part, red) >= target) v = cand;
+    }
+    float gt = 0.0f;
+    int ties = 0;
+    for (int i = i0; i < i1; ++i) {
+      const unsigned b = __float_as_uint(sp[i]);
+      if (b > v) gt += sp[i];
+      ties += b == v;
+    }
+    const float mass_gt = block_sum(gt, red);
+    const float pv = __uint_as_float(v);
+    int total_ties;
+    int rank = block_scan_int(ties, iscan, total_ties);
+    // equal values added in index order until the target is reached (at least one, at most all)
+    int need = total_ties;
+    if (pv > 0.0f) {
+      const float n = ceilf((target - mass_gt) / pv);
+      need = n < 1.0f ? 1 : (n > static_cast<float>(total_ties) ? total_ties : static_cast<int>(n));
+    }
+    float kept = 0.0f;
+    for (int i = i0; i < i1; ++i) {
+      const unsigned b = __float_as_uint(sp[i]);
+      bool keep = b > v;
+      if (b == v && pv > 0.0f) keep = rank++ < need;
+      if (!keep) sp[i] = 0.0f;
+      kept += sp[i];
+    }
+    mass = block_sum(kept, red);
+  }
+  // ---- the draw: first index whose cumulative kept mass exceeds u * mass
+  float mine = 0.0f;
+  for (int i = i0; i < i1; ++i) mine += sp[i];
+  float tot;
+  const float before = block_scan_float(mine, fscan, tot);
+  const float thr = uniform[blockIdx.x] * tot;
+  int last = -1;                                     // the last kept index of this chunk
+  for (int i = i0; i < i1; ++i)
+    if (sp[i] > 0.0f) last = i;
+  int found = V;
+  if (before <= thr && before + mine > thr) {        // the crossing lies in this chunk
+    float acc = before;
+    for (int i = i0; i < i1; ++i) {
+      acc += sp[i];
+      if (acc > thr && sp[i] > 0.0f) { found = i; break; }
+    }
+    if (found == V) found = last;                    // rounding between the two summation orders
+  }
+  __syncthreads();
+  int cand = found;
+  for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  int lmax = last;
+  for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  if ((threadIdx.x & 31) == 0) {
+    iscan[threadIdx.x >> 5] = cand;
+    iscan[32 + (threadIdx.x >> 5)] = lmax;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int r = V, lk = -1;
+    for (int w = 0; w < kSampThreads / 32; ++w) {
+      r = min(r, iscan[w]);
+      lk = max(lk, iscan[32 + w]);
+    }
+    out[blockIdx.x] = r < V ? r : lk;
+  }
+}
+
 template <int EPI, int SPLIT>
 cudaError_t gemv_rows(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, const float* bias, void* out,
                       int ldo, int M, int N, int K, int gelu_erf, cudaStream_t s) {
@@ -326,6 +546,22 @@ cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y,
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
   set_int_kernel<<<1, 1, 0, s>>>(p, v);
   return cudaGetLastError();
+}
+
+cudaError_t launch_sample(const float* logits, int B, int V, float temperature, int top_k, float top_p,
+                          const float* uniform, int32_t* out, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  if (V <= 0 || V > kSampleMaxV) return cudaErrorInvalidValue;
+  const size_t smem = (static_cast<size_t>(V) + 32 + 2 * kSampThreads) * 4;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>((kSampleMaxV + 32 + 2 * kSampThreads) * 4));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_k(sample_kernel, dim3(B), dim3(kSampThreads), smem, s, logits, V, temperature, top_k, top_p, uniform,
+                  out);
 }
 
 cudaError_t launch_kv_store(const void* qkv, void* cache_layer, int B, int T, int C, int ctx, cudaStream_t s) {

@@ -114,6 +114,11 @@ cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y,
                                     const int* pos_dev, cudaStream_t s);
 // *p = v (the decode position, written on the stream before a captured decode step runs).
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
+// Next-token draw per row of logits [B, V] fp32 (temperature <= 0: greedy; top_k / top_p
+// filters; uniform[b] in [0, 1)); V <= kSampleMaxV (the row's probabilities sit in shared memory).
+constexpr int kSampleMaxV = 55296;
+cudaError_t launch_sample(const float* logits, int B, int V, float temperature, int top_k, float top_p,
+                          const float* uniform, int32_t* out, cudaStream_t s);
 // cache[b][t][0:2C] = qkv[b, t][C:3C] for a prompt of T tokens.
 cudaError_t launch_kv_store(const void* qkv, void* cache_layer, int B, int T, int C, int ctx, cudaStream_t s);
 

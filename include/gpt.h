@@ -190,6 +190,22 @@ int gpt_prefill(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t T, float*
  */
 int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, float* d_logits, void* stream);
 
+/*
+ * Next-token draw for each row of d_logits [B, V] (device fp32, row stride V)
+ * ("预训练一个 Mini GPT" 第7步 text generation; "02 GPT 架构" 8.1-8.3):
+ * temperature <= 0 is greedy (the most probable token, the lowest index among
+ * equal maxima); otherwise probabilities softmax(logits / temperature), then
+ * top_k (> 0 and < V: keep the k most probable), then top_p (in (0, 1): keep
+ * the smallest leading set, by probability then index, whose mass reaches
+ * top_p of the kept mass), renormalise, and take the first index (in index
+ * order) whose cumulative probability exceeds d_uniform[b] (device fp32 [B],
+ * values in [0, 1), drawn by the caller). Writes d_ids [B] (device int32).
+ * Requires 1 <= V <= 55296 (the row's probabilities are held on chip).
+ * Stream-ordered and asynchronous; model-independent.
+ */
+int gpt_sample(const float* d_logits, int32_t B, int32_t V, float temperature, int32_t top_k, float top_p,
+               const float* d_uniform, int32_t* d_ids, void* stream);
+
 /* Synchronise the stream, read and clear the model's device error word. */
 int gpt_status(gpt_model* m, void* stream);
 
