@@ -26,7 +26,7 @@ namespace gptgb {
 namespace {
 
 constexpr int kGemvWarps = 8;                 // output columns per block
-constexpr int kAttnDecThreads = 128;
+constexpr int kAttnDecWarps = 8;
 
 __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
   float2 t;
@@ -64,8 +64,6 @@ template <int EPI, int MR, int SPLIT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* __restrict__ W,
             const float* __restrict__ bias, void* out, int ldo, int M, int N, int K, int gelu_erf) {
-  pdl_wait();
-  pdl_trigger();
   __shared__ float red[kGemvWarps][MR];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -78,11 +76,24 @@ gemv_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* _
 #pragma unroll
   for (int r = 0; r < MR; ++r) acc[r] = 0.0f;
   constexpr int U = 4;                                       // loads in flight per lane
-  for (int c0 = part * 32 + lane; live && c0 < chunks; c0 += U * 32 * SPLIT) {
-    uint4 wv[U];
+  constexpr int STEP = U * 32 * SPLIT;
+  // The weights do not depend on the previous kernel: the first loads are issued before
+  // waiting for it, so their latency overlaps its tail.
+  int c0 = part * 32 + lane;
+  uint4 wv[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int c = c0 + u * 32 * SPLIT;
+    wv[u] = (live && c < chunks) ? ld_stream_u4(wr + 8 * c) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+  pdl_trigger();
+  for (; live && c0 < chunks; c0 += STEP) {
+    uint4 cur[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * 32 * SPLIT;
+      cur[u] = wv[u];
+      const int c = c0 + STEP + u * 32 * SPLIT;              // the next batch, in flight during this one
       wv[u] = c < chunks ? ld_stream_u4(wr + 8 * c) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
@@ -90,7 +101,7 @@ gemv_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* _
       const int c = c0 + u * 32 * SPLIT;
       if (c >= chunks) break;
       float wf[8];
-      unpack8(wv[u], wf);
+      unpack8(cur[u], wf);
 #pragma unroll
       for (int r = 0; r < MR; ++r) {
         if (r < M) {
@@ -143,86 +154,109 @@ gemv_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* _
   }
 }
 
-// One (sequence b, head h) per block. The new token's key and value (from its
-// qkv row) are first stored in the cache at position pos; then every thread
-// takes keys j = tid, tid + 128, ... <= pos with its own running (max, sum,
-// output) in base 2, and the block merges the 128 partial results.
+// One (sequence b, head h) per block of kAttnDecWarps warps. The new token's key
+// and value (from its qkv row) are first stored in the cache at position pos;
+// then warp w takes the 32-key chunks w, w + kAttnDecWarps, ... of keys 0..pos:
+// lane i scores key 32c + i against q (shared memory), the warp turns the
+// chunk's scores into probabilities against its running max (base 2), and each
+// lane accumulates its D/32 output columns over the chunk's 32 value rows (each
+// row read by the whole warp: 128 contiguous bytes at D = 64). The warps' partial
+// results are merged in a fixed order.
 template <int D>
-__global__ void __launch_bounds__(kAttnDecThreads)
+__global__ void __launch_bounds__(kAttnDecWarps * 32)
 attn_decode_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* cache, __nv_bfloat16* __restrict__ y,
                    int H, int C, int ctx, const int* __restrict__ pos_dev, float scale_log2) {
+  constexpr int DL = D / 32;                                       // output columns per lane
+  constexpr int V8 = D / 8;                                        // 16-byte chunks per head slice
+  __shared__ float s_q[D];
+  __shared__ float s_m[kAttnDecWarps], s_l[kAttnDecWarps];
+  __shared__ float s_o[kAttnDecWarps][D];
   pdl_wait();
   pdl_trigger();
   const int pos = *pos_dev;
-  __shared__ float s_m[kAttnDecThreads];
-  __shared__ float s_l[kAttnDecThreads];
-  __shared__ float s_o[D][kAttnDecThreads + 1];
   const int b = blockIdx.x / H, h = blockIdx.x % H;
-  const int tid = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const __nv_bfloat16* qrow = qkv + (size_t)b * 3 * C;
   __nv_bfloat16* cb = cache + (size_t)b * ctx * 2 * C;             // this sequence's rows
-  constexpr int V8 = D / 8;                                        // 16-byte chunks per head slice
-  if (tid < 2 * V8) {                                              // key chunks, then value chunks
-    const int part = tid / V8, c8 = tid % V8;
+  if (threadIdx.x < 2 * V8) {                                      // key chunks, then value chunks
+    const int part = threadIdx.x / V8, c8 = threadIdx.x % V8;
     const uint4 v = *reinterpret_cast<const uint4*>(qrow + (1 + part) * C + h * D + 8 * c8);
     *reinterpret_cast<uint4*>(cb + (size_t)pos * 2 * C + part * C + h * D + 8 * c8) = v;
   }
-  __syncthreads();                                                 // the new row is visible to the block
-  float q[D];
+  if (threadIdx.x < D) s_q[threadIdx.x] = __bfloat162float(qrow[h * D + threadIdx.x]) * scale_log2;
+  __syncthreads();                                                 // the new row and q are visible
+  float m = -INFINITY, l = 0.0f, o[DL];
 #pragma unroll
-  for (int c8 = 0; c8 < V8; ++c8) {
-    float f[8];
-    unpack8(*reinterpret_cast<const uint4*>(qrow + h * D + 8 * c8), f);
+  for (int d = 0; d < DL; ++d) o[d] = 0.0f;
+  for (int c = warp; c * 32 <= pos; c += kAttnDecWarps) {
+    const int j = c * 32 + lane;
+    float sc = -INFINITY;
+    if (j <= pos) {
+      const __nv_bfloat16* kr = cb + (size_t)j * 2 * C + h * D;
+      uint4 kv[V8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[8 * c8 + i] = f[i] * scale_log2;
+      for (int c8 = 0; c8 < V8; ++c8) kv[c8] = *reinterpret_cast<const uint4*>(kr + 8 * c8);
+      sc = 0.0f;
+#pragma unroll
+      for (int c8 = 0; c8 < V8; ++c8) {
+        float f[8];
+        unpack8(kv[c8], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc = fmaf(s_q[8 * c8 + i], f[i], sc);
+      }
+    }
+    float cm = sc;                                                 // the chunk's maximum
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    const float mn = fmaxf(m, cm);                                 // finite: key 32c <= pos exists
+    const float alpha = ex2_approx(m - mn);                        // 0 on the first chunk
+    const float p = ex2_approx(sc - mn);                           // 0 past pos
+    float ps = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l = l * alpha + ps;
+#pragma unroll
+    for (int d = 0; d < DL; ++d) o[d] *= alpha;
+    m = mn;
+    const int nk = min(32, pos + 1 - c * 32);                      // valid keys of this chunk
+    const __nv_bfloat16* vb = cb + (size_t)(c * 32) * 2 * C + C + h * D + lane * DL;
+    // all of the chunk's value loads first (32 in flight per lane), then the sums
+    uint32_t vv[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const __nv_bfloat16* vr = vb + (size_t)jj * 2 * C;
+      if (DL == 2) vv[jj] = jj < nk ? *reinterpret_cast<const uint32_t*>(vr) : 0u;
+      else vv[jj] = jj < nk ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(vr)) : 0u;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);             // 0 for keys past pos
+      if (DL == 2) {
+        const float2 v2 = unpack_bf16x2(vv[jj]);
+        o[0] = fmaf(pj, v2.x, o[0]);
+        o[DL - 1] = fmaf(pj, v2.y, o[DL - 1]);
+      } else {
+        o[0] = fmaf(pj, unpack_bf16x2(vv[jj]).x, o[0]);               // the low half holds the value
+      }
+    }
   }
-  float m = -INFINITY, l = 0.0f, o[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) o[d] = 0.0f;
-  for (int j = tid; j <= pos; j += kAttnDecThreads) {
-    const __nv_bfloat16* kr = cb + (size_t)j * 2 * C + h * D;
-    float sc = 0.0f;
-#pragma unroll
-    for (int c8 = 0; c8 < V8; ++c8) {
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(kr + 8 * c8), f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sc = fmaf(q[8 * c8 + i], f[i], sc);
-    }
-    if (sc > m) {                                                  // raise the running max
-      const float alpha = ex2_approx(m - sc);                      // 0 for the first key
-      l *= alpha;
-#pragma unroll
-      for (int d = 0; d < D; ++d) o[d] *= alpha;
-      m = sc;
-    }
-    const float p = ex2_approx(sc - m);
-    l += p;
-    const __nv_bfloat16* vr = kr + C;
-#pragma unroll
-    for (int c8 = 0; c8 < V8; ++c8) {
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(vr + 8 * c8), f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[8 * c8 + i] = fmaf(p, f[i], o[8 * c8 + i]);
-    }
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
   }
-  s_m[tid] = m;
-  __syncthreads();
-  float gm = -INFINITY;                                            // key 0 is always present: finite
-  for (int t = 0; t < kAttnDecThreads; ++t) gm = fmaxf(gm, s_m[t]);
-  const float w = (m == -INFINITY) ? 0.0f : ex2_approx(m - gm);  // threads without keys add nothing
-  s_l[tid] = l * w;
 #pragma unroll
-  for (int d = 0; d < D; ++d) s_o[d][tid] = o[d] * w;
+  for (int d = 0; d < DL; ++d) s_o[warp][lane * DL + d] = o[d];
   __syncthreads();
-  if (tid < D) {
+  if (threadIdx.x < D) {
+    float gm = -INFINITY;
+    for (int w = 0; w < kAttnDecWarps; ++w) gm = fmaxf(gm, s_m[w]);
     float num = 0.0f, den = 0.0f;
-    for (int t = 0; t < kAttnDecThreads; ++t) {                    // fixed order: deterministic
-      num += s_o[tid][t];
-      den += s_l[t];
+    for (int w = 0; w < kAttnDecWarps; ++w) {                      // fixed order: deterministic
+      const float sw = (s_m[w] == -INFINITY) ? 0.0f : ex2_approx(s_m[w] - gm);   // warps without keys add 0
+      num = fmaf(sw, s_o[w][threadIdx.x], num);
+      den = fmaf(sw, s_l[w], den);
     }
-    y[(size_t)b * C + h * D + tid] = __float2bfloat16_rn(num / den);
+    y[(size_t)b * C + h * D + threadIdx.x] = __float2bfloat16_rn(num / den);
   }
 }
 
@@ -466,6 +500,84 @@ sample_kernel(const float* __restrict__ logits, int V, float temperature, int to
   }
 }
 
+// 5..16 rows: the rows are the 16-row A operand of mma.sync m16n8k16 (bf16 in,
+// fp32 accumulate). Block = one 8-column tile of out; its 8 warps split K into
+// contiguous ranges of whole 16-wide steps, and their 16 x 8 partial tiles are
+// summed in shared memory in warp order. Fragment layout of m16n8k16: lane =
+// 4 g + t holds A (g, 2t..2t+1), (g+8, ..), (g, 2t+8..), (g+8, 2t+8..);
+// B (k = 2t..2t+1 and 2t+8.., n = g); C (g, 2t..2t+1) and (g+8, 2t..2t+1).
+__device__ __forceinline__ uint32_t ld_u32_or0(const __nv_bfloat16* p, bool ok) {
+  return ok ? *reinterpret_cast<const uint32_t*>(p) : 0u;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemvWarps * 32)
+gemv_mma_kernel(const __nv_bfloat16* __restrict__ a, int lda, const __nv_bfloat16* __restrict__ W,
+                const float* __restrict__ bias, void* out, int ldo, int M, int N, int K, int gelu_erf) {
+  __shared__ float red[kGemvWarps][16][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int n0 = blockIdx.x * 8;
+  const int n = n0 + g;                                       // this lane's B column
+  const bool ncol = n < N;
+  const int steps = K / 16;                                   // whole 16-wide K steps (K % 16 == 0)
+  const int per = (steps + kGemvWarps - 1) / kGemvWarps;
+  const int s0 = warp * per, s1 = min(steps, s0 + per);
+  const __nv_bfloat16* wr = W + (size_t)(ncol ? n : 0) * K;
+  // the weights do not depend on the previous kernel: the first step's B is loaded before the wait
+  uint32_t b0 = 0u, b1 = 0u;
+  if (s0 < s1) {
+    b0 = ld_u32_or0(wr + s0 * 16 + 2 * t, ncol);
+    b1 = ld_u32_or0(wr + s0 * 16 + 2 * t + 8, ncol);
+  }
+  pdl_wait();
+  pdl_trigger();
+  float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+  const bool r0 = g < M, r1 = g + 8 < M;
+  for (int st = s0; st < s1; ++st) {
+    const int k = st * 16 + 2 * t;
+    uint32_t nb0 = 0u, nb1 = 0u;
+    if (st + 1 < s1) {                                        // next step's weights in flight
+      nb0 = ld_u32_or0(wr + k + 16, ncol);
+      nb1 = ld_u32_or0(wr + k + 24, ncol);
+    }
+    const uint32_t a0 = ld_u32_or0(a + (size_t)g * lda + k, r0);
+    const uint32_t a1 = ld_u32_or0(a + (size_t)(g + 8) * lda + k, r1);
+    const uint32_t a2 = ld_u32_or0(a + (size_t)g * lda + k + 8, r0);
+    const uint32_t a3 = ld_u32_or0(a + (size_t)(g + 8) * lda + k + 8, r1);
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    b0 = nb0;
+    b1 = nb1;
+  }
+  red[warp][g][2 * t] = c0;
+  red[warp][g][2 * t + 1] = c1;
+  red[warp][g + 8][2 * t] = c2;
+  red[warp][g + 8][2 * t + 1] = c3;
+  __syncthreads();
+  for (int e = threadIdx.x; e < 16 * 8; e += kGemvWarps * 32) {
+    const int r = e >> 3, cn = e & 7;
+    const int col = n0 + cn;
+    if (r >= M || col >= N) continue;
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kGemvWarps; ++w) v += red[w][r][cn];   // fixed order
+    if (bias != nullptr) v += __ldg(bias + col);
+    if (EPI == EPI_BIAS_OUT) {
+      reinterpret_cast<__nv_bfloat16*>(out)[(size_t)r * ldo + col] = __float2bfloat16_rn(v);
+    } else if (EPI == EPI_BIAS_GELU_OUT) {
+      reinterpret_cast<__nv_bfloat16*>(out)[(size_t)r * ldo + col] = __float2bfloat16_rn(gelu_dec(v, gelu_erf));
+    } else if (EPI == EPI_BIAS_RESID) {
+      reinterpret_cast<float*>(out)[(size_t)r * ldo + col] += v;
+    } else {
+      reinterpret_cast<float*>(out)[(size_t)r * ldo + col] = v;
+    }
+  }
+}
+
 template <int EPI, int SPLIT>
 cudaError_t gemv_rows(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, const float* bias, void* out,
                       int ldo, int M, int N, int K, int gelu_erf, cudaStream_t s) {
@@ -485,6 +597,9 @@ cudaError_t gemv_rows(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, c
 template <int EPI>
 cudaError_t gemv_dispatch(const __nv_bfloat16* a, int lda, const __nv_bfloat16* W, const float* bias, void* out,
                           int ldo, int M, int N, int K, int gelu_erf, cudaStream_t s) {
+  if (M > 4 && K % 16 == 0)                                    // 5..16 rows: tensor-core tiles
+    return launch_k(gemv_mma_kernel<EPI>, dim3((N + 7) / 8), dim3(kGemvWarps * 32), 0, s, a, lda, W, bias, out, ldo,
+                    M, N, K, gelu_erf);
   const int rows512 = (K / 8 + 31) / 32;
   int split = 1;
   while (split < 8 && N * split < 2048 && split * 2 <= rows512) split *= 2;
@@ -535,10 +650,10 @@ cudaError_t launch_attention_decode(const void* qkv, void* cache_layer, void* y,
   auto* c = reinterpret_cast<__nv_bfloat16*>(cache_layer);
   auto* yo = reinterpret_cast<__nv_bfloat16*>(y);
   if (D == 64)
-    return launch_k(attn_decode_kernel<64>, dim3(B * H), dim3(kAttnDecThreads), 0, s, q, c, yo, H, C, ctx, pos_dev,
+    return launch_k(attn_decode_kernel<64>, dim3(B * H), dim3(kAttnDecWarps * 32), 0, s, q, c, yo, H, C, ctx, pos_dev,
                     scale_log2);
   if (D == 32)
-    return launch_k(attn_decode_kernel<32>, dim3(B * H), dim3(kAttnDecThreads), 0, s, q, c, yo, H, C, ctx, pos_dev,
+    return launch_k(attn_decode_kernel<32>, dim3(B * H), dim3(kAttnDecWarps * 32), 0, s, q, c, yo, H, C, ctx, pos_dev,
                     scale_log2);
   return cudaErrorInvalidValue;
 }

@@ -62,9 +62,11 @@ def test_decode_head_width_32_and_many_rows(gpt_lib):
     _decode_case(cfg, w, ids, 1, 39)                     # a one-token prompt, then up to the last position
 
 
-def test_decode_gpt2_small(gpt_lib):
+@pytest.mark.parametrize("B", [2, 6])
+def test_decode_gpt2_small(gpt_lib, B):
+    # 2 rows: SIMT matrix-vector products; 6 rows: the mma.sync tiles (rows 6..15 of the tile empty)
     wl = workload("gpt2_small")
-    w, ids, _ = generate(wl, B=2, T=160)
+    w, ids, _ = generate(wl, B=B, T=160)
     _decode_case(wl.cfg, w, ids, 150, 10)
 
 
