@@ -218,6 +218,18 @@ def cpu_baseline(wl, w, ids, tg, budget_s: float = 12.0):
             "seconds": spent}
 
 
+def replica_rate(ms_local: float, units_local: float, world: int, device):
+    """Independent replicas (weak scaling): the job's time is the slowest rank's, and its rate is
+    every rank's units over that time. Collective: every rank must call it."""
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, units_local * world / (ms_max / 1e3)
+
+
 def run_reference(args, rank, world):
     """--impl reference: the oracle timed on host cores (rank 0 only)."""
     if rank != 0:
@@ -325,12 +337,7 @@ def run_ours(args, rank, world, local_rank):
     ms = start.elapsed_time(stop)
     lib.gpt_time_step(model.handle, -1, -1, None, None)
     dom_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    tokens = B * T * args.steps * world
-    value = tokens / (ms_max / 1e3)
+    ms_max, value = replica_rate(ms, B * T * args.steps, world, dev)
 
     # e2e: the host-buffer C-ABI call (H2D of ids and targets, D2H of the loss and
     # the status word inside every step), timed on the host clock
@@ -344,10 +351,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.steps):
         model.forward_host_ptrs(pin_ids.data_ptr(), pin_tg.data_ptr(), B, T, pin_loss.data_ptr())
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = tokens / float(te.item())
+    _, e2e_value = replica_rate(1e3 * e2e_s, B * T * args.steps, world, dev)
 
     if rank != 0:
         model.close()
