@@ -9,7 +9,7 @@ section. The computation is the definition written out in numpy float64 with
 no online softmax. Inputs (weights stored as fp32, bf16-representable on bf16
 workloads) are upcast exactly to fp64.
 
-Readings where the pages are silent or disagree (each is listed in the design doc):
+Readings where the pages are silent or disagree:
   * LayerNorm uses the biased variance with eps inside the square root.
   * GELU is the tanh approximation unless the erf form is asked for.
   * Q, K and U are the first, second and third C-wide thirds of c_attn's
