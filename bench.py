@@ -218,6 +218,41 @@ def cpu_baseline(wl, w, ids, tg, budget_s: float = 12.0):
             "seconds": spent}
 
 
+class RuntimeEvents:
+    """CUDA events from the CUDA runtime library itself (ctypes), for the timing probe of the timed
+    region: the library replays one captured forward per step and points its two event-record nodes
+    at each step's events, which the driver accepts for these events (not for torch's)."""
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.rt = None
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                self.rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.rt is None:
+            raise RuntimeError("libcudart not found for the timing events")
+
+    def create(self) -> int:
+        h = self.ct.c_void_p()
+        if self.rt.cudaEventCreate(self.ct.byref(h)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        return h.value
+
+    def elapsed_ms(self, a: int, b: int) -> float:
+        ms = self.ct.c_float()
+        rc = self.rt.cudaEventElapsedTime(self.ct.byref(ms), self.ct.c_void_p(a), self.ct.c_void_p(b))
+        if rc != 0:
+            raise RuntimeError(f"cudaEventElapsedTime failed ({rc})")
+        return float(ms.value)
+
+    def destroy(self, h: int) -> None:
+        self.rt.cudaEventDestroy(self.ct.c_void_p(h))
+
+
 def replica_rate(ms_local: float, units_local: float, world: int, device):
     """Independent replicas (weak scaling): the job's time is the slowest rank's, and its rate is
     every rank's units over that time. Collective: every rank must call it."""
@@ -291,18 +326,17 @@ def run_ours(args, rank, world, local_rank):
     launches_per_step = lib.gpt_last_launch_count(model.handle)
 
     # per-step breakdown (untimed): every launch of one forward bracketed by events, one probe per forward
-    pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pa.record(stream)             # torch creates the CUDA event on first record; the library re-records it
-    pb.record(stream)
+    rte = RuntimeEvents()
+    pa, pb = rte.create(), rte.create()
     breakdown = {}
     for name, sid, per_block in STEP_KINDS:
         times = []
         for layer in (range(cfg.L) if per_block else [-1]):
-            lib.gpt_time_step(model.handle, sid, layer, pa.cuda_event, pb.cuda_event)
+            lib.gpt_time_step(model.handle, sid, layer, pa, pb)
             model.forward(ids, tg, loss, None, check=False)
             torch.cuda.synchronize()
             if lib.gpt_last_probe_hits(model.handle) == 1:
-                times.append(pa.elapsed_time(pb))
+                times.append(rte.elapsed_ms(pa, pb))
         if not times:                 # the step did not run in this configuration
             continue
         work, bound = step_work(name, cfg, B, T)
@@ -312,11 +346,16 @@ def run_ours(args, rank, world, local_rank):
     dom = max(breakdown, key=lambda k: breakdown[k]["ms_per_step"])
     dom_sid, dom_per_block = next((sid, pb_) for n, sid, pb_ in STEP_KINDS if n == dom)
 
-    # timed region: K steps, one launch of the dominant step in each bracketed by events
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for e in ev0 + ev1:
-        e.record(stream)
+    # timed region: K steps, one launch of the dominant step in each bracketed by events (the same
+    # block's launch every step, so the library replays one captured graph whose two event-record
+    # nodes it points at each step's events)
+    ev0 = [rte.create() for _ in range(args.steps)]
+    ev1 = [rte.create() for _ in range(args.steps)]
+    dom_layer = (cfg.L // 2) if dom_per_block else -1
+    for k in range(2):                # untimed: capture (and replay once) the probed forward
+        lib.gpt_time_step(model.handle, dom_sid, dom_layer, ev0[k], ev1[k])
+        model.forward(ids, tg, loss, None, check=False)
+    torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
@@ -326,8 +365,7 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)
     start.record(stream)
     for k in range(args.steps):
-        lib.gpt_time_step(model.handle, dom_sid, (k % cfg.L) if dom_per_block else -1,
-                          ev0[k].cuda_event, ev1[k].cuda_event)
+        lib.gpt_time_step(model.handle, dom_sid, dom_layer, ev0[k], ev1[k])
         model.forward(ids, tg, loss, None, check=False)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -336,7 +374,9 @@ def run_ours(args, rank, world, local_rank):
     model.status()
     ms = start.elapsed_time(stop)
     lib.gpt_time_step(model.handle, -1, -1, None, None)
-    dom_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    dom_ms = [rte.elapsed_ms(a, b) for a, b in zip(ev0, ev1)]
+    for h in ev0 + ev1 + [pa, pb]:
+        rte.destroy(h)
     ms_max, value = replica_rate(ms, B * T * args.steps, world, dev)
 
     # e2e: the host-buffer C-ABI call (H2D of ids and targets, D2H of the loss and

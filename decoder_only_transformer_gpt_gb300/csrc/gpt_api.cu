@@ -100,6 +100,8 @@ void free_model(gpt_model* m) {
   cudaFree(m->kv);
   cudaFree(m->dec_pos);
   if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);
+  if (m->fwd_exec) cudaGraphExecDestroy(m->fwd_exec);
+  if (m->fwd_graph) cudaGraphDestroy(m->fwd_graph);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   cudaFreeHost(m->h_pinned);
   delete m;

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <vector>
 
 using namespace gptgb;
 
@@ -37,14 +38,20 @@ bool probe_hit(const gpt_model* m, int step, int layer) {
 }
 
 // One step = one kernel launch, optionally bracketed by the armed probe events.
+// An armed probe's events around one step. Inside a graph capture the records become event-record
+// nodes (external events), outside it they are plain records.
 #define GPT_STEP(step, layer, expr)                                                 \
   do {                                                                              \
     const bool hit_ = probe_hit(m, (step), (layer));                                \
-    if (hit_) cudaEventRecord(m->prof_ev0, s);                                      \
+    const unsigned fl_ = m->capturing ? cudaEventRecordExternal : cudaEventRecordDefault; \
+    if (hit_) GPT_CUDA(cudaEventRecordWithFlags(m->prof_ev0, s, fl_));              \
     const int rc_ = (expr);                                                         \
     if (rc_ != GPT_OK) return rc_;                                                  \
     ++m->launches;                                                                  \
-    if (hit_) { cudaEventRecord(m->prof_ev1, s); ++m->probe_hits; }                 \
+    if (hit_) {                                                                     \
+      GPT_CUDA(cudaEventRecordWithFlags(m->prof_ev1, s, fl_));                      \
+      ++m->probe_hits;                                                              \
+    }                                                                               \
   } while (0)
 
 int ensure_act_maps(gpt_model* m, int B, int T) {
@@ -237,9 +244,9 @@ int check_shape(const gpt_model* m, int B, int T) {
   return GPT_OK;
 }
 
-// Decode steps are captured once into a CUDA graph and replayed (GPT_GB300_NO_GRAPH=1: launched
-// directly each step); the results are the same either way.
-bool decode_graphs_enabled() {
+// Forward passes and decode steps are captured into CUDA graphs and replayed (GPT_GB300_NO_GRAPH=1:
+// launched directly each time); the results are the same either way.
+bool graphs_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("GPT_GB300_NO_GRAPH");
     return !(v && v[0] == '1');
@@ -295,6 +302,101 @@ int decode_bf16(gpt_model* m, const int32_t* ids, int B, const int* pos_dev, flo
   return GPT_OK;
 }
 
+// Point an event-record node of an executable graph at another event, through the driver entry
+// point. The driver refuses this for some callers' events (those of a framework's own copy of the
+// runtime, seen with PyTorch's); the caller then captures the forward again with the new events.
+cudaError_t graph_exec_set_event(cudaGraphExec_t exec, cudaGraphNode_t node, cudaEvent_t ev) {
+  using Fn = CUresult (*)(CUgraphExec, CUgraphNode, CUevent);
+  static Fn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuGraphExecEventRecordNodeSetEvent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<Fn>(p);
+  }();
+  if (!fn) return cudaErrorNotSupported;
+  return fn(reinterpret_cast<CUgraphExec>(exec), reinterpret_cast<CUgraphNode>(node), reinterpret_cast<CUevent>(ev)) ==
+                 CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+// gpt_forward on the bf16 path through a CUDA graph: captured on the first call for a set of
+// (pointers, B, T, armed probe) and replayed while they repeat. An armed probe's events are
+// event-record nodes of the graph; a replay points them at the probe's current events.
+int forward_graphed(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss,
+                    float* d_logits, cudaStream_t s) {
+  const bool probe = m->prof_ev0 != nullptr;
+  const void* key[8] = {ids, tg, d_loss, d_logits, reinterpret_cast<const void*>(static_cast<intptr_t>(B)),
+                        reinterpret_cast<const void*>(static_cast<intptr_t>(T)),
+                        reinterpret_cast<const void*>(static_cast<intptr_t>(probe ? m->prof_step : -1)),
+                        reinterpret_cast<const void*>(static_cast<intptr_t>(probe ? m->prof_layer : -2))};
+  bool same = m->fwd_exec != nullptr;
+  for (int i = 0; i < 8 && same; ++i) same = m->fwd_key[i] == key[i];
+  if (same && probe && m->fwd_ev_node[0] && m->fwd_ev_node[1]) {
+    // point the captured event-record nodes at this call's events; events the driver does not
+    // accept there (some runtimes' own) mean a fresh capture with them instead
+    same = graph_exec_set_event(m->fwd_exec, m->fwd_ev_node[0], m->prof_ev0) == cudaSuccess &&
+           graph_exec_set_event(m->fwd_exec, m->fwd_ev_node[1], m->prof_ev1) == cudaSuccess;
+  }
+  if (!same) {
+    if (m->fwd_exec) {
+      GPT_CUDA(cudaStreamSynchronize(s));    // the old graph may still be running
+      GPT_CUDA(cudaGraphExecDestroy(m->fwd_exec));
+      m->fwd_exec = nullptr;
+    }
+    if (m->fwd_graph) {
+      cudaGraphDestroy(m->fwd_graph);
+      m->fwd_graph = nullptr;
+    }
+    if (!m->cap_stream) GPT_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+    GPT_CUDA(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    m->launches = 0;
+    m->probe_hits = 0;
+    m->capturing = true;
+    const int rc = forward_bf16(m, ids, tg, B, T, d_loss, d_logits, m->cap_stream);
+    m->capturing = false;
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
+    if (rc != GPT_OK) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    GPT_CUDA(e);
+    m->fwd_ev_node[0] = m->fwd_ev_node[1] = nullptr;
+    if (m->probe_hits > 0) {                 // find the probe's two event-record nodes
+      size_t n = 0;
+      GPT_CUDA(cudaGraphGetNodes(g, nullptr, &n));
+      std::vector<cudaGraphNode_t> nodes(n);
+      GPT_CUDA(cudaGraphGetNodes(g, nodes.data(), &n));
+      for (cudaGraphNode_t nd : nodes) {
+        cudaGraphNodeType ty;
+        GPT_CUDA(cudaGraphNodeGetType(nd, &ty));
+        if (ty != cudaGraphNodeTypeEventRecord) continue;
+        cudaEvent_t ev = nullptr;
+        GPT_CUDA(cudaGraphEventRecordNodeGetEvent(nd, &ev));
+        if (ev == m->prof_ev0) m->fwd_ev_node[0] = nd;
+        if (ev == m->prof_ev1) m->fwd_ev_node[1] = nd;
+      }
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&m->fwd_exec, g, 0);
+    if (ei != cudaSuccess) {
+      cudaGraphDestroy(g);
+      GPT_CUDA(ei);
+    }
+    m->fwd_graph = g;                        // kept: its nodes name the event-record nodes
+    for (int i = 0; i < 8; ++i) m->fwd_key[i] = key[i];
+    m->fwd_launches = m->launches;
+    m->fwd_probe_hits = m->probe_hits;
+  }
+  GPT_CUDA(cudaGraphLaunch(m->fwd_exec, s));
+  m->launches = m->fwd_launches;
+  m->probe_hits = m->fwd_probe_hits;
+  return GPT_OK;
+}
+
 int map_device_error(int code) {
   switch (code) {
     case GPT_DEV_OK: return GPT_OK;
@@ -316,8 +418,11 @@ int gpt_forward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, in
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   m->launches = 0;
   m->probe_hits = 0;
-  rc = m->bf16 ? forward_bf16(m, d_ids, d_targets, B, T, d_loss, d_logits, s)
-               : forward_f32(m, d_ids, d_targets, B, T, d_loss, d_logits, s);
+  if (m->bf16 && graphs_enabled())
+    rc = forward_graphed(m, d_ids, d_targets, B, T, d_loss, d_logits, s);
+  else
+    rc = m->bf16 ? forward_bf16(m, d_ids, d_targets, B, T, d_loss, d_logits, s)
+                 : forward_f32(m, d_ids, d_targets, B, T, d_loss, d_logits, s);
   m->prof_ev0 = m->prof_ev1 = nullptr;       // a probe covers one forward
   m->prof_step = m->prof_layer = -1;
   return rc;
@@ -356,7 +461,7 @@ int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, 
   // the step reads its ids and position from model memory, so one captured graph serves every step
   GPT_CUDA(cudaMemcpyAsync(m->stage_ids, d_ids, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
   GPT_CUDA(launch_set_int(m->dec_pos, pos, s));
-  if (!decode_graphs_enabled()) {
+  if (!graphs_enabled()) {
     m->launches = 1;
     return decode_bf16(m, m->stage_ids, B, m->dec_pos, d_logits, s);
   }
@@ -369,7 +474,9 @@ int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, 
     if (!m->cap_stream) GPT_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
     GPT_CUDA(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
     m->launches = 0;
+    m->capturing = true;
     const int rc = decode_bf16(m, m->stage_ids, B, m->dec_pos, d_logits, m->cap_stream);
+    m->capturing = false;
     cudaGraph_t g = nullptr;
     const cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
     if (rc != GPT_OK) {

@@ -50,6 +50,14 @@ struct gpt_model {
   int dec_B = 0;
   float* dec_logits = nullptr;
   int dec_launches = 0;
+  // the captured forward pass, for one set of arguments and one timing probe (see gpt_forward)
+  cudaGraph_t fwd_graph = nullptr;
+  cudaGraphExec_t fwd_exec = nullptr;
+  const void* fwd_key[8] = {};
+  cudaGraphNode_t fwd_ev_node[2] = {nullptr, nullptr};   // the probe's event-record nodes
+  int fwd_launches = 0;
+  int fwd_probe_hits = 0;
+  bool capturing = false;       // a forward or decode step is being captured into a graph
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;

@@ -107,6 +107,9 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* weights, gpt_model** ou
  * return immediately; device-found errors (token ids, targets, timeouts) are
  * recorded on the device and returned by the next gpt_status(). Calls on one
  * model share its workspace, so they must be ordered on one stream.
+ * bf16 models capture the pass into a CUDA graph on the first call with a
+ * given (pointers, B, T, armed probe) and replay it while those repeat
+ * (GPT_GB300_NO_GRAPH=1 launches the kernels directly; same results).
  */
 int gpt_forward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, int32_t B,
                 int32_t T, float* d_loss, float* d_logits, void* stream);
@@ -140,7 +143,11 @@ enum {
  * (cudaEvent_t) is recorded on the forward's stream just before the kernel of
  * `step` (in block `layer`; ignored for steps outside the blocks) and ev_stop
  * just after it. The probe disarms after that forward. Pass ev_start == NULL
- * to disarm.
+ * to disarm. On the graph-replayed bf16 forward the two records are nodes of
+ * the graph; a later call with the same (step, layer) points them at its own
+ * events when the driver accepts those events for that (events from
+ * cudaEventCreate do; PyTorch's are refused), else it captures the pass again
+ * (correct, but slower by the capture). A failed record returns GPT_ECUDA.
  */
 int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_stop);
 

@@ -225,3 +225,43 @@ def test_errors(gpt_lib):
     loss, _ = m.forward_host(ids, tg)                        # the handle still works
     assert np.isfinite(loss)
     m.close()
+
+
+def test_time_step_probe_through_replayed_graphs(gpt_lib):
+    """The timing probe on the captured forward. The first probed call captures the graph with the
+    probe's event-record nodes; later calls replay it with the nodes pointed at their own events
+    (runtime-created events) or capture it again (PyTorch's events, which the driver does not let
+    a replay retarget). Every call gives the same loss and a timed interval."""
+    import bench
+    from decoder_only_transformer_gpt_gb300 import binding
+    wl = workload("minigpt")
+    w, ids, tg = generate(wl)
+    B, T = ids.shape
+    m = binding.GPTModel(wl.cfg, w, B * T)
+    d_ids, d_tg = dev_i32(ids), dev_i32(tg)
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    rte = bench.RuntimeEvents()
+    losses = []
+    for k in range(6):
+        if k < 3:
+            a, b = rte.create(), rte.create()
+            m.lib.gpt_time_step(m.handle, 5, 1, a, b)                      # c_fc of block 1
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            e1.record()
+            m.lib.gpt_time_step(m.handle, 5, 1, e0.cuda_event, e1.cuda_event)
+        m.forward(d_ids, d_tg, loss, None, check=True)
+        assert m.lib.gpt_last_probe_hits(m.handle) == 1
+        torch.cuda.synchronize()
+        if k < 3:
+            assert rte.elapsed_ms(a, b) > 0.0
+            rte.destroy(a)
+            rte.destroy(b)
+        else:
+            assert e0.elapsed_time(e1) > 0.0
+        losses.append(float(loss.item()))
+    m.forward(d_ids, d_tg, loss, None, check=True)                          # no probe: another graph
+    losses.append(float(loss.item()))
+    assert len(set(losses)) == 1
+    m.close()
