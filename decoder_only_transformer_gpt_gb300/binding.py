@@ -14,6 +14,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgpt_gb300.so")
 
 GPT_OK, GPT_EINVAL, GPT_ECONFIG, GPT_ESEQ, GPT_ETOKEN, GPT_ECUDA, GPT_ENOMEM, GPT_EDEVICE, GPT_EUNSUPPORTED = range(9)
+# parameters of gpt_grad, in the library's order; the per-block ones take a layer index
+GRAD_PARAMS = ("wte", "wpe", "lnf_g", "lnf_b", "ln1_g", "ln1_b", "attn_w", "attn_b", "proj_w", "proj_b",
+               "ln2_g", "ln2_b", "fc_w", "fc_b", "mp_w", "mp_b")
 EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESID, EPI_F32 = range(4)
 
 _fp = ctypes.POINTER(ctypes.c_float)
@@ -77,6 +80,9 @@ def load(path: str = LIB_PATH):
         "gpt_prefill": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
         "gpt_decode_step": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
         "gpt_sample": (ctypes.c_int, [vp, i32, i32, ctypes.c_float, i32, ctypes.c_float, vp, vp, vp]),
+        "gpt_backward": (ctypes.c_int, [vp, vp, vp, i32, i32, vp, vp]),
+        "gpt_grad": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(i64)]),
+        "gpt_grad_copy": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
@@ -191,6 +197,34 @@ class GPTModel:
         """Append ids [B] (device int32) at position pos; logits [B, V] of the next token."""
         _check(self.lib.gpt_decode_step(self.handle, _ptr(ids), ids.shape[0], pos, _ptr(logits), _stream(stream)),
                "gpt_decode_step")
+
+    def backward(self, ids, targets, loss=None, stream=None, check: bool = True) -> None:
+        """Forward, loss and the gradient of every parameter (device int32 ids / targets [B, T])."""
+        B, T = ids.shape
+        _check(self.lib.gpt_backward(self.handle, _ptr(ids), _ptr(targets), B, T, _ptr(loss), _stream(stream)),
+               "gpt_backward")
+        if check:
+            self.status(stream)
+
+    def grad(self, name: str, layer: int = -1, stream=None):
+        """A copy of one parameter's gradient from the last backward, as a device fp32 tensor shaped like it."""
+        import torch
+        param = GRAD_PARAMS.index(name)
+        ptr, n = ctypes.c_void_p(), ctypes.c_int64()
+        _check(self.lib.gpt_grad(self.handle, param, layer, ctypes.byref(ptr), ctypes.byref(n)), "gpt_grad")
+        c = self.cfg
+        shapes = {"wte": (c.V, c.C), "wpe": (c.ctx, c.C), "attn_w": (3 * c.C, c.C), "attn_b": (3 * c.C,),
+                  "proj_w": (c.C, c.C), "fc_w": (c.ffn, c.C), "fc_b": (c.ffn,), "mp_w": (c.C, c.ffn)}
+        out = torch.empty(shapes.get(name, (c.C,)), dtype=torch.float32, device="cuda")
+        assert out.numel() == n.value
+        _check(self.lib.gpt_grad_copy(self.handle, param, layer, _ptr(out), _stream(stream)), "gpt_grad_copy")
+        return out
+
+    def grads(self, stream=None) -> dict:
+        """Every gradient, keyed like the weight dict ("layers" a list of per-block dicts)."""
+        g = {k: self.grad(k, -1, stream) for k in GRAD_PARAMS[:4]}
+        g["layers"] = [{k: self.grad(k, l, stream) for k in GRAD_PARAMS[4:]} for l in range(self.cfg.L)]
+        return g
 
     def status(self, stream=None):
         _check(self.lib.gpt_status(self.handle, _stream(stream)), "gpt_status")

@@ -1,0 +1,505 @@
+// gpt_backward and gpt_grad: the gradient of the mean next-token cross-entropy
+// with respect to every parameter of a bf16 model, the back-propagation step
+// of the training loop in "预训练一个 Mini GPT" (训练循环).
+//
+// Sequence (M = B*T tokens; every product is a tcgen05 GEMM of the form
+// out = A . B^T with both operands K-major, so the activations and weights a
+// product needs along another axis are transposed first):
+//   forward + loss, keeping each block's input x_l (fp32)
+//   head: dz = (softmax(z) - onehot) / M in bf16 straight from the GEMM that
+//         recomputes z = h E^T (the row's log-sum-exp from the forward's loss);
+//         dh = dz E; dE += dz^T h ("第 25 章" §25.4: the tied table's two uses add)
+//   ln_f: dx = LN'(x_L) dh
+//   per block, last to first: recompute the block's activations from x_l
+//         (LN, c_attn, attention, c_proj, LN, c_fc pre- and post-GELU), then
+//         dW_mp += dx^T g, db_mp, dg = dx W_mp, du = dg gelu'(u), dW_fc += du^T a2,
+//         db_fc, da2 = du W_fc, LN2', dW_proj += ds1^T y, db_proj, dy = ds1 W_proj,
+//         attention' -> dqkv, dW_attn += dqkv^T a1, db_attn, da1 = dqkv W_attn, LN1'
+//   embedding: dE[id] += dx_0, dP[t] += dx_0.
+// Weight gradients with few output tiles split K (the token axis) and add their
+// partials with reduce-add stores into the zeroed fp32 gradient.
+#include "model.h"
+
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <vector>
+
+using namespace gptgb;
+
+struct gpt_layer_grad {
+  float *attn_w, *attn_b, *proj_w, *proj_b, *fc_w, *fc_b, *mp_w, *mp_b, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  CUtensorMap tg_attn_w, tg_proj_w, tg_fc_w, tg_mp_w;      // fp32 reduce-add targets
+  void *attn_wT, *proj_wT, *fc_wT, *mp_wT;                  // bf16 transposed weights [in, out]
+  CUtensorMap tb_attn_wT, tb_proj_wT, tb_fc_wT, tb_mp_wT;  // as B operands
+};
+
+struct gpt_train {
+  size_t Mx = 0;                 // token capacity (max_tokens)
+  int Vp = 0;                    // V rounded up to 8 (row stride of dz and E^T)
+  uint8_t* buf = nullptr;        // one allocation for everything below
+  size_t grad_floats = 0;
+  float* gbuf = nullptr;         // all gradients, contiguous
+  float *g_wte = nullptr, *g_wpe = nullptr, *g_lnf_g = nullptr, *g_lnf_b = nullptr;
+  std::vector<gpt_layer_grad> lg;
+  CUtensorMap tg_wte;
+  void* wteT = nullptr;          // [C][Vp] bf16
+  CUtensorMap tb_wteT;
+  bool wT_ready = false;
+  float* xs = nullptr;           // [L][Mx][C] block inputs
+  // recomputed activations
+  void *a1, *qkv, *yb, *a2, *u, *gg;
+  float *s1, *nb, *s2;
+  // gradients of activations
+  float *dx, *da;
+  void *dxb, *dyb, *dqkv, *du;
+  void *dxT, *gT, *duT, *a2T, *yT, *a1T, *dqkvT, *hT;
+  float *lse2, *dsum;
+  void *dz, *dzT;
+  // activation maps, for one (B, T)
+  int mB = -1, mT = -1;
+  CUtensorMap A_dz, A_dzT, A_a1, A_yb, A_a2, A_gg, A_dxT, A_dxb, A_duT, A_du, A_dqkvT, A_dqkv;
+  CUtensorMap B_hT, B_gT, B_a2T, B_yT, B_a1T;
+  CUtensorMap C_dz, C_qkv, C_u, C_gg, C_du, C_dyb, C_s1, C_s2, C_da, C_dx, Q3;
+  int launches = 0;
+};
+
+namespace gptgb {
+void free_train(gpt_model* m) {
+  if (!m || !m->tr) return;
+  cudaFree(m->tr->buf);
+  delete m->tr;
+  m->tr = nullptr;
+}
+}  // namespace gptgb
+
+namespace {
+
+int cu(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return GPT_OK;
+  set_detail(what, e);
+  return GPT_ECUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Bump allocator over one buffer: the first pass sizes it, the second hands out pointers.
+struct Carve {
+  uint8_t* base = nullptr;
+  size_t off = 0;
+  void* take(size_t bytes) {
+    off = align_up(off, 256);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+int alloc_train(gpt_model* m) {
+  const gpt_config& c = m->cfg;
+  const size_t Mx = static_cast<size_t>(c.max_tokens), C = c.C, F = c.ffn, V = c.V, L = c.L, ctx = c.ctx;
+  const size_t Vp = (V + 7) / 8 * 8;
+  gpt_train* t = new gpt_train();
+  t->Mx = Mx;
+  t->Vp = static_cast<int>(Vp);
+  t->lg.resize(L);
+  const size_t per_layer_grad = 3 * C * C + 3 * C + C * C + C + F * C + F + C * F + C + 4 * C;
+  t->grad_floats = V * C + ctx * C + 2 * C + L * per_layer_grad;
+  // sizes, then one allocation
+  auto layout = [&](Carve& cv) {
+    t->gbuf = static_cast<float*>(cv.take(t->grad_floats * 4));
+    t->wteT = cv.take(C * Vp * 2);
+    for (size_t l = 0; l < L; ++l) {
+      gpt_layer_grad& g = t->lg[l];
+      g.attn_wT = cv.take(3 * C * C * 2);
+      g.proj_wT = cv.take(C * C * 2);
+      g.fc_wT = cv.take(F * C * 2);
+      g.mp_wT = cv.take(C * F * 2);
+    }
+    t->xs = static_cast<float*>(cv.take(L * Mx * C * 4));
+    t->a1 = cv.take(Mx * C * 2);
+    t->qkv = cv.take(Mx * 3 * C * 2);
+    t->yb = cv.take(Mx * C * 2);
+    t->a2 = cv.take(Mx * C * 2);
+    t->u = cv.take(Mx * F * 2);
+    t->gg = cv.take(Mx * F * 2);
+    t->s1 = static_cast<float*>(cv.take(Mx * C * 4));
+    t->nb = static_cast<float*>(cv.take(Mx * C * 4));
+    t->s2 = static_cast<float*>(cv.take(Mx * C * 4));
+    t->dx = static_cast<float*>(cv.take(Mx * C * 4));
+    t->da = static_cast<float*>(cv.take(Mx * C * 4));
+    t->dxb = cv.take(Mx * C * 2);
+    t->dyb = cv.take(Mx * C * 2);
+    t->dqkv = cv.take(Mx * 3 * C * 2);
+    t->du = cv.take(Mx * F * 2);
+    t->dxT = cv.take(C * Mx * 2);
+    t->gT = cv.take(F * Mx * 2);
+    t->duT = cv.take(F * Mx * 2);
+    t->a2T = cv.take(C * Mx * 2);
+    t->yT = cv.take(C * Mx * 2);
+    t->a1T = cv.take(C * Mx * 2);
+    t->dqkvT = cv.take(3 * C * Mx * 2);
+    t->hT = cv.take(C * Mx * 2);
+    t->lse2 = static_cast<float*>(cv.take(Mx * c.H * 4));
+    t->dsum = static_cast<float*>(cv.take(Mx * c.H * 4));
+    t->dz = cv.take(Mx * Vp * 2);
+    t->dzT = cv.take(V * Mx * 2);
+  };
+  Carve sizing;
+  layout(sizing);
+  if (cudaMalloc(&t->buf, sizing.off) != cudaSuccess) {
+    cudaGetLastError();
+    delete t;
+    return GPT_ENOMEM;
+  }
+  Carve real;
+  real.base = t->buf;
+  layout(real);
+  // gradient pointers in the order of the weights
+  float* p = t->gbuf;
+  auto take = [&](size_t n) { float* q = p; p += n; return q; };
+  t->g_wte = take(V * C);
+  t->g_wpe = take(ctx * C);
+  t->g_lnf_g = take(C);
+  t->g_lnf_b = take(C);
+  for (size_t l = 0; l < L; ++l) {
+    gpt_layer_grad& g = t->lg[l];
+    g.ln1_g = take(C); g.ln1_b = take(C);
+    g.attn_w = take(3 * C * C); g.attn_b = take(3 * C);
+    g.proj_w = take(C * C); g.proj_b = take(C);
+    g.ln2_g = take(C); g.ln2_b = take(C);
+    g.fc_w = take(F * C); g.fc_b = take(F);
+    g.mp_w = take(C * F); g.mp_b = take(C);
+  }
+  // fixed descriptors: gradient reduce-add targets and transposed weights
+  bool ok = make_tmap_2d(&t->tg_wte, t->g_wte, 4, V, C, 32, kEpiRows) &&
+            make_tmap_2d_bf16(&t->tb_wteT, t->wteT, C, V, gemm_tc_bn(), Vp);
+  for (size_t l = 0; l < L && ok; ++l) {
+    gpt_layer_grad& g = t->lg[l];
+    ok = make_tmap_2d(&g.tg_attn_w, g.attn_w, 4, 3 * C, C, 32, kEpiRows) &&
+         make_tmap_2d(&g.tg_proj_w, g.proj_w, 4, C, C, 32, kEpiRows) &&
+         make_tmap_2d(&g.tg_fc_w, g.fc_w, 4, F, C, 32, kEpiRows) &&
+         make_tmap_2d(&g.tg_mp_w, g.mp_w, 4, C, F, 32, kEpiRows) &&
+         make_tmap_2d_bf16(&g.tb_attn_wT, g.attn_wT, C, 3 * C, gemm_tc_bn()) &&
+         make_tmap_2d_bf16(&g.tb_proj_wT, g.proj_wT, C, C, gemm_tc_bn()) &&
+         make_tmap_2d_bf16(&g.tb_fc_wT, g.fc_wT, C, F, gemm_tc_bn()) &&
+         make_tmap_2d_bf16(&g.tb_mp_wT, g.mp_wT, F, C, gemm_tc_bn());
+  }
+  if (!ok) {
+    cudaFree(t->buf);
+    delete t;
+    set_detail_text("backward tensor map");
+    return GPT_ECUDA;
+  }
+  m->tr = t;
+  return GPT_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// Activation descriptors for one (B, T): A operands (128-row boxes), B operands (256-row
+// boxes), epilogue outputs (bf16 64 x 32 or fp32 32 x 32 boxes) and the attention input.
+int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
+  if (t->mB == B && t->mT == T) return GPT_OK;
+  const gpt_config& c = m->cfg;
+  const uint64_t M = static_cast<uint64_t>(B) * T, C = c.C, F = c.ffn, V = c.V, Vp = t->Vp;
+  const uint32_t BA = kGemmBM, BB = gemm_tc_bn();
+  const bool ok =
+      make_tmap_2d_bf16(&t->A_dz, t->dz, M, V, BA, Vp) && make_tmap_2d_bf16(&t->A_dzT, t->dzT, V, M, BA) &&
+      make_tmap_2d_bf16(&t->A_a1, t->a1, M, C, BA) && make_tmap_2d_bf16(&t->A_yb, t->yb, M, C, BA) &&
+      make_tmap_2d_bf16(&t->A_a2, t->a2, M, C, BA) && make_tmap_2d_bf16(&t->A_gg, t->gg, M, F, BA) &&
+      make_tmap_2d_bf16(&t->A_dxT, t->dxT, C, M, BA) && make_tmap_2d_bf16(&t->A_dxb, t->dxb, M, C, BA) &&
+      make_tmap_2d_bf16(&t->A_duT, t->duT, F, M, BA) && make_tmap_2d_bf16(&t->A_du, t->du, M, F, BA) &&
+      make_tmap_2d_bf16(&t->A_dqkvT, t->dqkvT, 3 * C, M, BA) && make_tmap_2d_bf16(&t->A_dqkv, t->dqkv, M, 3 * C, BA) &&
+      make_tmap_2d_bf16(&t->B_hT, t->hT, C, M, BB) && make_tmap_2d_bf16(&t->B_gT, t->gT, F, M, BB) &&
+      make_tmap_2d_bf16(&t->B_a2T, t->a2T, C, M, BB) && make_tmap_2d_bf16(&t->B_yT, t->yT, C, M, BB) &&
+      make_tmap_2d_bf16(&t->B_a1T, t->a1T, C, M, BB) &&
+      make_tmap_2d(&t->C_dz, t->dz, 2, M, V, 64, kEpiRows, Vp) && make_tmap_2d(&t->C_qkv, t->qkv, 2, M, 3 * C, 64, kEpiRows) &&
+      make_tmap_2d(&t->C_u, t->u, 2, M, F, 64, kEpiRows) && make_tmap_2d(&t->C_gg, t->gg, 2, M, F, 64, kEpiRows) &&
+      make_tmap_2d(&t->C_du, t->du, 2, M, F, 64, kEpiRows) && make_tmap_2d(&t->C_dyb, t->dyb, 2, M, C, 64, kEpiRows) &&
+      make_tmap_2d(&t->C_s1, t->s1, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_s2, t->s2, 4, M, C, 32, kEpiRows) &&
+      make_tmap_2d(&t->C_da, t->da, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_dx, t->dx, 4, M, C, 32, kEpiRows) &&
+      make_tmap_qkv(&t->Q3, t->qkv, B, T, 3 * C, C / c.H);
+  if (!ok) {
+    t->mB = t->mT = -1;
+    set_detail_text("backward activation tensor map");
+    return GPT_ECUDA;
+  }
+  t->mB = B;
+  t->mT = T;
+  return GPT_OK;
+}
+
+// A weight-gradient product: out [N0, N1] fp32 += A [N0, M] . B [N1, M]^T over the M tokens,
+// split along M so that about two units per CTA are in flight.
+int grad_gemm(gpt_model* m, const CUtensorMap& A, const CUtensorMap& Bm, const CUtensorMap& out_map, float* out,
+              int N0, int N1, int M, cudaStream_t s) {
+  GemmArgs a{};
+  a.M = N0; a.N = N1; a.K = M;
+  a.out = out;
+  a.ldo = N1;
+  a.err = m->err;
+  a.m_fastest = (N1 > N0) ? 1 : 0;
+  const int tiles = ((N0 + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(N1);
+  const int KB = (M + kGemmBK - 1) / kGemmBK;
+  int ks = (2 * m->num_sms + tiles - 1) / tiles;
+  if (ks > KB / 4) ks = KB / 4;          // at least 4 K blocks per unit
+  if (ks < 1) ks = 1;
+  a.ksplit = ks;
+  if (ks == 1) {                          // enough tiles: whole tiles (stream-K where it applies)
+    a.sk_part = m->sk_part;
+    a.sk_flag = m->sk_flag;
+  }
+  GPT_CUDA(launch_gemm_tc(A, Bm, out_map, a, EPI_BIAS_RESID, m->num_sms, s));
+  return GPT_OK;
+}
+
+}  // namespace
+
+namespace {
+
+#define BW(expr)                   \
+  do {                             \
+    const int rc_ = (expr);        \
+    if (rc_ != GPT_OK) return rc_; \
+    ++t->launches;                 \
+  } while (0)
+
+// The transposed weights the input-gradient products read (the weights do not change
+// after gpt_create, so once per model).
+int prepare_weights(gpt_model* m, gpt_train* t, cudaStream_t s) {
+  if (t->wT_ready) return GPT_OK;
+  const gpt_config& c = m->cfg;
+  const int C = c.C, F = c.ffn, V = c.V;
+  BW(cu(launch_transpose_bf16(m->wte, V, C, C, t->wteT, t->Vp, s), "transpose wte"));
+  for (int l = 0; l < c.L; ++l) {
+    const gpt_layer_dev& w = m->layers[l];
+    gpt_layer_grad& g = t->lg[l];
+    BW(cu(launch_transpose_bf16(w.attn_w, 3 * C, C, C, g.attn_wT, 3 * C, s), "transpose attn_w"));
+    BW(cu(launch_transpose_bf16(w.proj_w, C, C, C, g.proj_wT, C, s), "transpose proj_w"));
+    BW(cu(launch_transpose_bf16(w.fc_w, F, C, C, g.fc_wT, F, s), "transpose fc_w"));
+    BW(cu(launch_transpose_bf16(w.mp_w, C, F, F, g.mp_wT, C, s), "transpose mp_w"));
+  }
+  t->wT_ready = true;
+  return GPT_OK;
+}
+
+// The head and ln_f: dx = d loss / d x_L (the last block's output) in t->dx.
+int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStream_t s) {
+  const gpt_config& c = m->cfg;
+  const int C = c.C, V = c.V;
+  // dz = (softmax(h E^T) - onehot) / M, bf16 [M, V] (row stride Vp), and its transpose
+  GemmArgs a{};
+  a.M = M; a.N = V; a.K = C;
+  a.out = t->dz;
+  a.ldo = t->Vp;
+  a.targets = tg;
+  a.row_nll = m->nll;
+  a.ztgt = m->ztgt;
+  a.scale = 1.0f / static_cast<float>(M);
+  a.err = m->err;
+  a.m_fastest = 1;
+  a.b_const = 1;                          // the token table
+  BW(cu(launch_gemm_tc(m->tm_a, m->tm_wte, t->C_dz, a, EPI_CE_GRAD, m->num_sms, s), "head grad"));
+  BW(cu(launch_transpose_bf16(t->dz, M, V, t->Vp, t->dzT, M, s), "transpose dz"));
+  BW(cu(launch_transpose_bf16(m->a, M, C, C, t->hT, M, s), "transpose h"));
+  // dE += dz^T h (the head's share of the tied table)
+  BW(grad_gemm(m, t->A_dzT, t->B_hT, t->tg_wte, t->g_wte, V, C, M, s));
+  // dh = dz E (fp32 into da)
+  GPT_CUDA(cudaMemsetAsync(t->da, 0, static_cast<size_t>(M) * C * sizeof(float), s));
+  BW(gemm_bf16(m, t->A_dz, t->tb_wteT, t->C_da, M, C, V, nullptr, t->da, EPI_BIAS_RESID, s));
+  if (c.final_ln) {
+    BW(cu(launch_layernorm_bwd(m->x, m->lnf_g, t->da, t->dx, 0, t->g_lnf_g, t->g_lnf_b, M, C, c.ln_eps, m->num_sms, s),
+          "ln_f backward"));
+  } else {
+    GPT_CUDA(cudaMemcpyAsync(t->dx, t->da, static_cast<size_t>(M) * C * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  }
+  return GPT_OK;
+}
+
+// Block l's activations again, from its saved input x_l.
+int recompute_block(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t s) {
+  const gpt_config& c = m->cfg;
+  const int M = B * T, C = c.C, F = c.ffn;
+  const bool pre = c.norm_mode == 0;
+  const gpt_layer_dev& w = m->layers[l];
+  const float* xl = t->xs + static_cast<size_t>(l) * M * C;
+  if (pre)
+    BW(cu(launch_layernorm(xl, w.ln1_g, w.ln1_b, t->a1, 1, nullptr, M, C, c.ln_eps, s), "ln1"));
+  else
+    BW(cu(launch_cast_transpose(xl, M, C, t->a1, nullptr, 0, s), "cast x"));
+  BW(gemm_bf16(m, t->A_a1, w.tm_attn_w, t->C_qkv, M, 3 * C, C, w.attn_b, t->qkv, EPI_BIAS_OUT, s));
+  BW(cu(launch_attention_tc(t->Q3, t->yb, B, T, c.H, C / c.H, m->err, s), "attention"));
+  GPT_CUDA(cudaMemcpyAsync(t->s1, xl, static_cast<size_t>(M) * C * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  BW(gemm_bf16(m, t->A_yb, w.tm_proj_w, t->C_s1, M, C, C, w.proj_b, t->s1, EPI_BIAS_RESID, s));
+  if (pre)
+    BW(cu(launch_layernorm(t->s1, w.ln2_g, w.ln2_b, t->a2, 1, nullptr, M, C, c.ln_eps, s), "ln2"));
+  else
+    BW(cu(launch_layernorm(t->s1, w.ln1_g, w.ln1_b, t->a2, 1, t->nb, M, C, c.ln_eps, s), "ln1"));
+  BW(gemm_bf16(m, t->A_a2, w.tm_fc_w, t->C_u, M, F, C, w.fc_b, t->u, EPI_BIAS_OUT, s));
+  BW(gemm_bf16(m, t->A_a2, w.tm_fc_w, t->C_gg, M, F, C, w.fc_b, t->gg, EPI_BIAS_GELU_OUT, s));
+  if (!pre) {
+    GPT_CUDA(cudaMemcpyAsync(t->s2, t->nb, static_cast<size_t>(M) * C * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    BW(gemm_bf16(m, t->A_gg, w.tm_mp_w, t->C_s2, M, C, F, w.mp_b, t->s2, EPI_BIAS_RESID, s));
+  }
+  return GPT_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// Block l backward: on entry t->dx = d loss / d (block output), on return d loss / d x_l.
+int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t s) {
+  const gpt_config& c = m->cfg;
+  const int M = B * T, C = c.C, F = c.ffn, H = c.H;
+  const bool pre = c.norm_mode == 0;
+  const float eps = c.ln_eps;
+  const gpt_layer_dev& w = m->layers[l];
+  gpt_layer_grad& g = t->lg[l];
+  const float* xl = t->xs + static_cast<size_t>(l) * M * C;
+  if (!pre)      // x_{l+1} = LN2(s2): d loss / d s2, in place
+    BW(cu(launch_layernorm_bwd(t->s2, w.ln2_g, t->dx, t->dx, 0, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
+  // MLP: s2 = n + g W_mp^T + b_mp, g = gelu(u), u = a2 W_fc^T + b_fc
+  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s), "cast dx"));
+  BW(cu(launch_colsum(t->dx, 0, M, C, C, g.mp_b, m->num_sms, s), "db_mp"));
+  BW(cu(launch_transpose_bf16(t->gg, M, F, F, t->gT, M, s), "transpose g"));
+  BW(grad_gemm(m, t->A_dxT, t->B_gT, g.tg_mp_w, g.mp_w, C, F, M, s));
+  BW(gemm_bf16(m, t->A_dxb, g.tb_mp_wT, t->C_du, M, F, C, nullptr, t->du, EPI_BIAS_OUT, s));      // dg
+  BW(cu(launch_gelu_bwd(t->u, t->du, t->du, static_cast<size_t>(M) * F, c.gelu, m->num_sms, s), "gelu'"));
+  BW(cu(launch_colsum(t->du, 1, M, F, F, g.fc_b, m->num_sms, s), "db_fc"));
+  BW(cu(launch_transpose_bf16(t->du, M, F, F, t->duT, M, s), "transpose du"));
+  BW(cu(launch_transpose_bf16(t->a2, M, C, C, t->a2T, M, s), "transpose a2"));
+  BW(grad_gemm(m, t->A_duT, t->B_a2T, g.tg_fc_w, g.fc_w, F, C, M, s));
+  if (pre) {
+    // da2 = du W_fc; s1 -> LN2 -> a2: dx += LN2'(da2)
+    BW(gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_da, M, C, F, nullptr, t->da, EPI_F32, s));
+    BW(cu(launch_layernorm_bwd(t->s1, w.ln2_g, t->da, t->dx, 1, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
+  } else {
+    // dn = ds2 + du W_fc; n = LN1(s1): d loss / d s1 in place
+    BW(gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_dx, M, C, F, nullptr, t->dx, EPI_BIAS_RESID, s));
+    BW(cu(launch_layernorm_bwd(t->s1, w.ln1_g, t->dx, t->dx, 0, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
+  }
+  // attention: s1 = x + y W_proj^T + b_proj, y = attention(qkv), qkv = a1 W_attn^T + b_attn
+  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s), "cast ds1"));
+  BW(cu(launch_colsum(t->dx, 0, M, C, C, g.proj_b, m->num_sms, s), "db_proj"));
+  BW(cu(launch_transpose_bf16(t->yb, M, C, C, t->yT, M, s), "transpose y"));
+  BW(grad_gemm(m, t->A_dxT, t->B_yT, g.tg_proj_w, g.proj_w, C, C, M, s));
+  BW(gemm_bf16(m, t->A_dxb, g.tb_proj_wT, t->C_dyb, M, C, C, nullptr, t->dyb, EPI_BIAS_OUT, s));   // dy
+  BW(cu(launch_attention_bwd(t->qkv, t->yb, t->dyb, t->dqkv, t->lse2, t->dsum, B, T, H, C / H, s), "attention'"));
+  ++t->launches;                                                                                   // two kernels
+  BW(cu(launch_colsum(t->dqkv, 1, M, 3 * C, 3 * C, g.attn_b, m->num_sms, s), "db_attn"));
+  BW(cu(launch_transpose_bf16(t->dqkv, M, 3 * C, 3 * C, t->dqkvT, M, s), "transpose dqkv"));
+  BW(cu(launch_transpose_bf16(t->a1, M, C, C, t->a1T, M, s), "transpose a1"));
+  BW(grad_gemm(m, t->A_dqkvT, t->B_a1T, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
+  if (pre) {
+    // da1 = dqkv W_attn; x -> LN1 -> a1: dx += LN1'(da1)
+    BW(gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_da, M, C, 3 * C, nullptr, t->da, EPI_F32, s));
+    BW(cu(launch_layernorm_bwd(xl, w.ln1_g, t->da, t->dx, 1, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
+  } else {
+    // a1 = x: dx += dqkv W_attn
+    BW(gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_dx, M, C, 3 * C, nullptr, t->dx, EPI_BIAS_RESID, s));
+  }
+  return GPT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gpt_backward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, int32_t B, int32_t T, float* d_loss,
+                 void* stream) {
+  if (!m || !d_ids || !d_targets) return GPT_EINVAL;
+  if (!m->bf16) return GPT_ECONFIG;
+  int rc = shape_ok(m, B, T);
+  if (rc != GPT_OK) return rc;
+  const int M = B * T;
+  if (M % 8 != 0) return GPT_EINVAL;             // rows of the transposed activations: 16-byte multiples
+  if (!m->tr) {
+    rc = alloc_train(m);
+    if (rc != GPT_OK) return rc;
+  }
+  gpt_train* t = m->tr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const gpt_config& c = m->cfg;
+  t->launches = 0;
+  rc = prepare_weights(m, t, s);
+  if (rc != GPT_OK) return rc;
+  rc = ensure_bwd_maps(m, t, B, T);
+  if (rc != GPT_OK) return rc;
+  GPT_CUDA(cudaMemsetAsync(t->gbuf, 0, t->grad_floats * sizeof(float), s));
+  // forward and loss, keeping every block's input
+  m->launches = 0;
+  m->save_x = t->xs;
+  rc = forward_bf16_direct(m, d_ids, d_targets, B, T, d_loss, s);
+  m->save_x = nullptr;
+  m->prof_ev0 = m->prof_ev1 = nullptr;
+  m->prof_step = m->prof_layer = -1;
+  if (rc != GPT_OK) return rc;
+  const int fwd_launches = m->launches;
+  rc = head_backward(m, t, d_targets, M, s);
+  if (rc != GPT_OK) return rc;
+  for (int l = c.L - 1; l >= 0; --l) {
+    rc = recompute_block(m, t, l, B, T, s);
+    if (rc != GPT_OK) return rc;
+    rc = block_backward(m, t, l, B, T, s);
+    if (rc != GPT_OK) return rc;
+  }
+  BW(cu(launch_embed_bwd(t->dx, d_ids, t->g_wte, t->g_wpe, M, T, c.C, c.V, s), "embedding'"));
+  m->launches = fwd_launches + t->launches;
+  return GPT_OK;
+}
+
+int gpt_grad(const gpt_model* m, int param, int layer, float** d_grad, int64_t* numel) {
+  if (!m || !d_grad || !m->tr) return GPT_EINVAL;
+  const gpt_config& c = m->cfg;
+  const int64_t C = c.C, F = c.ffn;
+  const gpt_train* t = m->tr;
+  float* p = nullptr;
+  int64_t n = 0;
+  if (param <= GPT_P_LNF_B) {
+    switch (param) {
+      case GPT_P_WTE: p = t->g_wte; n = static_cast<int64_t>(c.V) * C; break;
+      case GPT_P_WPE: p = t->g_wpe; n = static_cast<int64_t>(c.ctx) * C; break;
+      case GPT_P_LNF_G: p = t->g_lnf_g; n = C; break;
+      case GPT_P_LNF_B: p = t->g_lnf_b; n = C; break;
+      default: return GPT_EINVAL;
+    }
+  } else {
+    if (layer < 0 || layer >= c.L) return GPT_EINVAL;
+    const gpt_layer_grad& g = t->lg[layer];
+    switch (param) {
+      case GPT_P_LN1_G: p = g.ln1_g; n = C; break;
+      case GPT_P_LN1_B: p = g.ln1_b; n = C; break;
+      case GPT_P_ATTN_W: p = g.attn_w; n = 3 * C * C; break;
+      case GPT_P_ATTN_B: p = g.attn_b; n = 3 * C; break;
+      case GPT_P_PROJ_W: p = g.proj_w; n = C * C; break;
+      case GPT_P_PROJ_B: p = g.proj_b; n = C; break;
+      case GPT_P_LN2_G: p = g.ln2_g; n = C; break;
+      case GPT_P_LN2_B: p = g.ln2_b; n = C; break;
+      case GPT_P_FC_W: p = g.fc_w; n = F * C; break;
+      case GPT_P_FC_B: p = g.fc_b; n = F; break;
+      case GPT_P_MP_W: p = g.mp_w; n = C * F; break;
+      case GPT_P_MP_B: p = g.mp_b; n = C; break;
+      default: return GPT_EINVAL;
+    }
+  }
+  *d_grad = p;
+  if (numel) *numel = n;
+  return GPT_OK;
+}
+
+}  // extern "C"
+
+extern "C" int gpt_grad_copy(const gpt_model* m, int param, int layer, float* d_dst, void* stream) {
+  if (!d_dst) return GPT_EINVAL;
+  float* src = nullptr;
+  int64_t n = 0;
+  const int rc = gpt_grad(m, param, layer, &src, &n);
+  if (rc != GPT_OK) return rc;
+  GPT_CUDA(cudaMemcpyAsync(d_dst, src, static_cast<size_t>(n) * sizeof(float), cudaMemcpyDeviceToDevice,
+                           reinterpret_cast<cudaStream_t>(stream)));
+  return GPT_OK;
+}

@@ -86,6 +86,7 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   a.m_fastest = (N > M) ? 1 : 0;        // keep the larger operand's tiles shared by co-running CTAs
   a.sk_part = m->sk_part;               // used where whole tiles would leave the last wave part-idle
   a.sk_flag = m->sk_flag;
+  a.b_const = 1;                        // every caller's B is a weight (or a transposed copy made earlier)
   GPT_CUDA(launch_gemm_tc(tmA, tmB, tmC, a, epi, m->num_sms, s));
   return GPT_OK;
 }
@@ -122,6 +123,9 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
   }
   for (int l = 0; l < L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
+    if (m->save_x)                          // training: keep each block's input for the backward pass
+      GPT_CUDA(cudaMemcpyAsync(m->save_x + static_cast<size_t>(l) * M * C, m->x, static_cast<size_t>(M) * C * sizeof(float),
+                               cudaMemcpyDeviceToDevice, s));
     GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
     if (m->kv_fill) {                       // prefill: keep every token's key and value
       ++m->launches;
@@ -161,6 +165,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     a.logits = d_logits;
     a.err = m->err;
     a.m_fastest = 1;
+    a.b_const = 1;
     GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
     GPT_STEP(GPT_STEP_CE, -1,
              cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, m->block_sums, M, gemm_tc_num_ntiles(c.V),
@@ -396,6 +401,27 @@ int forward_graphed(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, 
   m->probe_hits = m->fwd_probe_hits;
   return GPT_OK;
 }
+
+}  // namespace
+
+namespace gptgb {
+
+// The bf16 forward pass and loss launched directly (no graph), for the backward pass.
+int forward_bf16_direct(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss,
+                        cudaStream_t s) {
+  return forward_bf16(m, ids, tg, B, T, d_loss, nullptr, s);
+}
+
+int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
+              int K, const float* bias, void* out, int epi, cudaStream_t s) {
+  return tc_gemm(m, tmA, tmB, tmC, M, N, K, bias, out, epi, s);
+}
+
+int shape_ok(const gpt_model* m, int B, int T) { return check_shape(m, B, T); }
+
+}  // namespace gptgb
+
+namespace {
 
 int map_device_error(int code) {
   switch (code) {

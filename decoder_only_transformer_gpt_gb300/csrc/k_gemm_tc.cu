@@ -40,7 +40,8 @@ constexpr int EPI_NBUF = 1;                        // staging boxes per warp
 // box per epilogue warp and a copy of the tile's bias.
 template <int EPI>
 struct Layout {
-  static constexpr bool kTmaOut = (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID);
+  static constexpr bool kTmaOut =
+      (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_CE_GRAD);
   static constexpr int STAGES = 4;
   static constexpr int STAGING = STAGES * STAGE_BYTES;
   static constexpr int BIAS = STAGING + (kTmaOut ? EPI_WARPS * EPI_NBUF * EPI_BUF : 0);   // each warp's copy of the tile's bias
@@ -50,6 +51,7 @@ struct Layout {
   static_assert(STAGES <= MAX_STAGES, "barrier arrays");
 };
 constexpr float kLog2e = 1.4426950408889634f;
+__device__ constexpr float kLog2eDev = 1.4426950408889634f;
 
 struct __align__(8) Bars {
   uint64_t full[MAX_STAGES];
@@ -294,6 +296,21 @@ __device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t* 
   }
 }
 
+// Cross-entropy gradient of 64 consecutive logits of one row, packed as bf16 pairs:
+// (exp(z - lse) - [column == tcol]) * scale, tcol the target's column within the chunk
+// (outside [0, 64) when the target is elsewhere). z <= lse, so every exponential is <= 1.
+__device__ __forceinline__ void ce_grad_chunk(const uint32_t* r, float lse, int tcol, float scale, uint32_t (&w)[32]) {
+  const float l2 = lse * kLog2eDev;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2eDev, -l2));
+    float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2eDev, -l2));
+    if (2 * i == tcol) p0 -= 1.0f;
+    if (2 * i + 1 == tcol) p1 -= 1.0f;
+    w[i] = pack_bf16x2(p0 * scale, p1 * scale);
+  }
+}
+
 // ---------------------------------------------------------------- work list
 
 // A CTA's work as a sequence of segments (tile, K blocks [kb0, kb1)).
@@ -312,7 +329,8 @@ __device__ __forceinline__ void finish_chunk(const GemmArgs& a, const uint32_t* 
 struct SegIter {
   int KB;
   long long k, kend;          // stream-K units still to deal
-  int t, stride, count;       // whole tiles still to deal
+  int t, stride, count;       // whole tiles (or split-K units) still to deal
+  int ksplit;
   __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
     if (k < kend) {
       tile = static_cast<int>(k / KB);
@@ -323,15 +341,22 @@ struct SegIter {
       return true;
     }
     if (t >= count) return false;
-    tile = t;
-    kb0 = 0;
-    kb1 = KB;
+    if (ksplit > 1) {
+      tile = t / ksplit;
+      const int sl = t - tile * ksplit;
+      kb0 = static_cast<int>(static_cast<long long>(sl) * KB / ksplit);
+      kb1 = static_cast<int>(static_cast<long long>(sl + 1) * KB / ksplit);
+    } else {
+      tile = t;
+      kb0 = 0;
+      kb1 = KB;
+    }
     t += stride;
     return true;
   }
 };
 
-__device__ __forceinline__ SegIter make_seg_iter(bool sk, int num_tiles, int KB) {
+__device__ __forceinline__ SegIter make_seg_iter(bool sk, int num_tiles, int KB, int ksplit) {
   const int G = gridDim.x;
   const int S = !sk ? 0 : (num_tiles >= 2 * G ? G + num_tiles % G : num_tiles);
   SegIter it;
@@ -341,7 +366,8 @@ __device__ __forceinline__ SegIter make_seg_iter(bool sk, int num_tiles, int KB)
   it.kend = units * (blockIdx.x + 1) / G;
   it.t = S + blockIdx.x;
   it.stride = G;
-  it.count = num_tiles;
+  it.ksplit = (!sk && ksplit > 1) ? ksplit : 1;
+  it.count = num_tiles * it.ksplit;
   return it;
 }
 
@@ -400,11 +426,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t phase = 0;
       uint32_t issued = 0, last_par = 0;
       bool ok = true;
-      // The weights (B) do not depend on the previous kernel: the first tile's
+      // Weights (B, when b_const) do not depend on the previous kernel: the first tile's
       // first stages of B are requested before waiting for that kernel to finish.
       int pre = 0;
-      SegIter it = make_seg_iter(sk, num_tiles, KB);
-      {
+      SegIter it = make_seg_iter(sk, num_tiles, KB, args.ksplit);
+      if (args.b_const) {
         SegIter it0 = it;
         int tile0, kb00, kb10;
         if (it0.next(tile0, kb00, kb10)) {
@@ -454,7 +480,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      SegIter it = make_seg_iter(sk, num_tiles, KB);
+      SegIter it = make_seg_iter(sk, num_tiles, KB, args.ksplit);
       int tile, kb0, kb1;
       while (ok && it.next(tile, kb0, kb1)) {
         if (!mbar_wait_warp(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
@@ -489,7 +515,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     pdl_wait();                                      // outputs may be read-modified-written below
     int acc = 0;
     uint32_t acc_phase = 0;
-    SegIter it = make_seg_iter(sk, num_tiles, KB);
+    SegIter it = make_seg_iter(sk, num_tiles, KB, args.ksplit);
     int tile, kb0, kb1;
     while (it.next(tile, kb0, kb1)) {
       int mb, nb;
@@ -583,6 +609,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       } else if (kTmaOut) {
         constexpr int CW = (EPI == EPI_BIAS_RESID) ? 32 : 64;    // columns per 128-byte staged row
         const int m0 = mb * BM + sub * 32;
+        float row_lse = 0.0f;
+        int row_tgt = -1;
+        if (EPI == EPI_CE_GRAD && row_ok) {
+          row_lse = __ldg(args.row_nll + grow) + __ldg(args.ztgt + grow);
+          row_tgt = __ldg(args.targets + grow);
+        }
 #pragma unroll 1
         for (int c2 = 0; c2 < BN / 64; ++c2) {
           uint32_t r[64];
@@ -609,7 +641,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int n0 = nb * BN + c * CW;
             if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
             uint32_t w[32];
-            finish_chunk<EPI, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
+            if (EPI == EPI_CE_GRAD)
+              ce_grad_chunk(r + h * CW, row_lse, row_tgt - n0, args.scale, w);
+            else
+              finish_chunk<EPI, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
             uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
             ++n_staged;
             if (lane == 0) bulk_wait_read<EPI_NBUF - 1>();   // the store that last used this box has read it
@@ -679,6 +714,12 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
   constexpr bool kSplit = EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID;
+  if (a.ksplit > 1) {                 // split-K: (tile, K slice) units, reduce-add of each partial
+    if (EPI != EPI_BIAS_RESID || a.bias != nullptr || a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;
+    const long long units = static_cast<long long>(tiles) * a.ksplit;
+    const int g2 = units < grid_limit ? static_cast<int>(units) : grid_limit;
+    return launch_inst<EPI, false>(tmA, tmB, tmC, a, g2, s);
+  }
   if (kSplit && a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
     return launch_inst<EPI, kSplit>(tmA, tmB, tmC, a, grid, s);
   return launch_inst<EPI, false>(tmA, tmB, tmC, a, grid, s);
@@ -710,6 +751,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     case EPI_BIAS_RESID: return launch_one<EPI_BIAS_RESID>(tmA, tmB, tmC, a, grid_limit, s);
     case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, tmC, a, grid_limit, s);
     case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_CE_GRAD: return launch_one<EPI_CE_GRAD>(tmA, tmB, tmC, a, grid_limit, s);
     default: return cudaErrorInvalidValue;
   }
 }

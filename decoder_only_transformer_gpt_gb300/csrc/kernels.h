@@ -22,6 +22,7 @@ enum Epilogue : int {
   EPI_BIAS_RESID = 2,     // out fp32 += acc + bias
   EPI_F32 = 3,            // out fp32 = acc (+ bias)
   EPI_CE = 4,             // per-row partial logsumexp of the tile, target capture
+  EPI_CE_GRAD = 5,        // out bf16 = (exp(z - lse) - [col == target]) * scale, lse = nll + ztgt per row
 };
 
 struct GemmArgs {
@@ -43,6 +44,14 @@ struct GemmArgs {
   // CTA holding its first K blocks after adding the other's fp32 partial.
   float* sk_part;           // [grid + 1][BM x 256] fp32 partial tiles, or nullptr: whole tiles per CTA
   int* sk_flag;             // [grid + 1][4] per-warp "partial written" flags, zero between launches
+  // Split-K (EPI_BIAS_RESID without bias, whole-tile launches): ksplit > 1 deals (tile, K slice)
+  // units, slice s covering K blocks [s KB / ksplit, (s + 1) KB / ksplit); each adds its partial
+  // into the fp32 output with the reduce-add store.
+  int ksplit;
+  int b_const;              // 1: W was not written by the previous kernel on the stream (weights), so its
+                            //    first stages may be requested before waiting for that kernel
+  const float* row_nll;     // EPI_CE_GRAD: [M] per-row loss; with ztgt gives the row's logsumexp
+  float scale;              // EPI_CE_GRAD: factor of the gradient (1 / rows of the mean)
 };
 // Floats of stream-K partial workspace for a grid of `grid` CTAs, and ints of flags.
 size_t gemm_sk_part_floats(int grid);
@@ -90,14 +99,39 @@ cudaError_t launch_attention_simt(const float* qkv, float* y, int B, int T, int 
 cudaError_t launch_ce_rows(const float* logits, const int32_t* targets, float* nll, int M, int V,
                            int* err, cudaStream_t s);
 
+// ---- backward pass (bf16 path)
+// dst[c * ldd + r] = src[r * lds + c] for a bf16 [rows, cols] matrix.
+cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s);
+// fp32 [rows, cols] (dense) -> bf16 copy dst (nullable) and bf16 transpose dstT [cols, ldt] (nullable).
+cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s);
+// out[c] += sum over rows of src[r * lds + c] (src bf16 or fp32).
+cudaError_t launch_colsum(const void* src, int bf16, int rows, int cols, int lds, float* out, int num_sms,
+                          cudaStream_t s);
+// LayerNorm derivative per row: dx_io = (add ? dx_io : 0) + dLN/dx . dy; dg += sum dy xh, db += sum dy.
+// dy may be dx_io itself when add == 0.
+cudaError_t launch_layernorm_bwd(const float* x, const float* g, const float* dy, float* dx_io, int add, float* dg,
+                                 float* db, int M, int C, float eps, int num_sms, cudaStream_t s);
+// du = dg * gelu'(u) over n bf16 values (n % 8 == 0; du may alias dg).
+cudaError_t launch_gelu_bwd(const void* u, const void* dg, void* du, size_t n, int erf_form, int num_sms,
+                            cudaStream_t s);
+// dE[id[m]] += dx0[m], dP[m % T] += dx0[m].
+cudaError_t launch_embed_bwd(const float* dx0, const int32_t* ids, float* dE, float* dP, int M, int T, int C, int V,
+                             cudaStream_t s);
+// Causal attention derivative: dqkv [B*T, 3C] bf16 from qkv [B*T, 3C], the output y and its gradient dy
+// ([B*T, C] bf16); lse2 and dsum ([B*H*T] fp32) receive each query row's base-2 log-sum-exp of the
+// scaled scores and sum of dy * y. D = 32 or 64.
+cudaError_t launch_attention_bwd(const void* qkv, const void* y, const void* dy, void* dqkv, float* lse2, float* dsum,
+                                 int B, int T, int H, int D, cudaStream_t s);
+
 // ---- TMA descriptors (host)
-// 2-D row-major bf16 matrix [rows, cols] with a box of box_rows x 64 columns, 128-byte swizzle.
+// 2-D row-major bf16 matrix [rows, cols] (row stride ld elements, 0 = cols) with a box of
+// box_rows x 64 columns, 128-byte swizzle.
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                       uint32_t box_rows);
+                       uint32_t box_rows, uint64_t ld = 0);
 // General 2-D row-major matrix (bf16 or fp32) with a box of box_rows x box_cols, box_cols * elem_bytes == 128,
-// 128-byte swizzle (the GEMM epilogue's staging layout).
+// 128-byte swizzle (the GEMM epilogue's staging layout); row stride ld elements (0 = cols).
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t rows, uint64_t cols,
-                  uint32_t box_cols, uint32_t box_rows);
+                  uint32_t box_cols, uint32_t box_rows, uint64_t ld = 0);
 // qkv viewed as [B][T][3C] bf16 with a box of 128 rows x D columns (one batch).
 bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int D);
 

@@ -12,6 +12,8 @@ struct gpt_layer_dev {
   CUtensorMap tm_attn_w, tm_proj_w, tm_fc_w, tm_mp_w;      // bf16 path only
 };
 
+struct gpt_train;                 // backward-pass workspace and gradients (gpt_backward.cu)
+
 struct gpt_model {
   gpt_config cfg;
   int device = 0;
@@ -58,6 +60,8 @@ struct gpt_model {
   int fwd_launches = 0;
   int fwd_probe_hits = 0;
   bool capturing = false;       // a forward or decode step is being captured into a graph
+  gpt_train* tr = nullptr;      // allocated by the first gpt_backward
+  float* save_x = nullptr;      // when set, each block's input x is copied to save_x + l * M * C
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;
@@ -77,6 +81,14 @@ struct gpt_model {
 };
 
 namespace gptgb {
+void free_train(gpt_model* m);     // releases m->tr (gpt_backward.cu)
+// gpt_forward.cu: the bf16 forward + loss launched directly; one tcgen05 GEMM launch (stream-K
+// workspace attached); the (B, T) checks of gpt_forward.
+int forward_bf16_direct(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss,
+                        cudaStream_t s);
+int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
+              int K, const float* bias, void* out, int epi, cudaStream_t s);
+int shape_ok(const gpt_model* m, int B, int T);
 // thread-local text of the last failing CUDA call
 void set_detail(const char* what, cudaError_t e);
 void set_detail_text(const char* text);

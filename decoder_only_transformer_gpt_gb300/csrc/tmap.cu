@@ -29,11 +29,13 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                       uint64_t ld) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || ((cols * 2) & 15u)) return false;
+  if (ld == 0) ld = cols;
+  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || ((ld * 2) & 15u) || ld < cols) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {ld * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -42,13 +44,14 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64
 }
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t rows, uint64_t cols,
-                  uint32_t box_cols, uint32_t box_rows) {
+                  uint32_t box_cols, uint32_t box_rows, uint64_t ld) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || ((cols * elem_bytes) & 15u)) return false;
+  if (ld == 0) ld = cols;
+  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || ((ld * elem_bytes) & 15u) || ld < cols) return false;
   if (elem_bytes != 2 && elem_bytes != 4) return false;
   if (box_cols * static_cast<uint32_t>(elem_bytes) != 128) return false;      // one 128-byte swizzle row
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem_bytes)};
+  const cuuint64_t strides[1] = {ld * static_cast<uint64_t>(elem_bytes)};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;

@@ -213,6 +213,43 @@ int gpt_decode_step(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t pos, 
 int gpt_sample(const float* d_logits, int32_t B, int32_t V, float temperature, int32_t top_k, float top_p,
                const float* d_uniform, int32_t* d_ids, void* stream);
 
+/*
+ * Back-propagation of the mean next-token cross-entropy ("预训练一个 Mini GPT",
+ * 训练循环: forward, loss, then the gradient of every parameter), bf16 models
+ * only (GPT_ECONFIG otherwise). Runs the forward pass and loss (d_loss, device
+ * fp32, nullable) on ids and targets (device int32 [B, T]), then writes the
+ * gradient of that loss with respect to every parameter into model-owned fp32
+ * buffers, overwriting the previous call's. The tied token table's gradient
+ * is the sum of its embedding and head shares ("第 25 章 从小 GPT 到 GPT-2"
+ * §25.4). B*T must be a multiple of 8 (GPT_EINVAL), T <= ctx (GPT_ESEQ),
+ * B*T <= max_tokens. The first call allocates the workspace synchronously
+ * (about 6 GB for GPT-2 small at 16384 tokens; GPT_ENOMEM on failure); later
+ * calls are stream-ordered. Token and target errors are reported by
+ * gpt_status, as for gpt_forward.
+ */
+int gpt_backward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, int32_t B, int32_t T,
+                 float* d_loss, void* stream);
+
+/* Parameters, for gpt_grad (the per-block ones take a layer index). */
+enum {
+  GPT_P_WTE = 0, GPT_P_WPE = 1, GPT_P_LNF_G = 2, GPT_P_LNF_B = 3,
+  GPT_P_LN1_G = 4, GPT_P_LN1_B = 5, GPT_P_ATTN_W = 6, GPT_P_ATTN_B = 7,
+  GPT_P_PROJ_W = 8, GPT_P_PROJ_B = 9, GPT_P_LN2_G = 10, GPT_P_LN2_B = 11,
+  GPT_P_FC_W = 12, GPT_P_FC_B = 13, GPT_P_MP_W = 14, GPT_P_MP_B = 15
+};
+
+/*
+ * The device pointer (fp32, model-owned, laid out as the weight: [out, in]
+ * for the matrices) and element count of one parameter's gradient from the
+ * last gpt_backward. GPT_EINVAL before the first gpt_backward or for an
+ * unknown parameter or layer. Models without a final LayerNorm report zeros
+ * for GPT_P_LNF_G / GPT_P_LNF_B.
+ */
+int gpt_grad(const gpt_model* m, int param, int layer, float** d_grad, int64_t* numel);
+
+/* Copies that gradient into caller device memory d_dst (numel fp32 values), stream-ordered. */
+int gpt_grad_copy(const gpt_model* m, int param, int layer, float* d_dst, void* stream);
+
 /* Synchronise the stream, read and clear the model's device error word. */
 int gpt_status(gpt_model* m, void* stream);
 
