@@ -522,6 +522,178 @@ def run_decode(args, rank, world, local_rank):
     model.close()
 
 
+# backward steps that gpt_backward can bracket with the probe: (name, step id, per block, kernel)
+TRAIN_STEP_KINDS = [
+    ("b_dz", 16, False, "gemm_tc_kernel<EPI_CE_GRAD> (recomputed logits -> cross-entropy gradient dz)"),
+    ("b_dh", 17, False, "gemm_tc_kernel<EPI_BIAS_RESID> (dh = dz E)"),
+    ("b_de", 18, False, "gemm_tc_kernel<EPI_BIAS_RESID> (head share of the table gradient, dz^T h)"),
+    ("b_mp_w", 19, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP down-projection weight gradient)"),
+    ("b_dg", 20, True, "gemm_tc_kernel<EPI_BIAS_OUT> (dg = dx W_mp)"),
+    ("b_fc_w", 21, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP up-projection weight gradient)"),
+    ("b_da2", 22, True, "gemm_tc_kernel<EPI_F32> (du W_fc)"),
+    ("b_proj_w", 23, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (attention output projection weight gradient)"),
+    ("b_dy", 24, True, "gemm_tc_kernel<EPI_BIAS_OUT> (dy = ds1 W_proj)"),
+    ("b_attn", 25, True, "attn_bwd_dq_kernel<64> + attn_bwd_dkv_kernel<64> (causal attention derivative, mma.sync)"),
+    ("b_attn_w", 26, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (QKV projection weight gradient)"),
+    ("b_da1", 27, True, "gemm_tc_kernel<EPI_F32> (dqkv W_attn)"),
+]
+
+
+def train_work(name, cfg, B, T):
+    """Algorithmic FLOPs of one launch of a backward step (2 per multiply-add; attention's
+    derivative: the four products dP = dY U^T, dU = A^T dY, dQ = dS K, dK = dS^T Q over the
+    causal pairs, 8 D per pair and head; recomputed scores are not counted)."""
+    M, C, F, V = B * T, cfg.C, cfg.ffn, cfg.V
+    return {"b_dz": 2.0 * M * V * C, "b_dh": 2.0 * M * V * C, "b_de": 2.0 * M * V * C,
+            "b_mp_w": 2.0 * M * C * F, "b_dg": 2.0 * M * C * F, "b_fc_w": 2.0 * M * C * F, "b_da2": 2.0 * M * C * F,
+            "b_proj_w": 2.0 * M * C * C, "b_dy": 2.0 * M * C * C, "b_attn": 4.0 * B * C * T * (T + 1),
+            "b_attn_w": 6.0 * M * C * C, "b_da1": 6.0 * M * C * C}[name]
+
+
+def train_cpu_baseline(wl, w, ids, tg, budget_s: float = 20.0):
+    """The fp64 gradient oracle, as it stands, on whole sequences of the workload until about
+    budget_s seconds have been spent (at least one)."""
+    import oracle
+    rows, spent, T = 0, 0.0, ids.shape[1]
+    while rows < ids.shape[0] and (rows == 0 or spent * (rows + 1) / rows < budget_s):
+        t0 = time.perf_counter()
+        oracle.backward(wl.cfg, w, ids[rows:rows + 1], tg[rows:rows + 1])
+        spent += time.perf_counter() - t0
+        rows += 1
+    return {"value": rows * T / spent, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows} sequence(s) x {T} tokens of the same workload, loss and gradients, numpy float64",
+            "seconds": spent}
+
+
+def run_train(args, rank, world, local_rank):
+    """--train: tokens/s of a training step's forward + backward (gpt_backward: loss and the gradient
+    of every parameter; no optimiser update), a second measurement beside the forward line. FLOPs per
+    step = 3 x the forward's (the forward, then twice its products for the input and weight
+    gradients); the recomputed activations are not counted. The dominant probed step's launches are
+    timed inside the timed region for the roofline."""
+    import torch
+    from decoder_only_transformer_gpt_gb300 import binding
+    from workloads import workload
+    from workloads.generate import generate
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl_name, _, wl_label = MODELS[args.model]
+    wl = workload(wl_name)
+    cfg = wl.cfg
+    B, T = args.batch, args.seq
+    w, ids_np, tg_np = generate(wl, B=B, T=T)
+    model = binding.GPTModel(cfg, w, B * T)
+    lib = model.lib
+    ids = torch.from_numpy(ids_np).to(dev)
+    tg = torch.from_numpy(tg_np).to(dev)
+    loss = torch.zeros(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        model.backward(ids, tg, loss, check=False)
+    model.status()
+    launches_per_step = lib.gpt_last_launch_count(model.handle)
+    rte = RuntimeEvents()
+    pa, pb = rte.create(), rte.create()
+    breakdown = {}
+    for name, sid, per_block, _ in TRAIN_STEP_KINDS:
+        times = []
+        for layer in (range(cfg.L) if per_block else [-1]):
+            lib.gpt_time_step(model.handle, sid, layer, pa, pb)
+            model.backward(ids, tg, loss, check=False)
+            torch.cuda.synchronize()
+            if lib.gpt_last_probe_hits(model.handle) == 1:
+                times.append(rte.elapsed_ms(pa, pb))
+        if times:
+            breakdown[name] = {"launches_per_step": len(times), "avg_ms": statistics.mean(times),
+                               "ms_per_step": sum(times), "work": train_work(name, cfg, B, T)}
+    lib.gpt_time_step(model.handle, -1, -1, None, None)
+    dom = max(breakdown, key=lambda k: breakdown[k]["ms_per_step"])
+    dom_sid, dom_pb, dom_kernel = next((sid, p_, k_) for n, sid, p_, k_ in TRAIN_STEP_KINDS if n == dom)
+    dom_layer = cfg.L // 2 if dom_pb else -1
+
+    # timed region: K steps, the dominant step's launch in block dom_layer bracketed in each
+    ev0 = [rte.create() for _ in range(args.steps)]
+    ev1 = [rte.create() for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for k in range(args.steps):
+        lib.gpt_time_step(model.handle, dom_sid, dom_layer, ev0[k], ev1[k])
+        model.backward(ids, tg, loss, check=False)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    model.status()
+    ms = start.elapsed_time(stop)
+    dom_ms = [rte.elapsed_ms(a, b) for a, b in zip(ev0, ev1)]
+    for h in ev0 + ev1 + [pa, pb]:
+        rte.destroy(h)
+    ms_max, value = replica_rate(ms, B * T * args.steps, world, dev)
+
+    # e2e: ids and targets copied from pinned host memory and the loss read back inside every step
+    pin_ids = torch.from_numpy(ids_np).pin_memory()
+    pin_tg = torch.from_numpy(tg_np).pin_memory()
+    pin_loss = torch.zeros(1, dtype=torch.float32).pin_memory()
+    d_ids, d_tg = torch.empty_like(ids), torch.empty_like(tg)
+
+    def host_step():
+        d_ids.copy_(pin_ids, non_blocking=True)
+        d_tg.copy_(pin_tg, non_blocking=True)
+        model.backward(d_ids, d_tg, loss, check=False)
+        pin_loss.copy_(loss, non_blocking=True)
+        torch.cuda.synchronize()
+
+    host_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        host_step()
+    _, e2e_value = replica_rate(1e3 * (time.perf_counter() - t0), B * T * args.steps, world, dev)
+    if rank != 0:
+        model.close()
+        return
+    pk, pk_src = peaks()
+    peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    flops = 3.0 * step_flops(cfg, B, T)
+    total_ms = ms / args.steps
+    kernels = []
+    for name, v in sorted(breakdown.items(), key=lambda kv: -kv[1]["ms_per_step"]):
+        a = v["work"] / (v["avg_ms"] / 1e3) / 1e12
+        kernels.append({"step": name, "launches_per_step": v["launches_per_step"], "avg_ms": v["avg_ms"],
+                        "share_of_step": v["ms_per_step"] / total_ms, "bound": "tensor", "achieved": a,
+                        "unit": "TFLOP/s", "frac": a / peak_t})
+    dom_avg = statistics.mean(dom_ms)
+    achieved = breakdown[dom]["work"] / (dom_avg / 1e3) / 1e12
+    cpu = None if (args.no_cpu_baseline or world > 1) else train_cpu_baseline(wl, w, ids_np, tg_np)
+    line = {
+        "metric": f"{wl_label.split('_b')[0]} training forward+backward tokens/sec on 1 GB300", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.model}_train_b{B}_t{T}", "B": B, "T": T, "V": cfg.V, "C": cfg.C, "H": cfg.H,
+                   "L": cfg.L, "ids": "zipf(1.1) seed 4", "l2": "inputs larger than L2 (weights and activations)",
+                   "step": "forward + loss + gradient of every parameter (no optimiser update)",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": flops * args.steps * world / (ms_max / 1e3) / 1e12,
+        "frac_of_peak": flops / (ms_max / args.steps / 1e3) / 1e12 / float(pk["bf16_tflops"]),
+        "peak_source": f"{pk_src} bf16 {pk['bf16_tflops']} TFLOP/s burst",
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"kernel": dom_kernel, "step": dom, "bound": "tensor", "achieved": achieved, "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": achieved / peak_t, "traffic": None,
+                     "algorithmic": breakdown[dom]["work"], "peak_source": f"{pk_src} bf16 sustained",
+                     "avg_launch_ms": dom_avg, "launches_timed": len(dom_ms)},
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,6 +705,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--model", choices=sorted(MODELS), default="gpt2_small")
     ap.add_argument("--decode", action="store_true", help="time incremental decoding instead of the forward")
+    ap.add_argument("--train", action="store_true", help="time forward + backward (gpt_backward) instead")
     ap.add_argument("--prompt", type=int, default=512, help="--decode: prompt length before the timed steps")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -552,6 +725,8 @@ def main():
     if args.decode:
         if rank == 0:
             run_decode(args, rank, world, local_rank)
+    elif args.train:
+        run_train(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
     if world > 1:

@@ -5,13 +5,12 @@
 // Sequence (M = B*T tokens; every product is a tcgen05 GEMM of the form
 // out = A . B^T with both operands K-major, so the activations and weights a
 // product needs along another axis are transposed first):
-//   forward + loss, keeping each block's input x_l (fp32)
+//   forward + loss, keeping every block's input and activations (and c_fc's pre-activation)
 //   head: dz = (softmax(z) - onehot) / M in bf16 straight from the GEMM that
 //         recomputes z = h E^T (the row's log-sum-exp from the forward's loss);
 //         dh = dz E; dE += dz^T h ("第 25 章" §25.4: the tied table's two uses add)
 //   ln_f: dx = LN'(x_L) dh
-//   per block, last to first: recompute the block's activations from x_l
-//         (LN, c_attn, attention, c_proj, LN, c_fc pre- and post-GELU), then
+//   per block, last to first, from its kept activations:
 //         dW_mp += dx^T g, db_mp, dg = dx W_mp, du = dg gelu'(u), dW_fc += du^T a2,
 //         db_fc, da2 = du W_fc, LN2', dW_proj += ds1^T y, db_proj, dy = ds1 W_proj,
 //         attention' -> dqkv, dW_attn += dqkv^T a1, db_attn, da1 = dqkv W_attn, LN1'
@@ -34,6 +33,16 @@ struct gpt_layer_grad {
   CUtensorMap tb_attn_wT, tb_proj_wT, tb_fc_wT, tb_mp_wT;  // as B operands
 };
 
+// One block's activations from the training forward (kept for its backward).
+struct gpt_layer_act {
+  float* x = nullptr;            // block input [M, C] fp32
+  void *a1, *qkv, *y, *a2, *u, *g;   // bf16: ln_1 output (post-norm: x itself), c_attn out, attention
+                                     // out, ln_2 output (post-norm: n), c_fc pre- and post-GELU
+  float *s1, *n, *s2;            // fp32: x + attention branch; post-norm: LN1(s1), n + MLP branch
+  CUtensorMap A_a1, A_y, A_a2, A_g;        // as GEMM A operands
+  CUtensorMap C_qkv, C_u, C_g, Q3;         // as epilogue outputs; qkv as the attention input
+};
+
 struct gpt_train {
   size_t Mx = 0;                 // token capacity (max_tokens)
   int Vp = 0;                    // V rounded up to 8 (row stride of dz and E^T)
@@ -42,14 +51,11 @@ struct gpt_train {
   float* gbuf = nullptr;         // all gradients, contiguous
   float *g_wte = nullptr, *g_wpe = nullptr, *g_lnf_g = nullptr, *g_lnf_b = nullptr;
   std::vector<gpt_layer_grad> lg;
+  std::vector<gpt_layer_act> la;
   CUtensorMap tg_wte;
   void* wteT = nullptr;          // [C][Vp] bf16
   CUtensorMap tb_wteT;
   bool wT_ready = false;
-  float* xs = nullptr;           // [L][Mx][C] block inputs
-  // recomputed activations
-  void *a1, *qkv, *yb, *a2, *u, *gg;
-  float *s1, *nb, *s2;
   // gradients of activations
   float *dx, *da;
   void *dxb, *dyb, *dqkv, *du;
@@ -58,9 +64,9 @@ struct gpt_train {
   void *dz, *dzT;
   // activation maps, for one (B, T)
   int mB = -1, mT = -1;
-  CUtensorMap A_dz, A_dzT, A_a1, A_yb, A_a2, A_gg, A_dxT, A_dxb, A_duT, A_du, A_dqkvT, A_dqkv;
+  CUtensorMap A_dz, A_dzT, A_dxT, A_dxb, A_duT, A_du, A_dqkvT, A_dqkv;
   CUtensorMap B_hT, B_gT, B_a2T, B_yT, B_a1T;
-  CUtensorMap C_dz, C_qkv, C_u, C_gg, C_du, C_dyb, C_s1, C_s2, C_da, C_dx, Q3;
+  CUtensorMap C_dz, C_du, C_dyb, C_da, C_dx;
   int launches = 0;
 };
 
@@ -103,6 +109,7 @@ int alloc_train(gpt_model* m) {
   t->Mx = Mx;
   t->Vp = static_cast<int>(Vp);
   t->lg.resize(L);
+  t->la.resize(L);
   const size_t per_layer_grad = 3 * C * C + 3 * C + C * C + C + F * C + F + C * F + C + 4 * C;
   t->grad_floats = V * C + ctx * C + 2 * C + L * per_layer_grad;
   // sizes, then one allocation
@@ -116,16 +123,20 @@ int alloc_train(gpt_model* m) {
       g.fc_wT = cv.take(F * C * 2);
       g.mp_wT = cv.take(C * F * 2);
     }
-    t->xs = static_cast<float*>(cv.take(L * Mx * C * 4));
-    t->a1 = cv.take(Mx * C * 2);
-    t->qkv = cv.take(Mx * 3 * C * 2);
-    t->yb = cv.take(Mx * C * 2);
-    t->a2 = cv.take(Mx * C * 2);
-    t->u = cv.take(Mx * F * 2);
-    t->gg = cv.take(Mx * F * 2);
-    t->s1 = static_cast<float*>(cv.take(Mx * C * 4));
-    t->nb = static_cast<float*>(cv.take(Mx * C * 4));
-    t->s2 = static_cast<float*>(cv.take(Mx * C * 4));
+    const bool post = c.norm_mode != 0;
+    for (size_t l = 0; l < L; ++l) {
+      gpt_layer_act& q = t->la[l];
+      q.x = static_cast<float*>(cv.take(Mx * C * 4));
+      q.a1 = cv.take(Mx * C * 2);
+      q.qkv = cv.take(Mx * 3 * C * 2);
+      q.y = cv.take(Mx * C * 2);
+      q.a2 = cv.take(Mx * C * 2);
+      q.u = cv.take(Mx * F * 2);
+      q.g = cv.take(Mx * F * 2);
+      q.s1 = static_cast<float*>(cv.take(Mx * C * 4));
+      q.n = post ? static_cast<float*>(cv.take(Mx * C * 4)) : nullptr;
+      q.s2 = post ? static_cast<float*>(cv.take(Mx * C * 4)) : nullptr;
+    }
     t->dx = static_cast<float*>(cv.take(Mx * C * 4));
     t->da = static_cast<float*>(cv.take(Mx * C * 4));
     t->dxb = cv.take(Mx * C * 2);
@@ -206,22 +217,24 @@ int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
   const gpt_config& c = m->cfg;
   const uint64_t M = static_cast<uint64_t>(B) * T, C = c.C, F = c.ffn, V = c.V, Vp = t->Vp;
   const uint32_t BA = kGemmBM, BB = gemm_tc_bn();
-  const bool ok =
+  bool ok =
       make_tmap_2d_bf16(&t->A_dz, t->dz, M, V, BA, Vp) && make_tmap_2d_bf16(&t->A_dzT, t->dzT, V, M, BA) &&
-      make_tmap_2d_bf16(&t->A_a1, t->a1, M, C, BA) && make_tmap_2d_bf16(&t->A_yb, t->yb, M, C, BA) &&
-      make_tmap_2d_bf16(&t->A_a2, t->a2, M, C, BA) && make_tmap_2d_bf16(&t->A_gg, t->gg, M, F, BA) &&
       make_tmap_2d_bf16(&t->A_dxT, t->dxT, C, M, BA) && make_tmap_2d_bf16(&t->A_dxb, t->dxb, M, C, BA) &&
       make_tmap_2d_bf16(&t->A_duT, t->duT, F, M, BA) && make_tmap_2d_bf16(&t->A_du, t->du, M, F, BA) &&
       make_tmap_2d_bf16(&t->A_dqkvT, t->dqkvT, 3 * C, M, BA) && make_tmap_2d_bf16(&t->A_dqkv, t->dqkv, M, 3 * C, BA) &&
       make_tmap_2d_bf16(&t->B_hT, t->hT, C, M, BB) && make_tmap_2d_bf16(&t->B_gT, t->gT, F, M, BB) &&
       make_tmap_2d_bf16(&t->B_a2T, t->a2T, C, M, BB) && make_tmap_2d_bf16(&t->B_yT, t->yT, C, M, BB) &&
       make_tmap_2d_bf16(&t->B_a1T, t->a1T, C, M, BB) &&
-      make_tmap_2d(&t->C_dz, t->dz, 2, M, V, 64, kEpiRows, Vp) && make_tmap_2d(&t->C_qkv, t->qkv, 2, M, 3 * C, 64, kEpiRows) &&
-      make_tmap_2d(&t->C_u, t->u, 2, M, F, 64, kEpiRows) && make_tmap_2d(&t->C_gg, t->gg, 2, M, F, 64, kEpiRows) &&
+      make_tmap_2d(&t->C_dz, t->dz, 2, M, V, 64, kEpiRows, Vp) &&
       make_tmap_2d(&t->C_du, t->du, 2, M, F, 64, kEpiRows) && make_tmap_2d(&t->C_dyb, t->dyb, 2, M, C, 64, kEpiRows) &&
-      make_tmap_2d(&t->C_s1, t->s1, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_s2, t->s2, 4, M, C, 32, kEpiRows) &&
-      make_tmap_2d(&t->C_da, t->da, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_dx, t->dx, 4, M, C, 32, kEpiRows) &&
-      make_tmap_qkv(&t->Q3, t->qkv, B, T, 3 * C, C / c.H);
+      make_tmap_2d(&t->C_da, t->da, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_dx, t->dx, 4, M, C, 32, kEpiRows);
+  for (size_t l = 0; l < t->la.size() && ok; ++l) {
+    gpt_layer_act& q = t->la[l];
+    ok = make_tmap_2d_bf16(&q.A_a1, q.a1, M, C, BA) && make_tmap_2d_bf16(&q.A_y, q.y, M, C, BA) &&
+         make_tmap_2d_bf16(&q.A_a2, q.a2, M, C, BA) && make_tmap_2d_bf16(&q.A_g, q.g, M, F, BA) &&
+         make_tmap_2d(&q.C_qkv, q.qkv, 2, M, 3 * C, 64, kEpiRows) && make_tmap_2d(&q.C_u, q.u, 2, M, F, 64, kEpiRows) &&
+         make_tmap_2d(&q.C_g, q.g, 2, M, F, 64, kEpiRows) && make_tmap_qkv(&q.Q3, q.qkv, B, T, 3 * C, C / c.H);
+  }
   if (!ok) {
     t->mB = t->mT = -1;
     set_detail_text("backward activation tensor map");
@@ -267,6 +280,19 @@ namespace {
     ++t->launches;                 \
   } while (0)
 
+// A timed step of the backward: the armed probe's events around it (as GPT_STEP in the forward).
+#define BWS(step, layer, expr)                                                        \
+  do {                                                                                \
+    const bool hit_ = m->prof_ev0 != nullptr && m->prof_step == (step) &&             \
+                      ((layer) < 0 || m->prof_layer == (layer));                      \
+    if (hit_) GPT_CUDA(cudaEventRecord(m->prof_ev0, s));                              \
+    BW(expr);                                                                         \
+    if (hit_) {                                                                       \
+      GPT_CUDA(cudaEventRecord(m->prof_ev1, s));                                      \
+      ++m->probe_hits;                                                                \
+    }                                                                                 \
+  } while (0)
+
 // The transposed weights the input-gradient products read (the weights do not change
 // after gpt_create, so once per model).
 int prepare_weights(gpt_model* m, gpt_train* t, cudaStream_t s) {
@@ -302,14 +328,14 @@ int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStre
   a.err = m->err;
   a.m_fastest = 1;
   a.b_const = 1;                          // the token table
-  BW(cu(launch_gemm_tc(m->tm_a, m->tm_wte, t->C_dz, a, EPI_CE_GRAD, m->num_sms, s), "head grad"));
+  BWS(GPT_STEP_B_DZ, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, t->C_dz, a, EPI_CE_GRAD, m->num_sms, s), "head grad"));
   BW(cu(launch_transpose_bf16(t->dz, M, V, t->Vp, t->dzT, M, s), "transpose dz"));
   BW(cu(launch_transpose_bf16(m->a, M, C, C, t->hT, M, s), "transpose h"));
   // dE += dz^T h (the head's share of the tied table)
-  BW(grad_gemm(m, t->A_dzT, t->B_hT, t->tg_wte, t->g_wte, V, C, M, s));
+  BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->A_dzT, t->B_hT, t->tg_wte, t->g_wte, V, C, M, s));
   // dh = dz E (fp32 into da)
   GPT_CUDA(cudaMemsetAsync(t->da, 0, static_cast<size_t>(M) * C * sizeof(float), s));
-  BW(gemm_bf16(m, t->A_dz, t->tb_wteT, t->C_da, M, C, V, nullptr, t->da, EPI_BIAS_RESID, s));
+  BWS(GPT_STEP_B_DH, -1, gemm_bf16(m, t->A_dz, t->tb_wteT, t->C_da, M, C, V, nullptr, t->da, EPI_BIAS_RESID, s));
   if (c.final_ln) {
     BW(cu(launch_layernorm_bwd(m->x, m->lnf_g, t->da, t->dx, 0, t->g_lnf_g, t->g_lnf_b, M, C, c.ln_eps, m->num_sms, s),
           "ln_f backward"));
@@ -319,31 +345,74 @@ int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStre
   return GPT_OK;
 }
 
-// Block l's activations again, from its saved input x_l.
-int recompute_block(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t s) {
+// The forward pass and loss with every block's activations kept: the kernels and their order are
+// those of gpt_forward (so the loss is the same bit for bit), only the outputs go to per-block
+// buffers. c_fc also runs without its GELU, for the pre-activation the derivative needs.
+int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss,
+                  cudaStream_t s) {
   const gpt_config& c = m->cfg;
-  const int M = B * T, C = c.C, F = c.ffn;
+  const int M = B * T, C = c.C, F = c.ffn, L = c.L;
   const bool pre = c.norm_mode == 0;
-  const gpt_layer_dev& w = m->layers[l];
-  const float* xl = t->xs + static_cast<size_t>(l) * M * C;
-  if (pre)
-    BW(cu(launch_layernorm(xl, w.ln1_g, w.ln1_b, t->a1, 1, nullptr, M, C, c.ln_eps, s), "ln1"));
-  else
-    BW(cu(launch_cast_transpose(xl, M, C, t->a1, nullptr, 0, s), "cast x"));
-  BW(gemm_bf16(m, t->A_a1, w.tm_attn_w, t->C_qkv, M, 3 * C, C, w.attn_b, t->qkv, EPI_BIAS_OUT, s));
-  BW(cu(launch_attention_tc(t->Q3, t->yb, B, T, c.H, C / c.H, m->err, s), "attention"));
-  GPT_CUDA(cudaMemcpyAsync(t->s1, xl, static_cast<size_t>(M) * C * sizeof(float), cudaMemcpyDeviceToDevice, s));
-  BW(gemm_bf16(m, t->A_yb, w.tm_proj_w, t->C_s1, M, C, C, w.proj_b, t->s1, EPI_BIAS_RESID, s));
-  if (pre)
-    BW(cu(launch_layernorm(t->s1, w.ln2_g, w.ln2_b, t->a2, 1, nullptr, M, C, c.ln_eps, s), "ln2"));
-  else
-    BW(cu(launch_layernorm(t->s1, w.ln1_g, w.ln1_b, t->a2, 1, t->nb, M, C, c.ln_eps, s), "ln1"));
-  BW(gemm_bf16(m, t->A_a2, w.tm_fc_w, t->C_u, M, F, C, w.fc_b, t->u, EPI_BIAS_OUT, s));
-  BW(gemm_bf16(m, t->A_a2, w.tm_fc_w, t->C_gg, M, F, C, w.fc_b, t->gg, EPI_BIAS_GELU_OUT, s));
-  if (!pre) {
-    GPT_CUDA(cudaMemcpyAsync(t->s2, t->nb, static_cast<size_t>(M) * C * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    BW(gemm_bf16(m, t->A_gg, w.tm_mp_w, t->C_s2, M, C, F, w.mp_b, t->s2, EPI_BIAS_RESID, s));
+  const float eps = c.ln_eps;
+  const size_t MC4 = static_cast<size_t>(M) * C * sizeof(float);
+  {
+    int out_mode = 1;
+    const float* g = nullptr;
+    const float* b = nullptr;
+    if (pre) {
+      if (L > 0) { out_mode = 2; g = m->layers[0].ln1_g; b = m->layers[0].ln1_b; }
+      else if (c.final_ln) { out_mode = 2; g = m->lnf_g; b = m->lnf_b; }
+    }
+    void* out = L > 0 ? t->la[0].a1 : m->a;
+    BW(cu(launch_embed(ids, m->wte, m->wpe, 1, m->x, out, out_mode, 1, g, b, M, T, C, c.V, eps, m->err, s), "embed"));
   }
+  for (int l = 0; l < L; ++l) {
+    const gpt_layer_dev& w = m->layers[l];
+    gpt_layer_act& q = t->la[l];
+    void* next_a = (l + 1 < L) ? t->la[l + 1].a1 : m->a;
+    GPT_CUDA(cudaMemcpyAsync(q.x, m->x, MC4, cudaMemcpyDeviceToDevice, s));
+    BW(gemm_bf16(m, q.A_a1, w.tm_attn_w, q.C_qkv, M, 3 * C, C, w.attn_b, q.qkv, EPI_BIAS_OUT, s));
+    BW(cu(launch_attention_tc(q.Q3, q.y, B, T, c.H, C / c.H, m->err, s), "attention"));
+    BW(gemm_bf16(m, q.A_y, w.tm_proj_w, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
+    GPT_CUDA(cudaMemcpyAsync(q.s1, m->x, MC4, cudaMemcpyDeviceToDevice, s));
+    if (pre) {
+      BW(cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, q.a2, 1, nullptr, M, C, eps, s), "ln2"));
+    } else {
+      BW(cu(launch_layernorm(m->x, w.ln1_g, w.ln1_b, q.a2, 1, m->x, M, C, eps, s), "ln1"));
+      GPT_CUDA(cudaMemcpyAsync(q.n, m->x, MC4, cudaMemcpyDeviceToDevice, s));
+    }
+    BW(gemm_bf16(m, q.A_a2, w.tm_fc_w, q.C_u, M, F, C, w.fc_b, q.u, EPI_BIAS_OUT, s));
+    BW(gemm_bf16(m, q.A_a2, w.tm_fc_w, q.C_g, M, F, C, w.fc_b, q.g, EPI_BIAS_GELU_OUT, s));
+    BW(gemm_bf16(m, q.A_g, w.tm_mp_w, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
+    if (pre) {
+      const float* g = nullptr;
+      const float* b = nullptr;
+      if (l + 1 < L) { g = m->layers[l + 1].ln1_g; b = m->layers[l + 1].ln1_b; }
+      else if (c.final_ln) { g = m->lnf_g; b = m->lnf_b; }
+      BW(cu(launch_layernorm(m->x, g, b, next_a, 1, nullptr, M, C, eps, s), "ln"));
+    } else {
+      GPT_CUDA(cudaMemcpyAsync(q.s2, m->x, MC4, cudaMemcpyDeviceToDevice, s));
+      BW(cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, next_a, 1, m->x, M, C, eps, s), "ln2"));
+    }
+  }
+  if (!pre && c.final_ln)
+    BW(cu(launch_layernorm(m->x, m->lnf_g, m->lnf_b, m->a, 1, nullptr, M, C, eps, s), "ln_f"));
+  // tied head with the cross-entropy partials, then the loss
+  GemmArgs a{};
+  a.M = M; a.N = c.V; a.K = C;
+  a.ldo = c.V;
+  a.targets = tg;
+  a.pmax = m->pmax;
+  a.psum = m->psum;
+  a.ztgt = m->ztgt;
+  a.err = m->err;
+  a.m_fastest = 1;
+  a.b_const = 1;
+  BW(cu(launch_gemm_tc(m->tm_a, m->tm_wte, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
+  BW(cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, m->block_sums, M, gemm_tc_num_ntiles(c.V), c.V,
+                          m->err, s),
+        "ce_combine"));
+  if (d_loss) BW(cu(launch_mean(m->block_sums, ce_combine_blocks(M), M, d_loss, s), "mean"));
   return GPT_OK;
 }
 
@@ -359,48 +428,46 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
   const float eps = c.ln_eps;
   const gpt_layer_dev& w = m->layers[l];
   gpt_layer_grad& g = t->lg[l];
-  const float* xl = t->xs + static_cast<size_t>(l) * M * C;
+  const gpt_layer_act& q = t->la[l];
+  const float* xl = q.x;
   if (!pre)      // x_{l+1} = LN2(s2): d loss / d s2, in place
-    BW(cu(launch_layernorm_bwd(t->s2, w.ln2_g, t->dx, t->dx, 0, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
+    BW(cu(launch_layernorm_bwd(q.s2, w.ln2_g, t->dx, t->dx, 0, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
   // MLP: s2 = n + g W_mp^T + b_mp, g = gelu(u), u = a2 W_fc^T + b_fc
-  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s), "cast dx"));
-  BW(cu(launch_colsum(t->dx, 0, M, C, C, g.mp_b, m->num_sms, s), "db_mp"));
-  BW(cu(launch_transpose_bf16(t->gg, M, F, F, t->gT, M, s), "transpose g"));
-  BW(grad_gemm(m, t->A_dxT, t->B_gT, g.tg_mp_w, g.mp_w, C, F, M, s));
-  BW(gemm_bf16(m, t->A_dxb, g.tb_mp_wT, t->C_du, M, F, C, nullptr, t->du, EPI_BIAS_OUT, s));      // dg
-  BW(cu(launch_gelu_bwd(t->u, t->du, t->du, static_cast<size_t>(M) * F, c.gelu, m->num_sms, s), "gelu'"));
-  BW(cu(launch_colsum(t->du, 1, M, F, F, g.fc_b, m->num_sms, s), "db_fc"));
-  BW(cu(launch_transpose_bf16(t->du, M, F, F, t->duT, M, s), "transpose du"));
-  BW(cu(launch_transpose_bf16(t->a2, M, C, C, t->a2T, M, s), "transpose a2"));
-  BW(grad_gemm(m, t->A_duT, t->B_a2T, g.tg_fc_w, g.fc_w, F, C, M, s));
+  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s, g.mp_b), "cast dx, db_mp"));
+  BW(cu(launch_transpose_bf16(q.g, M, F, F, t->gT, M, s), "transpose g"));
+  BWS(GPT_STEP_B_MP_W, l, grad_gemm(m, t->A_dxT, t->B_gT, g.tg_mp_w, g.mp_w, C, F, M, s));
+  BWS(GPT_STEP_B_DG, l, gemm_bf16(m, t->A_dxb, g.tb_mp_wT, t->C_du, M, F, C, nullptr, t->du, EPI_BIAS_OUT, s));
+  BW(cu(launch_gelu_bwd(q.u, t->du, t->du, static_cast<size_t>(M) * F, c.gelu, m->num_sms, s), "gelu'"));
+  BW(cu(launch_transpose_bf16(t->du, M, F, F, t->duT, M, s, g.fc_b), "transpose du, db_fc"));
+  BW(cu(launch_transpose_bf16(q.a2, M, C, C, t->a2T, M, s), "transpose a2"));
+  BWS(GPT_STEP_B_FC_W, l, grad_gemm(m, t->A_duT, t->B_a2T, g.tg_fc_w, g.fc_w, F, C, M, s));
   if (pre) {
     // da2 = du W_fc; s1 -> LN2 -> a2: dx += LN2'(da2)
-    BW(gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_da, M, C, F, nullptr, t->da, EPI_F32, s));
-    BW(cu(launch_layernorm_bwd(t->s1, w.ln2_g, t->da, t->dx, 1, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
+    BWS(GPT_STEP_B_DA2, l, gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_da, M, C, F, nullptr, t->da, EPI_F32_OUT, s));
+    BW(cu(launch_layernorm_bwd(q.s1, w.ln2_g, t->da, t->dx, 1, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
   } else {
     // dn = ds2 + du W_fc; n = LN1(s1): d loss / d s1 in place
-    BW(gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_dx, M, C, F, nullptr, t->dx, EPI_BIAS_RESID, s));
-    BW(cu(launch_layernorm_bwd(t->s1, w.ln1_g, t->dx, t->dx, 0, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
+    BWS(GPT_STEP_B_DA2, l, gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_dx, M, C, F, nullptr, t->dx, EPI_BIAS_RESID, s));
+    BW(cu(launch_layernorm_bwd(q.s1, w.ln1_g, t->dx, t->dx, 0, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
   }
   // attention: s1 = x + y W_proj^T + b_proj, y = attention(qkv), qkv = a1 W_attn^T + b_attn
-  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s), "cast ds1"));
-  BW(cu(launch_colsum(t->dx, 0, M, C, C, g.proj_b, m->num_sms, s), "db_proj"));
-  BW(cu(launch_transpose_bf16(t->yb, M, C, C, t->yT, M, s), "transpose y"));
-  BW(grad_gemm(m, t->A_dxT, t->B_yT, g.tg_proj_w, g.proj_w, C, C, M, s));
-  BW(gemm_bf16(m, t->A_dxb, g.tb_proj_wT, t->C_dyb, M, C, C, nullptr, t->dyb, EPI_BIAS_OUT, s));   // dy
-  BW(cu(launch_attention_bwd(t->qkv, t->yb, t->dyb, t->dqkv, t->lse2, t->dsum, B, T, H, C / H, s), "attention'"));
+  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s, g.proj_b), "cast ds1, db_proj"));
+  BW(cu(launch_transpose_bf16(q.y, M, C, C, t->yT, M, s), "transpose y"));
+  BWS(GPT_STEP_B_PROJ_W, l, grad_gemm(m, t->A_dxT, t->B_yT, g.tg_proj_w, g.proj_w, C, C, M, s));
+  BWS(GPT_STEP_B_DY, l, gemm_bf16(m, t->A_dxb, g.tb_proj_wT, t->C_dyb, M, C, C, nullptr, t->dyb, EPI_BIAS_OUT, s));
+  BWS(GPT_STEP_B_ATTN, l,
+      cu(launch_attention_bwd(q.qkv, q.y, t->dyb, t->dqkv, t->lse2, t->dsum, B, T, H, C / H, s), "attention'"));
   ++t->launches;                                                                                   // two kernels
-  BW(cu(launch_colsum(t->dqkv, 1, M, 3 * C, 3 * C, g.attn_b, m->num_sms, s), "db_attn"));
-  BW(cu(launch_transpose_bf16(t->dqkv, M, 3 * C, 3 * C, t->dqkvT, M, s), "transpose dqkv"));
-  BW(cu(launch_transpose_bf16(t->a1, M, C, C, t->a1T, M, s), "transpose a1"));
-  BW(grad_gemm(m, t->A_dqkvT, t->B_a1T, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
+  BW(cu(launch_transpose_bf16(t->dqkv, M, 3 * C, 3 * C, t->dqkvT, M, s, g.attn_b), "transpose dqkv, db_attn"));
+  BW(cu(launch_transpose_bf16(q.a1, M, C, C, t->a1T, M, s), "transpose a1"));
+  BWS(GPT_STEP_B_ATTN_W, l, grad_gemm(m, t->A_dqkvT, t->B_a1T, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
   if (pre) {
     // da1 = dqkv W_attn; x -> LN1 -> a1: dx += LN1'(da1)
-    BW(gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_da, M, C, 3 * C, nullptr, t->da, EPI_F32, s));
+    BWS(GPT_STEP_B_DA1, l, gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_da, M, C, 3 * C, nullptr, t->da, EPI_F32_OUT, s));
     BW(cu(launch_layernorm_bwd(xl, w.ln1_g, t->da, t->dx, 1, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
   } else {
     // a1 = x: dx += dqkv W_attn
-    BW(gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_dx, M, C, 3 * C, nullptr, t->dx, EPI_BIAS_RESID, s));
+    BWS(GPT_STEP_B_DA1, l, gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_dx, M, C, 3 * C, nullptr, t->dx, EPI_BIAS_RESID, s));
   }
   return GPT_OK;
 }
@@ -432,23 +499,17 @@ int gpt_backward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, i
   GPT_CUDA(cudaMemsetAsync(t->gbuf, 0, t->grad_floats * sizeof(float), s));
   // forward and loss, keeping every block's input
   m->launches = 0;
-  m->save_x = t->xs;
-  rc = forward_bf16_direct(m, d_ids, d_targets, B, T, d_loss, s);
-  m->save_x = nullptr;
-  m->prof_ev0 = m->prof_ev1 = nullptr;
+  m->probe_hits = 0;
+  rc = forward_maps(m, B, T);
+  if (rc == GPT_OK) rc = train_forward(m, t, d_ids, d_targets, B, T, d_loss, s);
+  const int fwd_launches = 0;
+  if (rc == GPT_OK) rc = head_backward(m, t, d_targets, M, s);
+  for (int l = c.L - 1; l >= 0 && rc == GPT_OK; --l) rc = block_backward(m, t, l, B, T, s);
+  if (rc == GPT_OK) rc = cu(launch_embed_bwd(t->dx, d_ids, t->g_wte, t->g_wpe, M, T, c.C, c.V, s), "embedding'");
+  m->prof_ev0 = m->prof_ev1 = nullptr;            // a probe covers one call
   m->prof_step = m->prof_layer = -1;
   if (rc != GPT_OK) return rc;
-  const int fwd_launches = m->launches;
-  rc = head_backward(m, t, d_targets, M, s);
-  if (rc != GPT_OK) return rc;
-  for (int l = c.L - 1; l >= 0; --l) {
-    rc = recompute_block(m, t, l, B, T, s);
-    if (rc != GPT_OK) return rc;
-    rc = block_backward(m, t, l, B, T, s);
-    if (rc != GPT_OK) return rc;
-  }
-  BW(cu(launch_embed_bwd(t->dx, d_ids, t->g_wte, t->g_wpe, M, T, c.C, c.V, s), "embedding'"));
-  m->launches = fwd_launches + t->launches;
+  m->launches = fwd_launches + t->launches + 1;
   return GPT_OK;
 }
 

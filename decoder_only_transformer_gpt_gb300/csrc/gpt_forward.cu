@@ -123,9 +123,6 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
   }
   for (int l = 0; l < L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
-    if (m->save_x)                          // training: keep each block's input for the backward pass
-      GPT_CUDA(cudaMemcpyAsync(m->save_x + static_cast<size_t>(l) * M * C, m->x, static_cast<size_t>(M) * C * sizeof(float),
-                               cudaMemcpyDeviceToDevice, s));
     GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
     if (m->kv_fill) {                       // prefill: keep every token's key and value
       ++m->launches;
@@ -150,7 +147,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     GPT_STEP(GPT_STEP_LN_OUT, l,
              cu(launch_layernorm(m->x, out.g, out.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
   }
-  if (!pre && L == 0 && c.final_ln)
+  if (!pre && c.final_ln)                   // post-norm with a final LayerNorm: after the last block's ln_2
     GPT_STEP(GPT_STEP_LN_OUT, -1, cu(launch_layernorm(m->x, m->lnf_g, m->lnf_b, m->a, 1, nullptr, M, C, c.ln_eps, s), "ln"));
 
   // K5/K6: tied head
@@ -406,11 +403,8 @@ int forward_graphed(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, 
 
 namespace gptgb {
 
-// The bf16 forward pass and loss launched directly (no graph), for the backward pass.
-int forward_bf16_direct(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss,
-                        cudaStream_t s) {
-  return forward_bf16(m, ids, tg, B, T, d_loss, nullptr, s);
-}
+// The activation descriptors of the forward pass (x, a, ...) for this (B, T).
+int forward_maps(gpt_model* m, int B, int T) { return ensure_act_maps(m, B, T); }
 
 int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
               int K, const float* bias, void* out, int epi, cudaStream_t s) {
@@ -538,7 +532,8 @@ int gpt_time_step(gpt_model* m, int step, int layer, void* ev_start, void* ev_st
     m->prof_step = m->prof_layer = -1;
     return GPT_OK;
   }
-  if (!ev_stop || step < GPT_STEP_EMBED || step > GPT_STEP_MEAN) return GPT_EINVAL;
+  if (!ev_stop || step < GPT_STEP_EMBED || (step > GPT_STEP_MEAN && step < GPT_STEP_B_DZ) || step > GPT_STEP_B_DA1)
+    return GPT_EINVAL;
   m->prof_step = step;
   m->prof_layer = layer;
   m->prof_ev0 = reinterpret_cast<cudaEvent_t>(ev_start);

@@ -29,25 +29,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// dst[c][r] = src[r][c]: a 32 x 32 tile per block through shared memory (the padded
-// row of 34 halves puts a column's 32 entries in 32 different banks).
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ src, int rows, int cols,
-                                                             int lds, uint16_t* __restrict__ dst, int ldd) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ uint16_t t[kTr][kTr + 2];
-  const int c0 = blockIdx.x * kTr, r0 = blockIdx.y * kTr;
-  for (int i = threadIdx.y; i < kTr; i += 8) {
-    const int r = r0 + i, c = c0 + threadIdx.x;
-    t[i][threadIdx.x] = (r < rows && c < cols) ? src[static_cast<size_t>(r) * lds + c] : uint16_t(0);
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < kTr; i += 8) {
-    const int c = c0 + i, r = r0 + threadIdx.x;
-    if (c < cols && r < rows) dst[static_cast<size_t>(c) * ldd + r] = t[threadIdx.x][i];
-  }
-}
-
 // fp32 [rows, cols] -> bf16 copy (dst, nullable) and bf16 transpose (dstT [cols, rows], nullable).
 __global__ void __launch_bounds__(256) cast_transpose_kernel(const float* __restrict__ src, int rows, int cols,
                                                              uint16_t* __restrict__ dst, uint16_t* __restrict__ dstT,
@@ -213,22 +194,204 @@ __global__ void __launch_bounds__(256) embed_bwd_kernel(const float* __restrict_
   }
 }
 
-}  // namespace
+// 64 x 64 tiles with 16-byte global accesses. Load: 8 threads per 128-byte row segment into a
+// shared tile (row stride 72 halves keeps 16-byte alignment); store: consecutive threads take
+// consecutive output rows (tile columns), so the column gathers from shared memory hit 16
+// different banks per warp, and each thread writes 8 consecutive outputs (16 bytes).
+// SRC_F32: the source is fp32 [rows, cols] (dense), converted to bf16, also copied to dst_copy.
+constexpr int kT64 = 64, kT64S = 72;
 
-cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s) {
-  if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const dim3 grid((cols + kTr - 1) / kTr, (rows + kTr - 1) / kTr), block(kTr, 8);
-  if (grid.y > 65535u) return cudaErrorInvalidValue;
-  return launch_k(transpose_bf16_kernel, grid, block, 0, s, static_cast<const uint16_t*>(src), rows, cols, lds,
-                  static_cast<uint16_t*>(dst), ldd);
+// colsum (nullable): out[c] += the tile's column sums (of the fp32 values for an fp32 source).
+template <bool SRC_F32>
+__global__ void __launch_bounds__(256) transpose64_kernel(const void* __restrict__ src, int rows, int cols, int lds,
+                                                          uint16_t* __restrict__ dst_copy, uint16_t* __restrict__ dstT,
+                                                          int ldt, int vec, float* __restrict__ colsum) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ __align__(16) uint16_t t[kT64][kT64S];
+  __shared__ float csum[kT64];
+  const int c0 = blockIdx.x * kT64, r0 = blockIdx.y * kT64;
+  if (colsum) {
+    if (threadIdx.x < kT64) csum[threadIdx.x] = 0.0f;
+    __syncthreads();
+  }
+  float part[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  for (int i = threadIdx.x; i < kT64 * 8; i += 256) {
+    const int r = i >> 3, ch = i & 7;
+    const int gr = r0 + r, gc = c0 + ch * 8;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (gr < rows) {
+      if (SRC_F32) {
+        const float* sp = static_cast<const float*>(src) + static_cast<size_t>(gr) * lds + gc;
+        float f[8];
+        if (vec && gc + 8 <= cols) {
+          const float4 a = *reinterpret_cast<const float4*>(sp), b = *reinterpret_cast<const float4*>(sp + 4);
+          f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = gc + k < cols ? sp[k] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) part[k] += f[k];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = pack_bf16x2(f[2 * k], f[2 * k + 1]);
+        if (dst_copy) {
+          uint16_t* dp = dst_copy + static_cast<size_t>(gr) * lds + gc;
+          if (vec && gc + 8 <= cols) {
+            *reinterpret_cast<uint4*>(dp) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            for (int k = 0; k < 8 && gc + k < cols; ++k) dp[k] = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+          }
+        }
+      } else {
+        const uint16_t* sp = static_cast<const uint16_t*>(src) + static_cast<size_t>(gr) * lds + gc;
+        if (vec && gc + 8 <= cols) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sp);
+          w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (gc + k < cols) w[k >> 1] |= static_cast<uint32_t>(sp[k]) << (16 * (k & 1));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f2 = unpack_bf16x2(w[k]);
+          part[2 * k] += f2.x;
+          part[2 * k + 1] += f2.y;
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(&t[r][ch * 8]) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (colsum) {                  // a thread's columns are ch * 8 .. + 7, ch = lane & 7: fold lanes ch, +8, +16, +24
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float v = part[k];
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      if (lane < 8) atomicAdd(csum + lane * 8 + k, v);
+    }
+  }
+  __syncthreads();
+  if (colsum && threadIdx.x < kT64 && c0 + threadIdx.x < cols) atomicAdd(colsum + c0 + threadIdx.x, csum[threadIdx.x]);
+  for (int i = threadIdx.x; i < kT64 * 8; i += 256) {
+    const int cc = i & 63, ch = i >> 6;
+    const int oc = c0 + cc, orow = r0 + ch * 8;          // output row oc, columns orow .. orow + 7
+    if (oc >= cols || orow >= rows) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = static_cast<uint32_t>(t[ch * 8 + 2 * k][cc]) | (static_cast<uint32_t>(t[ch * 8 + 2 * k + 1][cc]) << 16);
+    uint16_t* dp = dstT + static_cast<size_t>(oc) * ldt + orow;
+    if (vec && orow + 8 <= rows) {
+      *reinterpret_cast<uint4*>(dp) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      for (int k = 0; k < 8 && orow + k < rows; ++k) dp[k] = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+    }
+  }
 }
 
-cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s) {
+// LayerNorm derivative with the row held in registers: C = 32 NPL, lane j-th column lane + 32 j
+// (128-byte coalesced), gain and shift gradients accumulated per lane across the warp's rows and
+// added once per warp (shared memory) and once per block (global). x and dy are read once.
+template <int NPL>
+__global__ void __launch_bounds__(256) layernorm_bwd_reg_kernel(const float* __restrict__ x, const float* __restrict__ g,
+                                                                const float* dy, float* dx_io, int add,
+                                                                float* __restrict__ dg, float* __restrict__ db, int M,
+                                                                float eps) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int C = 32 * NPL;
+  __shared__ float sg[C], sb[C];
+  for (int i = threadIdx.x; i < C; i += blockDim.x) sg[i] = sb[i] = 0.0f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  constexpr float invC = 1.0f / static_cast<float>(C);
+  float gam[NPL], ag[NPL], ab[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    gam[j] = g[lane + 32 * j];
+    ag[j] = ab[j] = 0.0f;
+  }
+  for (int row = blockIdx.x * wpb + warp; row < M; row += gridDim.x * wpb) {
+    const float* xr = x + static_cast<size_t>(row) * C;
+    const float* dr = dy + static_cast<size_t>(row) * C;
+    float xv[NPL], dv[NPL];
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      xv[j] = xr[lane + 32 * j];
+      dv[j] = dr[lane + 32 * j];
+      s += xv[j];
+    }
+    const float mean = warp_sum(s) * invC;
+    float v = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      xv[j] -= mean;
+      v += xv[j] * xv[j];
+    }
+    const float r = rsqrtf(warp_sum(v) * invC + eps);
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      xv[j] *= r;                                          // xh
+      const float dxh = dv[j] * gam[j];
+      s1 += dxh;
+      s2 += dxh * xv[j];
+      ag[j] += dv[j] * xv[j];
+      ab[j] += dv[j];
+    }
+    const float m1 = warp_sum(s1) * invC, m2 = warp_sum(s2) * invC;
+    float* o = dx_io + static_cast<size_t>(row) * C;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const float val = r * (dv[j] * gam[j] - m1 - xv[j] * m2);
+      o[lane + 32 * j] = add ? o[lane + 32 * j] + val : val;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    atomicAdd(sg + lane + 32 * j, ag[j]);
+    atomicAdd(sb + lane + 32 * j, ab[j]);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < C; i += blockDim.x) {
+    atomicAdd(dg + i, sg[i]);
+    atomicAdd(db + i, sb[i]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s,
+                                  float* colsum) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const dim3 grid((cols + kTr - 1) / kTr, (rows + kTr - 1) / kTr), block(kTr, 8);
+  const dim3 grid((cols + kT64 - 1) / kT64, (rows + kT64 - 1) / kT64);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
-  return launch_k(cast_transpose_kernel, grid, block, 0, s, src, rows, cols, static_cast<uint16_t*>(dst),
-                  static_cast<uint16_t*>(dstT), ldt);
+  const int vec = (lds % 8 == 0) && (ldd % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
+  return launch_k(transpose64_kernel<false>, grid, dim3(256), 0, s, src, rows, cols, lds, static_cast<uint16_t*>(nullptr),
+                  static_cast<uint16_t*>(dst), ldd, vec, colsum);
+}
+
+cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s,
+                                  float* colsum) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (dstT == nullptr) {                                   // a plain cast
+    if (colsum) return cudaErrorInvalidValue;
+    const dim3 grid((cols + kTr - 1) / kTr, (rows + kTr - 1) / kTr), block(kTr, 8);
+    if (grid.y > 65535u) return cudaErrorInvalidValue;
+    return launch_k(cast_transpose_kernel, grid, block, 0, s, src, rows, cols, static_cast<uint16_t*>(dst),
+                    static_cast<uint16_t*>(nullptr), ldt);
+  }
+  const dim3 grid((cols + kT64 - 1) / kT64, (rows + kT64 - 1) / kT64);
+  if (grid.y > 65535u) return cudaErrorInvalidValue;
+  const int vec = (cols % 8 == 0) && (ldt % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (reinterpret_cast<uintptr_t>(dstT) % 16 == 0);
+  return launch_k(transpose64_kernel<true>, grid, dim3(256), 0, s, static_cast<const void*>(src), rows, cols, cols,
+                  static_cast<uint16_t*>(dst), static_cast<uint16_t*>(dstT), ldt, vec, colsum);
 }
 
 cudaError_t launch_colsum(const void* src, int bf16, int rows, int cols, int lds, float* out, int num_sms,
@@ -247,8 +410,17 @@ cudaError_t launch_colsum(const void* src, int bf16, int rows, int cols, int lds
 cudaError_t launch_layernorm_bwd(const float* x, const float* g, const float* dy, float* dx_io, int add, float* dg,
                                  float* db, int M, int C, float eps, int num_sms, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  const int wpb = 8;
+  int wpb = 4;                                  // 128-thread blocks: several per SM at the kernel's registers
   int grid = (M + wpb - 1) / wpb;
+  if (grid > 4 * num_sms) grid = 4 * num_sms;
+#define GPT_LNB(NPL)                                                                                          \
+  if (C == 32 * NPL)                                                                                          \
+    return launch_k(layernorm_bwd_reg_kernel<NPL>, dim3(grid), dim3(wpb * 32), 0, s, x, g, dy, dx_io, add, dg, \
+                    db, M, eps);
+  GPT_LNB(2) GPT_LNB(4) GPT_LNB(8) GPT_LNB(12) GPT_LNB(16) GPT_LNB(24) GPT_LNB(32)
+#undef GPT_LNB
+  wpb = 8;
+  grid = (M + wpb - 1) / wpb;
   if (grid > 2 * num_sms) grid = 2 * num_sms;
   const size_t smem = 2 * static_cast<size_t>(C) * sizeof(float);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;

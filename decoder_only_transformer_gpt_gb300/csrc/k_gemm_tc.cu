@@ -41,7 +41,8 @@ constexpr int EPI_NBUF = 1;                        // staging boxes per warp
 template <int EPI>
 struct Layout {
   static constexpr bool kTmaOut =
-      (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_CE_GRAD);
+      (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_CE_GRAD ||
+       EPI == EPI_F32_OUT);
   static constexpr int STAGES = 4;
   static constexpr int STAGING = STAGES * STAGE_BYTES;
   static constexpr int BIAS = STAGING + (kTmaOut ? EPI_WARPS * EPI_NBUF * EPI_BUF : 0);   // each warp's copy of the tile's bias
@@ -331,6 +332,7 @@ struct SegIter {
   long long k, kend;          // stream-K units still to deal
   int t, stride, count;       // whole tiles (or split-K units) still to deal
   int ksplit;
+  template <bool KS>
   __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
     if (k < kend) {
       tile = static_cast<int>(k / KB);
@@ -341,7 +343,7 @@ struct SegIter {
       return true;
     }
     if (t >= count) return false;
-    if (ksplit > 1) {
+    if (KS) {
       tile = t / ksplit;
       const int sl = t - tile * ksplit;
       kb0 = static_cast<int>(static_cast<long long>(sl) * KB / ksplit);
@@ -356,7 +358,7 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ SegIter make_seg_iter(bool sk, int num_tiles, int KB, int ksplit) {
+__device__ __forceinline__ SegIter make_seg_iter(bool sk, bool ks, int num_tiles, int KB, int ksplit) {
   const int G = gridDim.x;
   const int S = !sk ? 0 : (num_tiles >= 2 * G ? G + num_tiles % G : num_tiles);
   SegIter it;
@@ -366,16 +368,19 @@ __device__ __forceinline__ SegIter make_seg_iter(bool sk, int num_tiles, int KB,
   it.kend = units * (blockIdx.x + 1) / G;
   it.t = S + blockIdx.x;
   it.stride = G;
-  it.ksplit = (!sk && ksplit > 1) ? ksplit : 1;
+  it.ksplit = (ks && ksplit > 1) ? ksplit : 1;
   it.count = num_tiles * it.ksplit;
   return it;
 }
 
 // ---------------------------------------------------------------- kernel
 
-// SK: whether the launch splits tiles (stream-K). Whole-tile launches use their
+// MODE 0: whole tiles; 1: stream-K (tiles split between CTAs, partials fixed up);
+// 2: split-K (units of (tile, K slice) added with reduce-add stores). Each mode is
+// its own instantiation, so whole-tile launches carry no segment bookkeeping.
+// (The stream-K notes below say SK for MODE == 1.) Whole-tile launches use their
 // own instantiation, whose loops have no segment bookkeeping.
-template <int EPI, bool SK>
+template <int EPI, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -397,6 +402,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int NB = (args.N + BN - 1) / BN;
   const int KB = (args.K + BK - 1) / BK;
   const int num_tiles = MB * NB;
+  constexpr bool SK = MODE == 1, KS = MODE == 2;
   constexpr bool sk = SK;
 
   if (threadIdx.x == 0) {
@@ -429,11 +435,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // Weights (B, when b_const) do not depend on the previous kernel: the first tile's
       // first stages of B are requested before waiting for that kernel to finish.
       int pre = 0;
-      SegIter it = make_seg_iter(sk, num_tiles, KB, args.ksplit);
+      SegIter it = make_seg_iter(sk, KS, num_tiles, KB, args.ksplit);
       if (args.b_const) {
         SegIter it0 = it;
         int tile0, kb00, kb10;
-        if (it0.next(tile0, kb00, kb10)) {
+        if (it0.template next<KS>(tile0, kb00, kb10)) {
           int mb0, nb0;
           tile_coords(tile0, MB, NB, args.m_fastest, mb0, nb0);
           pre = (kb10 - kb00) < STAGES ? (kb10 - kb00) : STAGES;
@@ -445,7 +451,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       pdl_wait();                     // A, written by the previous kernel, is now visible
       int tile, kb0, kb1;
-      while (ok && it.next(tile, kb0, kb1)) {
+      while (ok && it.template next<KS>(tile, kb0, kb1)) {
         int mb, nb;
         tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -480,9 +486,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      SegIter it = make_seg_iter(sk, num_tiles, KB, args.ksplit);
+      SegIter it = make_seg_iter(sk, KS, num_tiles, KB, args.ksplit);
       int tile, kb0, kb1;
-      while (ok && it.next(tile, kb0, kb1)) {
+      while (ok && it.template next<KS>(tile, kb0, kb1)) {
         if (!mbar_wait_warp(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -515,9 +521,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     pdl_wait();                                      // outputs may be read-modified-written below
     int acc = 0;
     uint32_t acc_phase = 0;
-    SegIter it = make_seg_iter(sk, num_tiles, KB, args.ksplit);
+    SegIter it = make_seg_iter(sk, KS, num_tiles, KB, args.ksplit);
     int tile, kb0, kb1;
-    while (it.next(tile, kb0, kb1)) {
+    while (it.template next<KS>(tile, kb0, kb1)) {
       int mb, nb;
       tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
       // stream-K: a suffix (kb0 > 0) hands its fp32 partial to the CTA before, in
@@ -607,7 +613,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           args.psum[(size_t)nb * args.M + grow] = s;
         }
       } else if (kTmaOut) {
-        constexpr int CW = (EPI == EPI_BIAS_RESID) ? 32 : 64;    // columns per 128-byte staged row
+        constexpr int CW = (EPI == EPI_BIAS_RESID || EPI == EPI_F32_OUT) ? 32 : 64;   // columns per 128-byte row
         const int m0 = mb * BM + sub * 32;
         float row_lse = 0.0f;
         int row_tgt = -1;
@@ -692,17 +698,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <int EPI, bool SK>
+template <int EPI, int MODE>
 cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                         int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, SK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<EPI>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(gemm_tc_kernel<EPI, SK>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
+  return launch_k(gemm_tc_kernel<EPI, MODE>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
 }
 
 template <int EPI>
@@ -713,16 +719,22 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   const int tiles = MB * NB;
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
-  constexpr bool kSplit = EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID;
+  constexpr bool kSplit = EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_F32_OUT;
   if (a.ksplit > 1) {                 // split-K: (tile, K slice) units, reduce-add of each partial
-    if (EPI != EPI_BIAS_RESID || a.bias != nullptr || a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;
-    const long long units = static_cast<long long>(tiles) * a.ksplit;
-    const int g2 = units < grid_limit ? static_cast<int>(units) : grid_limit;
-    return launch_inst<EPI, false>(tmA, tmB, tmC, a, g2, s);
+    if constexpr (EPI == EPI_BIAS_RESID) {
+      if (a.bias != nullptr || a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;
+      const long long units = static_cast<long long>(tiles) * a.ksplit;
+      const int g2 = units < grid_limit ? static_cast<int>(units) : grid_limit;
+      return launch_inst<EPI, 2>(tmA, tmB, tmC, a, g2, s);
+    } else {
+      return cudaErrorInvalidValue;
+    }
   }
-  if (kSplit && a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
-    return launch_inst<EPI, kSplit>(tmA, tmB, tmC, a, grid, s);
-  return launch_inst<EPI, false>(tmA, tmB, tmC, a, grid, s);
+  if constexpr (kSplit) {
+    if (a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
+      return launch_inst<EPI, 1>(tmA, tmB, tmC, a, grid, s);
+  }
+  return launch_inst<EPI, 0>(tmA, tmB, tmC, a, grid, s);
 }
 
 }  // namespace
@@ -734,7 +746,7 @@ int gemm_tc_bn() { return BN; }
 // the last wave is smaller than the cost of splitting (measured on GB300).
 constexpr int kSplitMinKB = 24;
 bool gemm_tc_stream_k(int M, int N, int K, int epi, int grid_limit) {
-  if (epi != EPI_BIAS_OUT && epi != EPI_BIAS_GELU_OUT && epi != EPI_BIAS_RESID) return false;
+  if (epi != EPI_BIAS_OUT && epi != EPI_BIAS_GELU_OUT && epi != EPI_BIAS_RESID && epi != EPI_F32_OUT) return false;
   const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int KB = (K + BK - 1) / BK;
   return KB >= kSplitMinKB && grid_limit > 0 && tiles > grid_limit && tiles % grid_limit != 0;
@@ -752,6 +764,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, tmC, a, grid_limit, s);
     case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, tmC, a, grid_limit, s);
     case EPI_CE_GRAD: return launch_one<EPI_CE_GRAD>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_F32_OUT: return launch_one<EPI_F32_OUT>(tmA, tmB, tmC, a, grid_limit, s);
     default: return cudaErrorInvalidValue;
   }
 }

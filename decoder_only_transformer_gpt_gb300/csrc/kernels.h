@@ -23,6 +23,7 @@ enum Epilogue : int {
   EPI_F32 = 3,            // out fp32 = acc (+ bias)
   EPI_CE = 4,             // per-row partial logsumexp of the tile, target capture
   EPI_CE_GRAD = 5,        // out bf16 = (exp(z - lse) - [col == target]) * scale, lse = nll + ztgt per row
+  EPI_F32_OUT = 6,        // out fp32 = acc (+ bias) through the TMA store (fp32 [M,N] box 32x32)
 };
 
 struct GemmArgs {
@@ -100,10 +101,13 @@ cudaError_t launch_ce_rows(const float* logits, const int32_t* targets, float* n
                            int* err, cudaStream_t s);
 
 // ---- backward pass (bf16 path)
-// dst[c * ldd + r] = src[r * lds + c] for a bf16 [rows, cols] matrix.
-cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s);
-// fp32 [rows, cols] (dense) -> bf16 copy dst (nullable) and bf16 transpose dstT [cols, ldt] (nullable).
-cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s);
+// dst[c * ldd + r] = src[r * lds + c] for a bf16 [rows, cols] matrix; colsum (nullable) += its column sums.
+cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s,
+                                  float* colsum = nullptr);
+// fp32 [rows, cols] (dense) -> bf16 copy dst (nullable) and bf16 transpose dstT [cols, ldt] (nullable);
+// colsum (nullable, needs dstT) += the column sums of the fp32 values.
+cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s,
+                                  float* colsum = nullptr);
 // out[c] += sum over rows of src[r * lds + c] (src bf16 or fp32).
 cudaError_t launch_colsum(const void* src, int bf16, int rows, int cols, int lds, float* out, int num_sms,
                           cudaStream_t s);

@@ -61,7 +61,6 @@ struct gpt_model {
   int fwd_probe_hits = 0;
   bool capturing = false;       // a forward or decode step is being captured into a graph
   gpt_train* tr = nullptr;      // allocated by the first gpt_backward
-  float* save_x = nullptr;      // when set, each block's input x is copied to save_x + l * M * C
   int* err = nullptr;       // device error word
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;
@@ -82,10 +81,9 @@ struct gpt_model {
 
 namespace gptgb {
 void free_train(gpt_model* m);     // releases m->tr (gpt_backward.cu)
-// gpt_forward.cu: the bf16 forward + loss launched directly; one tcgen05 GEMM launch (stream-K
-// workspace attached); the (B, T) checks of gpt_forward.
-int forward_bf16_direct(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int T, float* d_loss,
-                        cudaStream_t s);
+// gpt_forward.cu: the forward pass's activation descriptors for (B, T); one tcgen05 GEMM launch
+// (stream-K workspace attached); the (B, T) checks of gpt_forward.
+int forward_maps(gpt_model* m, int B, int T);
 int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
               int K, const float* bias, void* out, int epi, cudaStream_t s);
 int shape_ok(const gpt_model* m, int B, int T);

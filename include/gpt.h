@@ -135,11 +135,24 @@ enum {
   GPT_STEP_LN_OUT = 7,     /* the LayerNorm after the block (next ln_1, ln_f or post-norm ln_2) */
   GPT_STEP_HEAD = 8,       /* tied LM head (+ fused cross-entropy partials) */
   GPT_STEP_CE = 9,         /* cross-entropy combine */
-  GPT_STEP_MEAN = 10       /* mean of the per-position losses */
+  GPT_STEP_MEAN = 10,      /* mean of the per-position losses */
+  /* steps of gpt_backward (its forward part uses the ids above) */
+  GPT_STEP_B_DZ = 16,      /* cross-entropy gradient dz from the recomputed head logits */
+  GPT_STEP_B_DH = 17,      /* dh = dz E */
+  GPT_STEP_B_DE = 18,      /* the head's share of the table gradient, dz^T h */
+  GPT_STEP_B_MP_W = 19,    /* block `layer`: weight gradient of the MLP down-projection */
+  GPT_STEP_B_DG = 20,      /* dg = dx W_mp */
+  GPT_STEP_B_FC_W = 21,    /* weight gradient of the MLP up-projection */
+  GPT_STEP_B_DA2 = 22,     /* du W_fc */
+  GPT_STEP_B_PROJ_W = 23,  /* weight gradient of the attention output projection */
+  GPT_STEP_B_DY = 24,      /* dy = ds1 W_proj */
+  GPT_STEP_B_ATTN = 25,    /* causal attention derivative (two kernels) */
+  GPT_STEP_B_ATTN_W = 26,  /* weight gradient of the QKV projection */
+  GPT_STEP_B_DA1 = 27      /* dqkv W_attn */
 };
 
 /*
- * Arm a timing probe for the NEXT gpt_forward on this model: ev_start
+ * Arm a timing probe for the NEXT gpt_forward (or gpt_backward) on this model: ev_start
  * (cudaEvent_t) is recorded on the forward's stream just before the kernel of
  * `step` (in block `layer`; ignored for steps outside the blocks) and ev_stop
  * just after it. The probe disarms after that forward. Pass ev_start == NULL
@@ -222,8 +235,10 @@ int gpt_sample(const float* d_logits, int32_t B, int32_t V, float temperature, i
  * buffers, overwriting the previous call's. The tied token table's gradient
  * is the sum of its embedding and head shares ("第 25 章 从小 GPT 到 GPT-2"
  * §25.4). B*T must be a multiple of 8 (GPT_EINVAL), T <= ctx (GPT_ESEQ),
- * B*T <= max_tokens. The first call allocates the workspace synchronously
- * (about 6 GB for GPT-2 small at 16384 tokens; GPT_ENOMEM on failure); later
+ * B*T <= max_tokens. The first call allocates the workspace synchronously:
+ * every block's activations at max_tokens, the gradients, transposed weights
+ * and the head's dz (about 11 GB for GPT-2 small at 16384 tokens; GPT_ENOMEM
+ * on failure); later
  * calls are stream-ordered. Token and target errors are reported by
  * gpt_status, as for gpt_forward.
  */
