@@ -40,6 +40,7 @@ struct gpt_layer_act {
                                      // out, ln_2 output (post-norm: n), c_fc pre- and post-GELU
   float *s1, *n, *s2;            // fp32: x + attention branch; post-norm: LN1(s1), n + MLP branch
   CUtensorMap A_a1, A_y, A_a2, A_g;        // as GEMM A operands
+  CUtensorMap K_a1, K_y, K_a2, K_g;        // as MN-major operands of the weight-gradient products
   CUtensorMap C_qkv, C_u, C_g, Q3;         // as epilogue outputs; qkv as the attention input
 };
 
@@ -59,13 +60,12 @@ struct gpt_train {
   // gradients of activations
   float *dx, *da;
   void *dxb, *dyb, *dqkv, *du;
-  void *dxT, *gT, *duT, *a2T, *yT, *a1T, *dqkvT, *hT;
   float *lse2, *dsum;
-  void *dz, *dzT;
+  void* dz;
   // activation maps, for one (B, T)
   int mB = -1, mT = -1;
-  CUtensorMap A_dz, A_dzT, A_dxT, A_dxb, A_duT, A_du, A_dqkvT, A_dqkv;
-  CUtensorMap B_hT, B_gT, B_a2T, B_yT, B_a1T;
+  CUtensorMap A_dz, A_dxb, A_du, A_dqkv;
+  CUtensorMap K_dz, K_h, K_dxb, K_du, K_dqkv;    // MN-major operands (64-row boxes)
   CUtensorMap C_dz, C_du, C_dyb, C_da, C_dx;
   int launches = 0;
 };
@@ -143,18 +143,9 @@ int alloc_train(gpt_model* m) {
     t->dyb = cv.take(Mx * C * 2);
     t->dqkv = cv.take(Mx * 3 * C * 2);
     t->du = cv.take(Mx * F * 2);
-    t->dxT = cv.take(C * Mx * 2);
-    t->gT = cv.take(F * Mx * 2);
-    t->duT = cv.take(F * Mx * 2);
-    t->a2T = cv.take(C * Mx * 2);
-    t->yT = cv.take(C * Mx * 2);
-    t->a1T = cv.take(C * Mx * 2);
-    t->dqkvT = cv.take(3 * C * Mx * 2);
-    t->hT = cv.take(C * Mx * 2);
     t->lse2 = static_cast<float*>(cv.take(Mx * c.H * 4));
     t->dsum = static_cast<float*>(cv.take(Mx * c.H * 4));
     t->dz = cv.take(Mx * Vp * 2);
-    t->dzT = cv.take(V * Mx * 2);
   };
   Carve sizing;
   layout(sizing);
@@ -217,14 +208,13 @@ int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
   const gpt_config& c = m->cfg;
   const uint64_t M = static_cast<uint64_t>(B) * T, C = c.C, F = c.ffn, V = c.V, Vp = t->Vp;
   const uint32_t BA = kGemmBM, BB = gemm_tc_bn();
+  const uint32_t BK = kGemmBK;
   bool ok =
-      make_tmap_2d_bf16(&t->A_dz, t->dz, M, V, BA, Vp) && make_tmap_2d_bf16(&t->A_dzT, t->dzT, V, M, BA) &&
-      make_tmap_2d_bf16(&t->A_dxT, t->dxT, C, M, BA) && make_tmap_2d_bf16(&t->A_dxb, t->dxb, M, C, BA) &&
-      make_tmap_2d_bf16(&t->A_duT, t->duT, F, M, BA) && make_tmap_2d_bf16(&t->A_du, t->du, M, F, BA) &&
-      make_tmap_2d_bf16(&t->A_dqkvT, t->dqkvT, 3 * C, M, BA) && make_tmap_2d_bf16(&t->A_dqkv, t->dqkv, M, 3 * C, BA) &&
-      make_tmap_2d_bf16(&t->B_hT, t->hT, C, M, BB) && make_tmap_2d_bf16(&t->B_gT, t->gT, F, M, BB) &&
-      make_tmap_2d_bf16(&t->B_a2T, t->a2T, C, M, BB) && make_tmap_2d_bf16(&t->B_yT, t->yT, C, M, BB) &&
-      make_tmap_2d_bf16(&t->B_a1T, t->a1T, C, M, BB) &&
+      make_tmap_2d_bf16(&t->A_dz, t->dz, M, V, BA, Vp) && make_tmap_2d_bf16(&t->A_dxb, t->dxb, M, C, BA) &&
+      make_tmap_2d_bf16(&t->A_du, t->du, M, F, BA) && make_tmap_2d_bf16(&t->A_dqkv, t->dqkv, M, 3 * C, BA) &&
+      make_tmap_2d_bf16(&t->K_dz, t->dz, M, V, BK, Vp) && make_tmap_2d_bf16(&t->K_h, m->a, M, C, BK) &&
+      make_tmap_2d_bf16(&t->K_dxb, t->dxb, M, C, BK) && make_tmap_2d_bf16(&t->K_du, t->du, M, F, BK) &&
+      make_tmap_2d_bf16(&t->K_dqkv, t->dqkv, M, 3 * C, BK) &&
       make_tmap_2d(&t->C_dz, t->dz, 2, M, V, 64, kEpiRows, Vp) &&
       make_tmap_2d(&t->C_du, t->du, 2, M, F, 64, kEpiRows) && make_tmap_2d(&t->C_dyb, t->dyb, 2, M, C, 64, kEpiRows) &&
       make_tmap_2d(&t->C_da, t->da, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_dx, t->dx, 4, M, C, 32, kEpiRows);
@@ -232,6 +222,8 @@ int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
     gpt_layer_act& q = t->la[l];
     ok = make_tmap_2d_bf16(&q.A_a1, q.a1, M, C, BA) && make_tmap_2d_bf16(&q.A_y, q.y, M, C, BA) &&
          make_tmap_2d_bf16(&q.A_a2, q.a2, M, C, BA) && make_tmap_2d_bf16(&q.A_g, q.g, M, F, BA) &&
+         make_tmap_2d_bf16(&q.K_a1, q.a1, M, C, BK) && make_tmap_2d_bf16(&q.K_y, q.y, M, C, BK) &&
+         make_tmap_2d_bf16(&q.K_a2, q.a2, M, C, BK) && make_tmap_2d_bf16(&q.K_g, q.g, M, F, BK) &&
          make_tmap_2d(&q.C_qkv, q.qkv, 2, M, 3 * C, 64, kEpiRows) && make_tmap_2d(&q.C_u, q.u, 2, M, F, 64, kEpiRows) &&
          make_tmap_2d(&q.C_g, q.g, 2, M, F, 64, kEpiRows) && make_tmap_qkv(&q.Q3, q.qkv, B, T, 3 * C, C / c.H);
   }
@@ -245,8 +237,9 @@ int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
   return GPT_OK;
 }
 
-// A weight-gradient product: out [N0, N1] fp32 += A [N0, M] . B [N1, M]^T over the M tokens,
-// split along M so that about two units per CTA are in flight.
+// A weight-gradient product: out [N0, N1] fp32 += A^T B summed over the M tokens, A [M, N0] and
+// B [M, N1] the activations as stored (MN-major operands, maps with 64-row boxes), split along M
+// so that about two units per CTA are in flight.
 int grad_gemm(gpt_model* m, const CUtensorMap& A, const CUtensorMap& Bm, const CUtensorMap& out_map, float* out,
               int N0, int N1, int M, cudaStream_t s) {
   GemmArgs a{};
@@ -255,6 +248,7 @@ int grad_gemm(gpt_model* m, const CUtensorMap& A, const CUtensorMap& Bm, const C
   a.ldo = N1;
   a.err = m->err;
   a.m_fastest = (N1 > N0) ? 1 : 0;
+  a.mn_major = 1;
   const int tiles = ((N0 + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(N1);
   const int KB = (M + kGemmBK - 1) / kGemmBK;
   int ks = (2 * m->num_sms + tiles - 1) / tiles;
@@ -329,10 +323,8 @@ int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStre
   a.m_fastest = 1;
   a.b_const = 1;                          // the token table
   BWS(GPT_STEP_B_DZ, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, t->C_dz, a, EPI_CE_GRAD, m->num_sms, s), "head grad"));
-  BW(cu(launch_transpose_bf16(t->dz, M, V, t->Vp, t->dzT, M, s), "transpose dz"));
-  BW(cu(launch_transpose_bf16(m->a, M, C, C, t->hT, M, s), "transpose h"));
   // dE += dz^T h (the head's share of the tied table)
-  BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->A_dzT, t->B_hT, t->tg_wte, t->g_wte, V, C, M, s));
+  BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->K_dz, t->K_h, t->tg_wte, t->g_wte, V, C, M, s));
   // dh = dz E (fp32 into da)
   GPT_CUDA(cudaMemsetAsync(t->da, 0, static_cast<size_t>(M) * C * sizeof(float), s));
   BWS(GPT_STEP_B_DH, -1, gemm_bf16(m, t->A_dz, t->tb_wteT, t->C_da, M, C, V, nullptr, t->da, EPI_BIAS_RESID, s));
@@ -433,14 +425,12 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
   if (!pre)      // x_{l+1} = LN2(s2): d loss / d s2, in place
     BW(cu(launch_layernorm_bwd(q.s2, w.ln2_g, t->dx, t->dx, 0, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
   // MLP: s2 = n + g W_mp^T + b_mp, g = gelu(u), u = a2 W_fc^T + b_fc
-  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s, g.mp_b), "cast dx, db_mp"));
-  BW(cu(launch_transpose_bf16(q.g, M, F, F, t->gT, M, s), "transpose g"));
-  BWS(GPT_STEP_B_MP_W, l, grad_gemm(m, t->A_dxT, t->B_gT, g.tg_mp_w, g.mp_w, C, F, M, s));
+  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, nullptr, 0, s, g.mp_b), "cast dx, db_mp"));
+  BWS(GPT_STEP_B_MP_W, l, grad_gemm(m, t->K_dxb, q.K_g, g.tg_mp_w, g.mp_w, C, F, M, s));
   BWS(GPT_STEP_B_DG, l, gemm_bf16(m, t->A_dxb, g.tb_mp_wT, t->C_du, M, F, C, nullptr, t->du, EPI_BIAS_OUT, s));
   BW(cu(launch_gelu_bwd(q.u, t->du, t->du, static_cast<size_t>(M) * F, c.gelu, m->num_sms, s), "gelu'"));
-  BW(cu(launch_transpose_bf16(t->du, M, F, F, t->duT, M, s, g.fc_b), "transpose du, db_fc"));
-  BW(cu(launch_transpose_bf16(q.a2, M, C, C, t->a2T, M, s), "transpose a2"));
-  BWS(GPT_STEP_B_FC_W, l, grad_gemm(m, t->A_duT, t->B_a2T, g.tg_fc_w, g.fc_w, F, C, M, s));
+  BW(cu(launch_colsum(t->du, 1, M, F, F, g.fc_b, m->num_sms, s), "db_fc"));
+  BWS(GPT_STEP_B_FC_W, l, grad_gemm(m, t->K_du, q.K_a2, g.tg_fc_w, g.fc_w, F, C, M, s));
   if (pre) {
     // da2 = du W_fc; s1 -> LN2 -> a2: dx += LN2'(da2)
     BWS(GPT_STEP_B_DA2, l, gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_da, M, C, F, nullptr, t->da, EPI_F32_OUT, s));
@@ -451,16 +441,14 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
     BW(cu(launch_layernorm_bwd(q.s1, w.ln1_g, t->dx, t->dx, 0, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
   }
   // attention: s1 = x + y W_proj^T + b_proj, y = attention(qkv), qkv = a1 W_attn^T + b_attn
-  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, t->dxT, M, s, g.proj_b), "cast ds1, db_proj"));
-  BW(cu(launch_transpose_bf16(q.y, M, C, C, t->yT, M, s), "transpose y"));
-  BWS(GPT_STEP_B_PROJ_W, l, grad_gemm(m, t->A_dxT, t->B_yT, g.tg_proj_w, g.proj_w, C, C, M, s));
+  BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, nullptr, 0, s, g.proj_b), "cast ds1, db_proj"));
+  BWS(GPT_STEP_B_PROJ_W, l, grad_gemm(m, t->K_dxb, q.K_y, g.tg_proj_w, g.proj_w, C, C, M, s));
   BWS(GPT_STEP_B_DY, l, gemm_bf16(m, t->A_dxb, g.tb_proj_wT, t->C_dyb, M, C, C, nullptr, t->dyb, EPI_BIAS_OUT, s));
   BWS(GPT_STEP_B_ATTN, l,
       cu(launch_attention_bwd(q.qkv, q.y, t->dyb, t->dqkv, t->lse2, t->dsum, B, T, H, C / H, s), "attention'"));
   ++t->launches;                                                                                   // two kernels
-  BW(cu(launch_transpose_bf16(t->dqkv, M, 3 * C, 3 * C, t->dqkvT, M, s, g.attn_b), "transpose dqkv, db_attn"));
-  BW(cu(launch_transpose_bf16(q.a1, M, C, C, t->a1T, M, s), "transpose a1"));
-  BWS(GPT_STEP_B_ATTN_W, l, grad_gemm(m, t->A_dqkvT, t->B_a1T, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
+  BW(cu(launch_colsum(t->dqkv, 1, M, 3 * C, 3 * C, g.attn_b, m->num_sms, s), "db_attn"));
+  BWS(GPT_STEP_B_ATTN_W, l, grad_gemm(m, t->K_dqkv, q.K_a1, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
   if (pre) {
     // da1 = dqkv W_attn; x -> LN1 -> a1: dx += LN1'(da1)
     BWS(GPT_STEP_B_DA1, l, gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_da, M, C, 3 * C, nullptr, t->da, EPI_F32_OUT, s));

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const void* __restrict
   }
   __syncthreads();
   if (colsum && threadIdx.x < kT64 && c0 + threadIdx.x < cols) atomicAdd(colsum + c0 + threadIdx.x, csum[threadIdx.x]);
+  if (dstT == nullptr) return;                             // a cast (block-uniform)
   for (int i = threadIdx.x; i < kT64 * 8; i += 256) {
     const int cc = i & 63, ch = i >> 6;
     const int oc = c0 + cc, orow = r0 + ch * 8;          // output row oc, columns orow .. orow + 7
@@ -379,8 +380,7 @@ cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, 
 cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s,
                                   float* colsum) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  if (dstT == nullptr) {                                   // a plain cast
-    if (colsum) return cudaErrorInvalidValue;
+  if (dstT == nullptr && colsum == nullptr) {              // a plain cast
     const dim3 grid((cols + kTr - 1) / kTr, (rows + kTr - 1) / kTr), block(kTr, 8);
     if (grid.y > 65535u) return cudaErrorInvalidValue;
     return launch_k(cast_transpose_kernel, grid, block, 0, s, src, rows, cols, static_cast<uint16_t*>(dst),
@@ -388,7 +388,7 @@ cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* ds
   }
   const dim3 grid((cols + kT64 - 1) / kT64, (rows + kT64 - 1) / kT64);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
-  const int vec = (cols % 8 == 0) && (ldt % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
+  const int vec = (cols % 8 == 0) && (dstT == nullptr || ldt % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
                   (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (reinterpret_cast<uintptr_t>(dstT) % 16 == 0);
   return launch_k(transpose64_kernel<true>, grid, dim3(256), 0, s, static_cast<const void*>(src), rows, cols, cols,
                   static_cast<uint16_t*>(dst), static_cast<uint16_t*>(dstT), ldt, vec, colsum);

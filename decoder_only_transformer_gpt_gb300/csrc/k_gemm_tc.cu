@@ -380,7 +380,11 @@ __device__ __forceinline__ SegIter make_seg_iter(bool sk, bool ks, int num_tiles
 // its own instantiation, so whole-tile launches carry no segment bookkeeping.
 // (The stream-K notes below say SK for MODE == 1.) Whole-tile launches use their
 // own instantiation, whose loops have no segment bookkeeping.
-template <int EPI, int MODE>
+// MN: both operands MN-major (A stored [K][M], W stored [K][N], M and N contiguous): a stage
+// holds BM/64 (A) and BN/64 (W) boxes of 64 (M or N) x 64 (K) at 8 KB strides, the MMA reads
+// them with the MN-major 128-byte-swizzle layout (64-element atoms 8 KB apart, 8-row K groups
+// 1 KB apart), and a K step of 16 advances 16 rows (2 KB).
+template <int EPI, int MODE, bool MN = false>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -432,6 +436,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t phase = 0;
       uint32_t issued = 0, last_par = 0;
       bool ok = true;
+      auto load_a = [&](int st, int kb, int mb) {
+        if (MN) {
+#pragma unroll
+          for (int i = 0; i < BM / 64; ++i)
+            tma_load_2d(sA + st * A_BYTES + i * 8192, &tmA, &bars->full[st], mb * BM + 64 * i, kb * BK);
+        } else {
+          tma_load_2d(sA + st * A_BYTES, &tmA, &bars->full[st], kb * BK, mb * BM);
+        }
+      };
+      auto load_b = [&](int st, int kb, int nb) {
+        if (MN) {
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(sB + st * B_BYTES + i * 8192, &tmB, &bars->full[st], nb * BN + 64 * i, kb * BK);
+        } else {
+          tma_load_2d(sB + st * B_BYTES, &tmB, &bars->full[st], kb * BK, nb * BN);
+        }
+      };
       // Weights (B, when b_const) do not depend on the previous kernel: the first tile's
       // first stages of B are requested before waiting for that kernel to finish.
       int pre = 0;
@@ -445,7 +467,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           pre = (kb10 - kb00) < STAGES ? (kb10 - kb00) : STAGES;
           for (int i = 0; i < pre; ++i) {
             mbar_arrive_expect_tx(&bars->full[i], STAGE_BYTES);
-            tma_load_2d(sB + i * B_BYTES, &tmB, &bars->full[i], (kb00 + i) * BK, nb0 * BN);
+            load_b(i, kb00 + i, nb0);
           }
         }
       }
@@ -457,12 +479,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = kb0; kb < kb1; ++kb) {
           if (pre > 0) {                // stage armed and its B requested above
             --pre;
-            tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
+            load_a(stage, kb, mb);
           } else {
             if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
             mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, mb * BM);
-            tma_load_2d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, nb * BN);
+            load_a(stage, kb, mb);
+            load_b(stage, kb, nb);
           }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -476,11 +498,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp; one elected lane issues)
     {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, false);
-      // base descriptors of stage 0 (K-major, 128-byte swizzle, 8-row groups 1024 bytes apart);
-      // the start address is the low field, so other stages and K steps are plain adds
-      const uint64_t da0 = smem_desc(smem_u32(sA), 16, 1024, SWZ_128B);
-      const uint64_t db0 = smem_desc(smem_u32(sB), 16, 1024, SWZ_128B);
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, MN) | (MN ? (1u << 15) : 0u);   // bit 15: A MN-major
+      // base descriptors of stage 0 (K-major: 8-row groups 1024 bytes apart; MN-major: 64-element
+      // atoms 8 KB apart, 8-row K groups 1024 bytes apart; 128-byte swizzle); the start address
+      // is the low field, so other stages and K steps are plain adds
+      const uint64_t da0 = smem_desc(smem_u32(sA), MN ? 8192 : 16, 1024, SWZ_128B);
+      const uint64_t db0 = smem_desc(smem_u32(sB), MN ? 8192 : 16, 1024, SWZ_128B);
+      constexpr uint64_t kstep = MN ? (16 * 128) >> 4 : 2;    // one K step of 16, in 16-byte units
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -499,7 +523,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint64_t db = db0 + static_cast<uint64_t>((stage * B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_bf16_warp(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            tc_mma_bf16_warp(d_tmem, da + kstep * k, db + kstep * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           tc_commit_warp(&bars->empty[stage]);           // frees the stage once these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -698,17 +722,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <int EPI, int MODE>
+template <int EPI, int MODE, bool MN = false>
 cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                         int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, MODE, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<EPI>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(gemm_tc_kernel<EPI, MODE>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
+  return launch_k(gemm_tc_kernel<EPI, MODE, MN>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
 }
 
 template <int EPI>
@@ -720,6 +744,22 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   const int grid = tiles < grid_limit ? tiles : grid_limit;
   if (grid <= 0) return cudaSuccess;
   constexpr bool kSplit = EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_F32_OUT;
+  if (a.mn_major) {                   // weight gradients: both operands MN-major
+    if constexpr (EPI == EPI_BIAS_RESID) {
+      if (a.bias != nullptr) return cudaErrorInvalidValue;
+      if (a.ksplit > 1) {
+        if (a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;
+        const long long units = static_cast<long long>(tiles) * a.ksplit;
+        const int g2 = units < grid_limit ? static_cast<int>(units) : grid_limit;
+        return launch_inst<EPI, 2, true>(tmA, tmB, tmC, a, g2, s);
+      }
+      if (a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
+        return launch_inst<EPI, 1, true>(tmA, tmB, tmC, a, grid, s);
+      return launch_inst<EPI, 0, true>(tmA, tmB, tmC, a, grid, s);
+    } else {
+      return cudaErrorInvalidValue;
+    }
+  }
   if (a.ksplit > 1) {                 // split-K: (tile, K slice) units, reduce-add of each partial
     if constexpr (EPI == EPI_BIAS_RESID) {
       if (a.bias != nullptr || a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;

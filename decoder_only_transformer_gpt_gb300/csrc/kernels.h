@@ -49,6 +49,8 @@ struct GemmArgs {
   // units, slice s covering K blocks [s KB / ksplit, (s + 1) KB / ksplit); each adds its partial
   // into the fp32 output with the reduce-add store.
   int ksplit;
+  int mn_major;             // EPI_BIAS_RESID: both operands MN-major, A stored [K, M] and W [K, N] row-major
+                            //   (tensor maps with 64 x 64 boxes): out[M, N] += A^T W summed over K
   int b_const;              // 1: W was not written by the previous kernel on the stream (weights), so its
                             //    first stages may be requested before waiting for that kernel
   const float* row_nll;     // EPI_CE_GRAD: [M] per-row loss; with ztgt gives the row's logsumexp
