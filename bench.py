@@ -62,14 +62,23 @@ NCU_TRAFFIC = {
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
                   "digest": "42a0a54118b079c59411ffb054c71c4fbf5d5995"},
-    "head": {"bytes": 102.546432e6 + 17.707008e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+    "head": {"bytes": 102.552576e6 + 17.459456e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "2b4ddb1cbd737796727556269c4b582bb97632cb"},
-    "mlp_proj": {"bytes": 163.247872e6 + 25.978880e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+             "digest": "ef819a3571bd397b5ca4909bae45f9836d4a6c48"},
+    "mlp_proj": {"bytes": 163.005440e6 + 25.308672e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                 "digest": "2b4ddb1cbd737796727556269c4b582bb97632cb"},
+                 "digest": "ef819a3571bd397b5ca4909bae45f9836d4a6c48"},
+}
+
+# The same for the training step's dominant step at B = 16, T = 1024: the attention derivative's
+# two kernels, captured at B = 2 and scaled by the 8x more (sequence, head) pairs they process.
+TRAIN_NCU_TRAFFIC = {
+    "b_attn": {"bytes": 8 * (15.751e6 + 12.795e6), "profile": "profiles/attention_bwd_b2_t1024_h12_d64.md",
+               "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_bwd.cu",
+                           "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
+               "digest": "b005493621e7422fd64c3bb77462ffad5f82f7a7"},
 }
 
 
@@ -667,6 +676,11 @@ def run_train(args, rank, world, local_rank):
                         "unit": "TFLOP/s", "frac": a / peak_t})
     dom_avg = statistics.mean(dom_ms)
     achieved = breakdown[dom]["work"] / (dom_avg / 1e3) / 1e12
+    traffic = None
+    tr = TRAIN_NCU_TRAFFIC.get(dom)
+    if (tr is not None and args.model == "gpt2_small" and (B, T) == (16, 1024)
+            and source_digest(tr["sources"]) == tr["digest"]):
+        traffic = tr["bytes"]
     cpu = None if (args.no_cpu_baseline or world > 1) else train_cpu_baseline(wl, w, ids_np, tg_np)
     line = {
         "metric": f"{wl_label.split('_b')[0]} training forward+backward tokens/sec on 1 GB300", "value": value,
@@ -684,7 +698,7 @@ def run_train(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"kernel": dom_kernel, "step": dom, "bound": "tensor", "achieved": achieved, "peak": peak_t,
-                     "unit": "TFLOP/s", "frac": achieved / peak_t, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak_t, "traffic": traffic,
                      "algorithmic": breakdown[dom]["work"], "peak_source": f"{pk_src} bf16 sustained",
                      "avg_launch_ms": dom_avg, "launches_timed": len(dom_ms)},
         "kernels": kernels,

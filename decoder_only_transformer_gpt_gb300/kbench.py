@@ -4,6 +4,10 @@
     python -m decoder_only_transformer_gpt_gb300.kbench gemm --M 16384 --N 768 --K 768 --epi 2
     python -m decoder_only_transformer_gpt_gb300.kbench head --M 16384 --V 50257 --C 768
     python -m decoder_only_transformer_gpt_gb300.kbench layernorm --M 16384 --C 768
+    python -m decoder_only_transformer_gpt_gb300.kbench train --B 16 --T 1024
+
+(`train`: one gpt_backward call, forward + loss + every gradient, of GPT-2 small on
+seeded synthetic tokens.)
 
 Inputs are random device tensors; the figure printed is algorithmic TFLOP/s
 (or GB/s for the row-wise kernels) over the mean launch time.
@@ -32,7 +36,7 @@ def _time(fn, warmup, iters):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["attention", "gemm", "head", "layernorm"])
+    ap.add_argument("kernel", choices=["attention", "gemm", "head", "layernorm", "train"])
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=1024)
     ap.add_argument("--H", type=int, default=12)
@@ -73,6 +77,19 @@ def main():
         ms = _time(lambda: binding.lmhead_ce(h, E, tg, nll), a.warmup, a.iters)
         flop = 2.0 * a.M * a.V * a.C
         out = {"kernel": "head_ce", "shape": [a.M, a.V, a.C], "ms": ms, "tflops": flop / ms / 1e9}
+    elif a.kernel == "train":
+        from workloads import workload
+        from workloads.generate import generate
+        wl = workload("gpt2_small")
+        w, ids, tg = generate(wl, B=a.B, T=a.T)
+        m = binding.GPTModel(wl.cfg, w, a.B * a.T)
+        d_ids, d_tg = torch.from_numpy(ids).to(dev), torch.from_numpy(tg).to(dev)
+        loss = torch.zeros(1, device=dev)
+        ms = _time(lambda: m.backward(d_ids, d_tg, loss, check=False), a.warmup, a.iters)
+        m.status()
+        out = {"kernel": "train", "shape": [a.B, a.T], "ms": ms, "tokens_per_s": a.B * a.T / ms * 1e3,
+               "launches_per_call": m.lib.gpt_last_launch_count(m.handle)}
+        m.close()
     else:
         x = torch.randn(a.M, a.C, device=dev)
         g = torch.ones(a.C, device=dev)
