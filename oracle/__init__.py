@@ -13,7 +13,7 @@ from .gpt_oracle import (
 )
 from .gpt_grad import (
     linear_backward, layernorm_backward, gelu_backward, attention_backward,
-    causal_self_attention_backward, cross_entropy_backward, embed_backward, backward,
+    causal_self_attention_backward, cross_entropy_backward, embed_backward, backward, adamw_step,
 )
 
 __all__ = [
@@ -21,5 +21,5 @@ __all__ = [
     "causal_self_attention", "block_pre_norm", "block_post_norm", "forward_hidden",
     "lm_head", "cross_entropy_rows", "cross_entropy", "forward", "sample_next",
     "linear_backward", "layernorm_backward", "gelu_backward", "attention_backward",
-    "causal_self_attention_backward", "cross_entropy_backward", "embed_backward", "backward",
+    "causal_self_attention_backward", "cross_entropy_backward", "embed_backward", "backward", "adamw_step",
 ]

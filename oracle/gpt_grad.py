@@ -211,3 +211,44 @@ def backward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets: np.ndarray, part
         grads["wte_embed"] = dE_embed
         grads["wte_head"] = dE_head
     return loss, grads
+
+
+# ---------------------------------------------------------------- the optimiser step
+
+def adamw_step(w: dict, grads: dict, state: dict, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+               eps: float = 1e-8, weight_decay: float = 0.0) -> dict:
+    """One AdamW update of every parameter, in place on fp64 copies of the weights.
+
+    "Day 16 从零组装 MiniGPT" (the training loop: loss, backward, AdamW, parameters change, repeated) and
+    "预训练一个 Mini GPT" 训练循环 (the optimiser step after back-propagation; GPT-2 uses Adam). The update is
+    Adam with decoupled weight decay: p <- p - lr wd p; m <- b1 m + (1 - b1) g; v <- b2 v + (1 - b2) g^2;
+    p <- p - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), t the step count from 1. Reading: the decay
+    applies to the weight matrices and the two tables, not to biases and LayerNorm parameters.
+    state: {} on the first call; it keeps the step count and both moments per tensor.
+    Returns w (its arrays replaced by fp64 arrays holding the new values).
+    """
+    t = state.get("t", 0) + 1
+    state["t"] = t
+    bc1, bc2 = 1.0 - beta1 ** t, 1.0 - beta2 ** t
+
+    def upd(key, p, g, decay):
+        p = np.asarray(p, np.float64).copy()
+        g = np.asarray(g, np.float64)
+        m, v = state.get(key, (np.zeros_like(p), np.zeros_like(p)))
+        if decay:
+            p -= lr * weight_decay * p
+        m = beta1 * m + (1.0 - beta1) * g
+        v = beta2 * v + (1.0 - beta2) * g * g
+        p -= lr * (m / bc1) / (np.sqrt(v / bc2) + eps)
+        state[key] = (m, v)
+        return p
+
+    for k in ("wte", "wpe"):
+        w[k] = upd(k, w[k], grads[k], True)
+    for k in ("lnf_g", "lnf_b"):
+        if k in grads:
+            w[k] = upd(k, w[k], grads[k], False)
+    for i, (p, gl) in enumerate(zip(w["layers"], grads["layers"])):
+        for k in list(p):
+            p[k] = upd(f"{i}.{k}", p[k], gl[k], k.endswith("_w"))
+    return w

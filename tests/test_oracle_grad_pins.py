@@ -321,3 +321,40 @@ def test_planted_grad_mistakes_are_caught(mistake, monkeypatch):
             return dx, (dw.T if dw.shape[0] == dw.shape[1] else dw[::-1]), db
         monkeypatch.setattr(gg, "linear_backward", bad)
     assert not _grad_pins_pass(), f"planted mistake {mistake} went unnoticed"
+
+
+# ---------------------------------------------------------------- the optimiser step
+
+def test_adamw_step_matches_torch_adamw():
+    # the written-out update against torch.optim.AdamW (fp64, CPU), three steps, decay on matrices only
+    torch = pytest.importorskip("torch")
+    cfg = _cfg(L=1)
+    w, ids, tg, rng = _model(cfg, seed=107)
+    names = [n for n, _ in _tensors(cfg, w)]
+    tp = {n: torch.tensor(a.copy(), dtype=torch.float64, requires_grad=True) for n, a in _tensors(cfg, w)}
+    decay = [tp[n] for n in names if n.endswith("_w") or n in ("wte", "wpe")]
+    rest = [tp[n] for n in names if not (n.endswith("_w") or n in ("wte", "wpe"))]
+    opt = torch.optim.AdamW([{"params": decay, "weight_decay": 0.1}, {"params": rest, "weight_decay": 0.0}],
+                            lr=3e-3, betas=(0.9, 0.95), eps=1e-8)
+    state = {}
+    for _ in range(3):
+        _, g = oracle.backward(cfg, w, ids, tg)
+        for n in names:
+            tp[n].grad = torch.tensor(_grad_of(g, n), dtype=torch.float64)
+        opt.step()
+        oracle.adamw_step(w, g, state, lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+        for n, a in _tensors(cfg, w):
+            assert np.allclose(a, tp[n].detach().numpy(), rtol=1e-12, atol=1e-14), n
+
+
+def test_adamw_first_step_moves_each_weight_by_lr():
+    # at t = 1, m / (1 - b1) = g and sqrt(v / (1 - b2)) = |g|: each weight moves by lr * sign(g) (eps aside)
+    cfg = _cfg(L=1)
+    w, ids, tg, _ = _model(cfg, seed=108)
+    before = {n: a.copy() for n, a in _tensors(cfg, w)}
+    _, g = oracle.backward(cfg, w, ids, tg)
+    oracle.adamw_step(w, g, {}, lr=1e-3, eps=1e-12)
+    for n, a in _tensors(cfg, w):
+        gr = _grad_of(g, n)
+        big = np.abs(gr) > 1e-6
+        assert np.allclose((before[n] - a)[big], 1e-3 * np.sign(gr[big]), rtol=1e-5), n
