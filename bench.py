@@ -575,11 +575,12 @@ def train_cpu_baseline(wl, w, ids, tg, budget_s: float = 20.0):
 
 
 def run_train(args, rank, world, local_rank):
-    """--train: tokens/s of a training step's forward + backward (gpt_backward: loss and the gradient
-    of every parameter; no optimiser update), a second measurement beside the forward line. FLOPs per
-    step = 3 x the forward's (the forward, then twice its products for the input and weight
-    gradients); the recomputed activations are not counted. The dominant probed step's launches are
-    timed inside the timed region for the roofline."""
+    """--train: tokens/s of a whole training step, a second measurement beside the forward line: the
+    forward and loss, the gradient of every parameter (gpt_backward) and one AdamW update of every
+    weight (gpt_adamw_step, lr 1e-4). FLOPs per step = 3 x the forward's (the forward, then twice its
+    products for the input and weight gradients); the extra c_fc launch and the optimiser's
+    elementwise work are not counted. The dominant probed step's launches are timed inside the timed
+    region for the roofline."""
     import torch
     from decoder_only_transformer_gpt_gb300 import binding
     from workloads import workload
@@ -598,10 +599,15 @@ def run_train(args, rank, world, local_rank):
     tg = torch.from_numpy(tg_np).to(dev)
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
+    def train_step():
         model.backward(ids, tg, loss, check=False)
+        n = lib.gpt_last_launch_count(model.handle)
+        model.adamw_step(1e-4, 0.9, 0.95, 1e-8, 0.1)
+        return n + lib.gpt_last_launch_count(model.handle)
+
+    for _ in range(args.warmup):
+        launches_per_step = train_step()
     model.status()
-    launches_per_step = lib.gpt_last_launch_count(model.handle)
     rte = RuntimeEvents()
     pa, pb = rte.create(), rte.create()
     breakdown = {}
@@ -610,8 +616,10 @@ def run_train(args, rank, world, local_rank):
         for layer in (range(cfg.L) if per_block else [-1]):
             lib.gpt_time_step(model.handle, sid, layer, pa, pb)
             model.backward(ids, tg, loss, check=False)
+            hits = lib.gpt_last_probe_hits(model.handle)
+            model.adamw_step(1e-4, 0.9, 0.95, 1e-8, 0.1)
             torch.cuda.synchronize()
-            if lib.gpt_last_probe_hits(model.handle) == 1:
+            if hits == 1:
                 times.append(rte.elapsed_ms(pa, pb))
         if times:
             breakdown[name] = {"launches_per_step": len(times), "avg_ms": statistics.mean(times),
@@ -632,7 +640,7 @@ def run_train(args, rank, world, local_rank):
     start.record(stream)
     for k in range(args.steps):
         lib.gpt_time_step(model.handle, dom_sid, dom_layer, ev0[k], ev1[k])
-        model.backward(ids, tg, loss, check=False)
+        train_step()
     stop.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -653,6 +661,7 @@ def run_train(args, rank, world, local_rank):
         d_ids.copy_(pin_ids, non_blocking=True)
         d_tg.copy_(pin_tg, non_blocking=True)
         model.backward(d_ids, d_tg, loss, check=False)
+        model.adamw_step(1e-4, 0.9, 0.95, 1e-8, 0.1)
         pin_loss.copy_(loss, non_blocking=True)
         torch.cuda.synchronize()
 
@@ -689,7 +698,7 @@ def run_train(args, rank, world, local_rank):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.model}_train_b{B}_t{T}", "B": B, "T": T, "V": cfg.V, "C": cfg.C, "H": cfg.H,
                    "L": cfg.L, "ids": "zipf(1.1) seed 4", "l2": "inputs larger than L2 (weights and activations)",
-                   "step": "forward + loss + gradient of every parameter (no optimiser update)",
+                   "step": "forward + loss + gradient of every parameter + AdamW update",
                    "parallelism": f"replicas x{world}"},
         "tflops": flops * args.steps * world / (ms_max / 1e3) / 1e12,
         "frac_of_peak": flops / (ms_max / args.steps / 1e3) / 1e12 / float(pk["bf16_tflops"]),

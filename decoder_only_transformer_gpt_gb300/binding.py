@@ -83,6 +83,9 @@ def load(path: str = LIB_PATH):
         "gpt_backward": (ctypes.c_int, [vp, vp, vp, i32, i32, vp, vp]),
         "gpt_grad": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(i64)]),
         "gpt_grad_copy": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
+        "gpt_adamw_step": (ctypes.c_int, [vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_float, vp]),
+        "gpt_master_copy": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
@@ -219,6 +222,19 @@ class GPTModel:
         assert out.numel() == n.value
         _check(self.lib.gpt_grad_copy(self.handle, param, layer, _ptr(out), _stream(stream)), "gpt_grad_copy")
         return out
+
+    def adamw_step(self, lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                   weight_decay: float = 0.0, stream=None) -> None:
+        """One AdamW update of the model's weights from the last backward's gradients."""
+        _check(self.lib.gpt_adamw_step(self.handle, lr, beta1, beta2, eps, weight_decay, _stream(stream)),
+               "gpt_adamw_step")
+
+    def master(self, name: str, layer: int = -1, stream=None):
+        """A copy of one parameter's fp32 master weight (after an AdamW step)."""
+        g = self.grad(name, layer, stream)            # same shape and numel
+        _check(self.lib.gpt_master_copy(self.handle, GRAD_PARAMS.index(name), layer, _ptr(g), _stream(stream)),
+               "gpt_master_copy")
+        return g
 
     def grads(self, stream=None) -> dict:
         """Every gradient, keyed like the weight dict ("layers" a list of per-block dicts)."""

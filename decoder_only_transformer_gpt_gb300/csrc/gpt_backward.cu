@@ -21,6 +21,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstring>
 #include <vector>
 
@@ -68,11 +69,19 @@ struct gpt_train {
   CUtensorMap K_dz, K_h, K_dxb, K_du, K_dqkv;    // MN-major operands (64-row boxes)
   CUtensorMap C_dz, C_du, C_dyb, C_da, C_dx;
   int launches = 0;
+  // AdamW state (allocated by the first gpt_adamw_step): fp32 master weights and both moments, in the
+  // gradients' layout, and the parameter segments
+  float *master = nullptr, *m1 = nullptr, *m2 = nullptr;
+  OptSeg* d_segs = nullptr;
+  int nseg = 0;
+  int opt_t = 0;
 };
 
 namespace gptgb {
 void free_train(gpt_model* m) {
   if (!m || !m->tr) return;
+  cudaFree(m->tr->master);
+  cudaFree(m->tr->d_segs);
   cudaFree(m->tr->buf);
   delete m->tr;
   m->tr = nullptr;
@@ -550,5 +559,98 @@ extern "C" int gpt_grad_copy(const gpt_model* m, int param, int layer, float* d_
   if (rc != GPT_OK) return rc;
   GPT_CUDA(cudaMemcpyAsync(d_dst, src, static_cast<size_t>(n) * sizeof(float), cudaMemcpyDeviceToDevice,
                            reinterpret_cast<cudaStream_t>(stream)));
+  return GPT_OK;
+}
+
+namespace {
+
+// The optimiser's segment table (gradient order) and state, once.
+int alloc_optimizer(gpt_model* m, gpt_train* t) {
+  const gpt_config& c = m->cfg;
+  const long long C = c.C, F = c.ffn;
+  std::vector<OptSeg> segs;
+  auto add = [&](const float* g, long long n, void* dst, bool matrix) {
+    if (dst == nullptr) return;
+    OptSeg sg;
+    sg.off = g - t->gbuf;
+    sg.n = n;
+    sg.dst = dst;
+    sg.bf16 = (matrix && m->bf16) ? 1 : 0;
+    sg.decay = matrix ? 1 : 0;
+    segs.push_back(sg);
+  };
+  add(t->g_wte, static_cast<long long>(c.V) * C, m->wte, true);
+  add(t->g_wpe, static_cast<long long>(c.ctx) * C, m->wpe, true);
+  add(t->g_lnf_g, C, m->lnf_g, false);
+  add(t->g_lnf_b, C, m->lnf_b, false);
+  for (int l = 0; l < c.L; ++l) {
+    const gpt_layer_grad& g = t->lg[l];
+    const gpt_layer_dev& w = m->layers[l];
+    add(g.ln1_g, C, w.ln1_g, false);
+    add(g.ln1_b, C, w.ln1_b, false);
+    add(g.attn_w, 3 * C * C, w.attn_w, true);
+    add(g.attn_b, 3 * C, w.attn_b, false);
+    add(g.proj_w, C * C, w.proj_w, true);
+    add(g.proj_b, C, w.proj_b, false);
+    add(g.ln2_g, C, w.ln2_g, false);
+    add(g.ln2_b, C, w.ln2_b, false);
+    add(g.fc_w, F * C, w.fc_w, true);
+    add(g.fc_b, F, w.fc_b, false);
+    add(g.mp_w, C * F, w.mp_w, true);
+    add(g.mp_b, C, w.mp_b, false);
+  }
+  const size_t n = t->grad_floats;
+  if (cudaMalloc(&t->master, 3 * n * sizeof(float)) != cudaSuccess) {
+    cudaGetLastError();
+    t->master = nullptr;
+    return GPT_ENOMEM;
+  }
+  t->m1 = t->master + n;
+  t->m2 = t->m1 + n;
+  if (cudaMalloc(&t->d_segs, segs.size() * sizeof(OptSeg)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(t->master);
+    t->master = nullptr;
+    t->d_segs = nullptr;
+    return GPT_ENOMEM;
+  }
+  GPT_CUDA(cudaMemcpy(t->d_segs, segs.data(), segs.size() * sizeof(OptSeg), cudaMemcpyHostToDevice));
+  t->nseg = static_cast<int>(segs.size());
+  return GPT_OK;
+}
+
+}  // namespace
+
+extern "C" int gpt_adamw_step(gpt_model* m, float lr, float beta1, float beta2, float eps, float weight_decay,
+                              void* stream) {
+  if (!m || !m->tr) return GPT_EINVAL;
+  if (!(beta1 >= 0.0f && beta1 < 1.0f && beta2 >= 0.0f && beta2 < 1.0f && eps > 0.0f)) return GPT_EINVAL;
+  gpt_train* t = m->tr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!t->master) {
+    const int rc = alloc_optimizer(m, t);
+    if (rc != GPT_OK) return rc;
+    GPT_CUDA(cudaMemsetAsync(t->m1, 0, 2 * t->grad_floats * sizeof(float), s));
+    GPT_CUDA(cudaMemsetAsync(t->master, 0, t->grad_floats * sizeof(float), s));
+    GPT_CUDA(launch_master_init(t->d_segs, t->nseg, t->master, s));
+  }
+  t->opt_t += 1;
+  const float bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta1), t->opt_t));
+  const float bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta2), t->opt_t));
+  GPT_CUDA(launch_adamw(t->d_segs, t->nseg, t->gbuf, t->master, t->m1, t->m2, lr, beta1, beta2, eps, weight_decay, bc1,
+                        bc2, s));
+  t->wT_ready = false;             // the transposed weights are made again by the next backward
+  m->launches = 1;
+  return GPT_OK;
+}
+
+extern "C" int gpt_master_copy(const gpt_model* m, int param, int layer, float* d_dst, void* stream) {
+  if (!d_dst || !m || !m->tr || !m->tr->master) return GPT_EINVAL;
+  float* g = nullptr;
+  int64_t n = 0;
+  const int rc = gpt_grad(m, param, layer, &g, &n);
+  if (rc != GPT_OK) return rc;
+  GPT_CUDA(cudaMemcpyAsync(d_dst, m->tr->master + (g - m->tr->gbuf), static_cast<size_t>(n) * sizeof(float),
+                           cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
   return GPT_OK;
 }

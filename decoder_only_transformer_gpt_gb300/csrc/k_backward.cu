@@ -364,7 +364,56 @@ __global__ void __launch_bounds__(256) layernorm_bwd_reg_kernel(const float* __r
   }
 }
 
+// AdamW over every parameter: block row blockIdx.y is one parameter tensor (segment), whose values
+// sit at [off, off + n) of the flat gradient / master / moment arrays and are written back to dst
+// (bf16 or fp32). Decoupled decay for decay segments; bias corrections bc1 = 1 - b1^t, bc2 = 1 - b2^t.
+__global__ void __launch_bounds__(256) adamw_kernel(const OptSeg* __restrict__ segs, const float* __restrict__ grad,
+                                                    float* __restrict__ master, float* __restrict__ m1,
+                                                    float* __restrict__ m2, float lr, float b1, float b2, float eps,
+                                                    float wd, float bc1, float bc2) {
+  pdl_wait();
+  pdl_trigger();
+  const OptSeg sg = segs[blockIdx.y];
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < sg.n; i += static_cast<long long>(gridDim.x) * 256) {
+    const long long k = sg.off + i;
+    const float g = grad[k];
+    float p = master[k];
+    if (sg.decay) p -= lr * wd * p;
+    const float mm = b1 * m1[k] + (1.0f - b1) * g;
+    const float vv = b2 * m2[k] + (1.0f - b2) * g * g;
+    p -= lr * (mm / bc1) / (sqrtf(vv / bc2) + eps);
+    master[k] = p;
+    m1[k] = mm;
+    m2[k] = vv;
+    if (sg.bf16) static_cast<uint16_t*>(sg.dst)[i] = f2bf(p);
+    else static_cast<float*>(sg.dst)[i] = p;
+  }
+}
+
+// master[off + i] = the parameter's current value (bf16 or fp32 storage).
+__global__ void __launch_bounds__(256) master_init_kernel(const OptSeg* __restrict__ segs, float* __restrict__ master) {
+  pdl_wait();
+  pdl_trigger();
+  const OptSeg sg = segs[blockIdx.y];
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < sg.n; i += static_cast<long long>(gridDim.x) * 256)
+    master[sg.off + i] = sg.bf16 ? bf2f(static_cast<const uint16_t*>(sg.dst)[i]) : static_cast<const float*>(sg.dst)[i];
+}
+
 }  // namespace
+
+cudaError_t launch_adamw(const OptSeg* segs, int nseg, const float* grad, float* master, float* m1, float* m2, float lr,
+                         float b1, float b2, float eps, float wd, float bc1, float bc2, cudaStream_t s) {
+  if (nseg <= 0) return cudaSuccess;
+  if (nseg > 65535) return cudaErrorInvalidValue;
+  return launch_k(adamw_kernel, dim3(64, nseg), dim3(256), 0, s, segs, grad, master, m1, m2, lr, b1, b2, eps, wd, bc1,
+                  bc2);
+}
+
+cudaError_t launch_master_init(const OptSeg* segs, int nseg, float* master, cudaStream_t s) {
+  if (nseg <= 0) return cudaSuccess;
+  if (nseg > 65535) return cudaErrorInvalidValue;
+  return launch_k(master_init_kernel, dim3(64, nseg), dim3(256), 0, s, segs, master);
+}
 
 cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s,
                                   float* colsum) {

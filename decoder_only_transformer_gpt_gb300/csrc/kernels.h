@@ -129,6 +129,19 @@ cudaError_t launch_embed_bwd(const float* dx0, const int32_t* ids, float* dE, fl
 cudaError_t launch_attention_bwd(const void* qkv, const void* y, const void* dy, void* dqkv, float* lse2, float* dsum,
                                  int B, int T, int H, int D, cudaStream_t s);
 
+// One parameter tensor for the optimiser: values [off, off + n) of the flat gradient, master and
+// moment arrays, stored at dst (bf16 when bf16 != 0, else fp32); decay: decoupled weight decay applies.
+struct OptSeg {
+  long long off, n;
+  void* dst;
+  int bf16, decay;
+};
+// AdamW over nseg segments (see adamw_kernel); bc1 = 1 - b1^t, bc2 = 1 - b2^t.
+cudaError_t launch_adamw(const OptSeg* segs, int nseg, const float* grad, float* master, float* m1, float* m2, float lr,
+                         float b1, float b2, float eps, float wd, float bc1, float bc2, cudaStream_t s);
+// master = the parameters' current values.
+cudaError_t launch_master_init(const OptSeg* segs, int nseg, float* master, cudaStream_t s);
+
 // ---- TMA descriptors (host)
 // 2-D row-major bf16 matrix [rows, cols] (row stride ld elements, 0 = cols) with a box of
 // box_rows x 64 columns, 128-byte swizzle.

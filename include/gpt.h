@@ -265,6 +265,23 @@ int gpt_grad(const gpt_model* m, int param, int layer, float** d_grad, int64_t* 
 /* Copies that gradient into caller device memory d_dst (numel fp32 values), stream-ordered. */
 int gpt_grad_copy(const gpt_model* m, int param, int layer, float* d_dst, void* stream);
 
+/*
+ * One AdamW step on every parameter from the last gpt_backward's gradients
+ * ("Day 16 从零组装 MiniGPT": loss, backward, AdamW, parameters change;
+ * "预训练一个 Mini GPT" 训练循环): p -= lr wd p (weight matrices and the two
+ * tables only), m = b1 m + (1 - b1) g, v = b2 v + (1 - b2) g^2,
+ * p -= lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), t counting calls
+ * from 1. The model keeps fp32 master weights and both moments (allocated
+ * synchronously by the first call, 3 x 4 bytes per parameter; GPT_ENOMEM on
+ * failure) and writes the updated values into its own weights (bf16 matrices
+ * rounded to nearest). GPT_EINVAL before the first gpt_backward or for betas
+ * outside [0, 1) or eps <= 0. Stream-ordered.
+ */
+int gpt_adamw_step(gpt_model* m, float lr, float beta1, float beta2, float eps, float weight_decay, void* stream);
+
+/* Copies one parameter's fp32 master weight (after a gpt_adamw_step) into d_dst. GPT_EINVAL before. */
+int gpt_master_copy(const gpt_model* m, int param, int layer, float* d_dst, void* stream);
+
 /* Synchronise the stream, read and clear the model's device error word. */
 int gpt_status(gpt_model* m, void* stream);
 

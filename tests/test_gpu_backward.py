@@ -155,3 +155,72 @@ def test_backward_errors(gpt_lib):
         mf.backward(dev_i32(ids), dev_i32(tg))
     assert e.value.code == binding.GPT_ECONFIG
     mf.close()
+
+
+# ---- the optimiser step
+
+def _w64(w):
+    return {k: (np.asarray(v, np.float64).copy() if k != "layers" else
+                [{n: np.asarray(a, np.float64).copy() for n, a in p.items()} for p in v]) for k, v in w.items()}
+
+
+def test_adamw_step_against_oracle_and_next_gradient(gpt_lib):
+    # one AdamW step from the GPU's own gradients equals the oracle's update (fp32 vs fp64); the next
+    # backward then runs on the updated weights (bf16 matrices) and matches the oracle's gradient there
+    from decoder_only_transformer_gpt_gb300 import binding
+    from workloads import round_to_bf16
+    cfg = GPTConfig(V=300, C=128, H=2, L=2, ctx=80, ffn=512)
+    rng = np.random.Generator(np.random.PCG64(55))
+    w = make_weights(cfg, rng, affine="random", wstd=0.05)
+    ids, tg = make_tokens(cfg.V, 2, 64, rng)
+    m = binding.GPTModel(cfg, w, 128)
+    d_ids, d_tg = dev_i32(ids), dev_i32(tg)
+    m.backward(d_ids, d_tg)
+    g = m.grads()
+    gh = {k: host(v) for k, v in g.items() if k != "layers"}
+    gh["layers"] = [{k: host(v) for k, v in p.items()} for p in g["layers"]]
+    lr, b1, b2, eps, wd = 1e-2, 0.9, 0.95, 1e-8, 0.1
+    m.adamw_step(lr, b1, b2, eps, wd)
+    want = oracle.adamw_step(_w64(w), gh, {}, lr, b1, b2, eps, wd)
+    got = {k: host(m.master(k)) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
+    got["layers"] = [{k: host(m.master(k, l)) for k in want["layers"][l]} for l in range(cfg.L)]
+    for name, a, r in _pairs(cfg, got, want):
+        assert np.max(np.abs(a - r)) <= 1e-6 + 1e-3 * lr, name
+    # the weights the GPU now holds: bf16 matrices and tables, fp32 vectors
+    w1 = {k: (round_to_bf16(got[k]) if k in ("wte", "wpe") else got[k].astype(np.float32))
+          for k in ("wte", "wpe", "lnf_g", "lnf_b")}
+    w1["layers"] = [{k: (round_to_bf16(v) if k.endswith("_w") else v.astype(np.float32)) for k, v in p.items()}
+                    for p in got["layers"]]
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    m.backward(d_ids, d_tg, loss)
+    g2 = m.grads()
+    lref, ref = oracle.backward(cfg, w1, ids, tg)
+    assert abs(float(loss.item()) - lref) <= TLOSS
+    g2h = {k: host(v) for k, v in g2.items() if k != "layers"}
+    g2h["layers"] = [{k: host(v) for k, v in p.items()} for p in g2["layers"]]
+    for name, a, r in _pairs(cfg, g2h, ref):
+        nr = np.linalg.norm(r)
+        assert nr == 0.0 or np.linalg.norm(a - r) / nr <= REL, name
+    m.close()
+
+
+def test_overfit_one_batch_on_the_gpu(gpt_lib):
+    # the pages' sanity check before real training: repeated steps on one batch drive its loss down
+    from decoder_only_transformer_gpt_gb300 import binding
+    cfg = GPTConfig(V=300, C=128, H=2, L=2, ctx=80, ffn=512)
+    rng = np.random.Generator(np.random.PCG64(56))
+    w = make_weights(cfg, rng)
+    ids, tg = make_tokens(cfg.V, 4, 64, rng)
+    m = binding.GPTModel(cfg, w, 256)
+    d_ids, d_tg = dev_i32(ids), dev_i32(tg)
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    losses = []
+    for _ in range(60):
+        m.backward(d_ids, d_tg, loss, check=False)
+        losses.append(float(loss.item()))
+        m.adamw_step(3e-3, 0.9, 0.95, 1e-8, 0.0)
+    m.status()
+    m.close()
+    print(f"\nloss {losses[0]:.3f} -> {losses[-1]:.3f}")
+    assert abs(losses[0] - np.log(cfg.V)) < 0.05           # about ln V at initialisation
+    assert losses[-1] < 0.3 * losses[0]
