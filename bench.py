@@ -537,7 +537,7 @@ TRAIN_STEP_KINDS = [
     ("b_dh", 17, False, "gemm_tc_kernel<EPI_BIAS_RESID> (dh = dz E)"),
     ("b_de", 18, False, "gemm_tc_kernel<EPI_BIAS_RESID> (head share of the table gradient, dz^T h)"),
     ("b_mp_w", 19, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP down-projection weight gradient)"),
-    ("b_dg", 20, True, "gemm_tc_kernel<EPI_BIAS_OUT> (dg = dx W_mp)"),
+    ("b_dg", 20, True, "gemm_tc_kernel<EPI_GELU_GRAD> (du = (dx W_mp) gelu'(u))"),
     ("b_fc_w", 21, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP up-projection weight gradient)"),
     ("b_da2", 22, True, "gemm_tc_kernel<EPI_F32> (du W_fc)"),
     ("b_proj_w", 23, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (attention output projection weight gradient)"),

@@ -11,7 +11,7 @@
 //         dh = dz E; dE += dz^T h ("第 25 章" §25.4: the tied table's two uses add)
 //   ln_f: dx = LN'(x_L) dh
 //   per block, last to first, from its kept activations:
-//         dW_mp += dx^T g, db_mp, dg = dx W_mp, du = dg gelu'(u), dW_fc += du^T a2,
+//         dW_mp += dx^T g, db_mp, du = (dx W_mp) gelu'(u) (one GEMM), dW_fc += du^T a2,
 //         db_fc, da2 = du W_fc, LN2', dW_proj += ds1^T y, db_proj, dy = ds1 W_proj,
 //         attention' -> dqkv, dW_attn += dqkv^T a1, db_attn, da1 = dqkv W_attn, LN1'
 //   embedding: dE[id] += dx_0, dP[t] += dx_0.
@@ -436,8 +436,18 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
   // MLP: s2 = n + g W_mp^T + b_mp, g = gelu(u), u = a2 W_fc^T + b_fc
   BW(cu(launch_cast_transpose(t->dx, M, C, t->dxb, nullptr, 0, s, g.mp_b), "cast dx, db_mp"));
   BWS(GPT_STEP_B_MP_W, l, grad_gemm(m, t->K_dxb, q.K_g, g.tg_mp_w, g.mp_w, C, F, M, s));
-  BWS(GPT_STEP_B_DG, l, gemm_bf16(m, t->A_dxb, g.tb_mp_wT, t->C_du, M, F, C, nullptr, t->du, EPI_BIAS_OUT, s));
-  BW(cu(launch_gelu_bwd(q.u, t->du, t->du, static_cast<size_t>(M) * F, c.gelu, m->num_sms, s), "gelu'"));
+  {                                   // du = (dx W_mp) * gelu'(u), the GELU's derivative in the epilogue
+    GemmArgs a{};
+    a.M = M; a.N = F; a.K = C;
+    a.out = t->du;
+    a.ldo = F;
+    a.gelu_erf = c.gelu;
+    a.aux = q.u;
+    a.err = m->err;
+    a.m_fastest = (F > M) ? 1 : 0;
+    a.b_const = 1;
+    BWS(GPT_STEP_B_DG, l, cu(launch_gemm_tc(t->A_dxb, g.tb_mp_wT, t->C_du, a, EPI_GELU_GRAD, m->num_sms, s), "dg"));
+  }
   BW(cu(launch_colsum(t->du, 1, M, F, F, g.fc_b, m->num_sms, s), "db_fc"));
   BWS(GPT_STEP_B_FC_W, l, grad_gemm(m, t->K_du, q.K_a2, g.tg_fc_w, g.fc_w, F, C, M, s));
   if (pre) {

@@ -405,14 +405,15 @@ cudaError_t launch_adamw(const OptSeg* segs, int nseg, const float* grad, float*
                          float b1, float b2, float eps, float wd, float bc1, float bc2, cudaStream_t s) {
   if (nseg <= 0) return cudaSuccess;
   if (nseg > 65535) return cudaErrorInvalidValue;
-  return launch_k(adamw_kernel, dim3(64, nseg), dim3(256), 0, s, segs, grad, master, m1, m2, lr, b1, b2, eps, wd, bc1,
+  // 512 blocks per segment: the largest tensors (the token table) keep every SM streaming to the end
+  return launch_k(adamw_kernel, dim3(512, nseg), dim3(256), 0, s, segs, grad, master, m1, m2, lr, b1, b2, eps, wd, bc1,
                   bc2);
 }
 
 cudaError_t launch_master_init(const OptSeg* segs, int nseg, float* master, cudaStream_t s) {
   if (nseg <= 0) return cudaSuccess;
   if (nseg > 65535) return cudaErrorInvalidValue;
-  return launch_k(master_init_kernel, dim3(64, nseg), dim3(256), 0, s, segs, master);
+  return launch_k(master_init_kernel, dim3(512, nseg), dim3(256), 0, s, segs, master);
 }
 
 cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, void* dst, int ldd, cudaStream_t s,

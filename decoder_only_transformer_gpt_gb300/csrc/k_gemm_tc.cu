@@ -42,7 +42,7 @@ template <int EPI>
 struct Layout {
   static constexpr bool kTmaOut =
       (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_CE_GRAD ||
-       EPI == EPI_F32_OUT);
+       EPI == EPI_F32_OUT || EPI == EPI_GELU_GRAD);
   static constexpr int STAGES = 4;
   static constexpr int STAGING = STAGES * STAGE_BYTES;
   static constexpr int BIAS = STAGING + (kTmaOut ? EPI_WARPS * EPI_NBUF * EPI_BUF : 0);   // each warp's copy of the tile's bias
@@ -309,6 +309,48 @@ __device__ __forceinline__ void ce_grad_chunk(const uint32_t* r, float lse, int 
     if (2 * i == tcol) p0 -= 1.0f;
     if (2 * i + 1 == tcol) p1 -= 1.0f;
     w[i] = pack_bf16x2(p0 * scale, p1 * scale);
+  }
+}
+
+// 64 consecutive columns of one row times GELU's derivative at u (the row's 64 bf16 inputs at
+// urow, or fewer when the chunk passes N), packed as bf16 pairs. tanh form:
+// gelu' = 0.5 (1 + t) + 0.5 x (1 - t^2) c (1 + 3 * 0.044715 x^2), t = tanh(c (x + 0.044715 x^3));
+// erf form: Phi(x) + x phi(x).
+__device__ __forceinline__ void gelu_grad_chunk(const uint32_t* r, const __nv_bfloat16* urow, int nvalid, int erf_form,
+                                                uint32_t (&w)[32]) {
+  uint32_t uw[32];
+  if (nvalid >= 64) {
+    const uint4* u4 = reinterpret_cast<const uint4*>(urow);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 v = __ldg(u4 + q);
+      uw[4 * q] = v.x; uw[4 * q + 1] = v.y; uw[4 * q + 2] = v.z; uw[4 * q + 3] = v.w;
+    }
+  } else {
+    const uint16_t* u16 = reinterpret_cast<const uint16_t*>(urow);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t lo = (2 * i < nvalid) ? u16[2 * i] : 0u, hi = (2 * i + 1 < nvalid) ? u16[2 * i + 1] : 0u;
+      uw[i] = lo | (hi << 16);
+    }
+  }
+  constexpr float c0 = 0.7978845608028654f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float2 x = unpack_bf16x2(uw[i]);
+    float d[2];
+    const float xs[2] = {x.x, x.y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float xv = xs[e];
+      if (erf_form) {
+        d[e] = 0.5f * (1.0f + erff(xv * 0.70710678118654752f)) + xv * 0.39894228040143268f * __expf(-0.5f * xv * xv);
+      } else {
+        const float t = tanh_approx(c0 * xv * fmaf(0.044715f, xv * xv, 1.0f));
+        d[e] = 0.5f * (1.0f + t) + 0.5f * xv * (1.0f - t * t) * c0 * fmaf(3.0f * 0.044715f, xv * xv, 1.0f);
+      }
+    }
+    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * d[0], __uint_as_float(r[2 * i + 1]) * d[1]);
   }
 }
 
@@ -673,6 +715,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t w[32];
             if (EPI == EPI_CE_GRAD)
               ce_grad_chunk(r + h * CW, row_lse, row_tgt - n0, args.scale, w);
+            else if (EPI == EPI_GELU_GRAD)
+              gelu_grad_chunk(r + h * CW,
+                              static_cast<const __nv_bfloat16*>(args.aux) + static_cast<size_t>(row_ok ? grow : 0) * args.N + n0,
+                              row_ok ? args.N - n0 : 0, args.gelu_erf, w);
             else
               finish_chunk<EPI, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
             uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
@@ -805,6 +851,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, tmC, a, grid_limit, s);
     case EPI_CE_GRAD: return launch_one<EPI_CE_GRAD>(tmA, tmB, tmC, a, grid_limit, s);
     case EPI_F32_OUT: return launch_one<EPI_F32_OUT>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_GELU_GRAD: return launch_one<EPI_GELU_GRAD>(tmA, tmB, tmC, a, grid_limit, s);
     default: return cudaErrorInvalidValue;
   }
 }

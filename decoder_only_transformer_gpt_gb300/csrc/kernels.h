@@ -24,6 +24,7 @@ enum Epilogue : int {
   EPI_CE = 4,             // per-row partial logsumexp of the tile, target capture
   EPI_CE_GRAD = 5,        // out bf16 = (exp(z - lse) - [col == target]) * scale, lse = nll + ztgt per row
   EPI_F32_OUT = 6,        // out fp32 = acc (+ bias) through the TMA store (fp32 [M,N] box 32x32)
+  EPI_GELU_GRAD = 7,      // out bf16 = acc * gelu'(u), u = aux bf16 [M, N] (the GELU's input)
 };
 
 struct GemmArgs {
@@ -53,6 +54,7 @@ struct GemmArgs {
                             //   (tensor maps with 64 x 64 boxes): out[M, N] += A^T W summed over K
   int b_const;              // 1: W was not written by the previous kernel on the stream (weights), so its
                             //    first stages may be requested before waiting for that kernel
+  const void* aux;          // EPI_GELU_GRAD: u, bf16 [M, N] row-major
   const float* row_nll;     // EPI_CE_GRAD: [M] per-row loss; with ztgt gives the row's logsumexp
   float scale;              // EPI_CE_GRAD: factor of the gradient (1 / rows of the mean)
 };
