@@ -62,14 +62,14 @@ NCU_TRAFFIC = {
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
                   "digest": "42a0a54118b079c59411ffb054c71c4fbf5d5995"},
-    "head": {"bytes": 102.552576e6 + 17.459456e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+    "head": {"bytes": 102.547712e6 + 17.527808e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "ef819a3571bd397b5ca4909bae45f9836d4a6c48"},
-    "mlp_proj": {"bytes": 163.005440e6 + 25.308672e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+             "digest": "3ea2df4ebcc834918fd6bc43a1d46834aa28449e"},
+    "mlp_proj": {"bytes": 162.990592e6 + 25.069824e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                 "digest": "ef819a3571bd397b5ca4909bae45f9836d4a6c48"},
+                 "digest": "3ea2df4ebcc834918fd6bc43a1d46834aa28449e"},
 }
 
 # The same for the training step's dominant step at B = 16, T = 1024: the attention derivative's

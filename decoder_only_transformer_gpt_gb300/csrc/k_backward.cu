@@ -1,5 +1,6 @@
 // Kernels of the backward pass (bf16 path): layout changes, column sums, and the
-// derivatives of LayerNorm, GELU, the embedding lookup and causal attention.
+// derivatives of LayerNorm and the embedding lookup, and the optimiser step (the GELU and
+// causal-attention derivatives live in k_gemm_tc.cu and k_attn_bwd.cu).
 //
 // The training step of "预训练一个 Mini GPT" (训练循环) back-propagates the mean
 // next-token cross-entropy to every parameter; the projections' derivatives are
@@ -134,43 +135,6 @@ __global__ void __launch_bounds__(256) layernorm_bwd_kernel(const float* __restr
   for (int i = threadIdx.x; i < C; i += blockDim.x) {
     atomicAdd(dg + i, sg[i]);
     atomicAdd(db + i, sb[i]);
-  }
-}
-
-// du = dg * gelu'(u), elementwise over bf16 (du may alias dg). tanh form ("GPT-1 学习笔记" §3.6):
-// gelu = 0.5 u (1 + tanh s), s = c (u + 0.044715 u^3), c = sqrt(2/pi), so
-// gelu' = 0.5 (1 + tanh s) + 0.5 u (1 - tanh^2 s) c (1 + 3 * 0.044715 u^2);
-// erf form gelu = u Phi(u): gelu' = Phi(u) + u phi(u).
-__global__ void __launch_bounds__(256) gelu_bwd_kernel(const uint4* __restrict__ u, const uint4* dg, uint4* du,
-                                                       size_t n8, int erf_form) {
-  pdl_wait();
-  pdl_trigger();
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 uu = u[i], gg = dg[i];
-    const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-    const uint32_t gw[4] = {gg.x, gg.y, gg.z, gg.w};
-    uint32_t ow[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 uv = unpack_bf16x2(uw[q]);
-      const float2 gv = unpack_bf16x2(gw[q]);
-      float d[2];
-      const float xs[2] = {uv.x, uv.y};
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float xv = xs[e];
-        if (erf_form) {
-          d[e] = 0.5f * (1.0f + erff(xv * 0.70710678118654752f)) + xv * 0.39894228040143268f * expf(-0.5f * xv * xv);
-        } else {
-          constexpr float c0 = 0.7978845608028654f;
-          const float t = tanhf(c0 * (xv + 0.044715f * xv * xv * xv));
-          d[e] = 0.5f * (1.0f + t) + 0.5f * xv * (1.0f - t * t) * c0 * (1.0f + 3.0f * 0.044715f * xv * xv);
-        }
-      }
-      ow[q] = pack_bf16x2(gv.x * d[0], gv.y * d[1]);
-    }
-    du[i] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
   }
 }
 
@@ -475,17 +439,6 @@ cudaError_t launch_layernorm_bwd(const float* x, const float* g, const float* dy
   const size_t smem = 2 * static_cast<size_t>(C) * sizeof(float);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
   return launch_k(layernorm_bwd_kernel, dim3(grid), dim3(wpb * 32), smem, s, x, g, dy, dx_io, add, dg, db, M, C, eps);
-}
-
-cudaError_t launch_gelu_bwd(const void* u, const void* dg, void* du, size_t n, int erf_form, int num_sms,
-                            cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
-  if (n % 8) return cudaErrorInvalidValue;
-  const size_t n8 = n / 8;
-  size_t grid = (n8 + 255) / 256;
-  if (grid > static_cast<size_t>(8 * num_sms)) grid = 8 * num_sms;
-  return launch_k(gelu_bwd_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, static_cast<const uint4*>(u),
-                  static_cast<const uint4*>(dg), static_cast<uint4*>(du), n8, erf_form);
 }
 
 cudaError_t launch_embed_bwd(const float* dx0, const int32_t* ids, float* dE, float* dP, int M, int T, int C, int V,

@@ -119,9 +119,6 @@ cudaError_t launch_colsum(const void* src, int bf16, int rows, int cols, int lds
 // dy may be dx_io itself when add == 0.
 cudaError_t launch_layernorm_bwd(const float* x, const float* g, const float* dy, float* dx_io, int add, float* dg,
                                  float* db, int M, int C, float eps, int num_sms, cudaStream_t s);
-// du = dg * gelu'(u) over n bf16 values (n % 8 == 0; du may alias dg).
-cudaError_t launch_gelu_bwd(const void* u, const void* dg, void* du, size_t n, int erf_form, int num_sms,
-                            cudaStream_t s);
 // dE[id[m]] += dx0[m], dP[m % T] += dx0[m].
 cudaError_t launch_embed_bwd(const float* dx0, const int32_t* ids, float* dE, float* dP, int M, int T, int C, int V,
                              cudaStream_t s);
