@@ -22,7 +22,7 @@ import numpy as np
 
 from workloads.configs import GPTConfig, PRE_NORM, GELU_TANH
 from .gpt_oracle import (embed, layernorm, gelu, linear, attention_probs, causal_self_attention,
-                         lm_head, cross_entropy)
+                         lm_head, head_matrix, cross_entropy)
 
 
 # ---------------------------------------------------------------- one step each
@@ -133,8 +133,8 @@ def backward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets: np.ndarray, part
     """(loss, grads) of the mean next-token cross-entropy.
 
     grads has the keys of the weight dict: "wte", "wpe", "lnf_g", "lnf_b" (when
-    the model has a final LayerNorm) and "layers", one dict per block with the
-    parameters' names. With parts=True it also holds "wte_embed" and "wte_head",
+    the model has a final LayerNorm), "head" (an untied head) and "layers", one
+    dict per block with the parameters' names. With parts=True it also holds "wte_embed" and "wte_head",
     the two contributions whose sum is "wte".
     """
     ids = np.asarray(ids)
@@ -163,7 +163,8 @@ def backward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets: np.ndarray, part
         x = s2 if pre else layernorm(s2, p["ln2_g"], p["ln2_b"], eps)
         saved.append(s)
     h = layernorm(x, w["lnf_g"], w["lnf_b"], eps) if cfg.final_ln else x
-    z = lm_head(h, w["wte"])
+    Wh = head_matrix(cfg, w)
+    z = lm_head(h, Wh)
     loss = cross_entropy(z, targets)
 
     # backward
@@ -171,7 +172,7 @@ def backward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets: np.ndarray, part
     dz = cross_entropy_backward(z, targets)
     C = cfg.C
     dz2 = dz.reshape(-1, cfg.V)
-    dh = dz @ np.asarray(w["wte"], np.float64)
+    dh = dz @ np.asarray(Wh, np.float64)
     dE_head = dz2.T @ h.reshape(-1, C)
     if cfg.final_ln:
         dx, grads["lnf_g"], grads["lnf_b"] = layernorm_backward(x, w["lnf_g"], dh, eps)
@@ -206,7 +207,11 @@ def backward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets: np.ndarray, part
             dx = ds1 + da1
         grads["layers"][li] = gl
     dE_embed, grads["wpe"] = embed_backward(dx, ids, cfg.V, w["wpe"].shape[0])
-    grads["wte"] = dE_embed + dE_head
+    if getattr(cfg, "untied_head", 0):
+        grads["wte"] = dE_embed
+        grads["head"] = dE_head
+    else:
+        grads["wte"] = dE_embed + dE_head
     if parts:
         grads["wte_embed"] = dE_embed
         grads["wte_head"] = dE_head
@@ -243,8 +248,9 @@ def adamw_step(w: dict, grads: dict, state: dict, lr: float, beta1: float = 0.9,
         state[key] = (m, v)
         return p
 
-    for k in ("wte", "wpe"):
-        w[k] = upd(k, w[k], grads[k], True)
+    for k in ("wte", "wpe", "head"):
+        if k in grads:
+            w[k] = upd(k, w[k], grads[k], True)
     for k in ("lnf_g", "lnf_b"):
         if k in grads:
             w[k] = upd(k, w[k], grads[k], False)

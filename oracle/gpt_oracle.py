@@ -29,7 +29,7 @@ import numpy as np
 from workloads.configs import GPTConfig, PRE_NORM, GELU_TANH
 
 
-def param_count(cfg: GPTConfig, tied: bool = True) -> int:
+def param_count(cfg: GPTConfig, tied=None) -> int:
     """Unique trainable parameters, counted tensor by tensor.
 
     "第 25 章 从小 GPT 到 GPT-2" §25.4: per block the four attention
@@ -49,6 +49,8 @@ def param_count(cfg: GPTConfig, tied: bool = True) -> int:
     total += cfg.ctx * C                    # position table P
     if cfg.final_ln:
         total += 2 * C                      # ln_f
+    if tied is None:
+        tied = not cfg.untied_head
     if not tied:
         total += cfg.V * C
     return total
@@ -175,6 +177,12 @@ def forward_hidden(cfg: GPTConfig, w: dict, ids: np.ndarray) -> np.ndarray:
     return x
 
 
+def head_matrix(cfg: GPTConfig, w: dict) -> np.ndarray:
+    """The head's [V, C] matrix: E itself (tied, "第 25 章" §25.4) or the untied head of
+    "Day 16 从零组装 MiniGPT" (its own nn.Linear(C, V) without bias)."""
+    return w["head"] if getattr(cfg, "untied_head", 0) else w["wte"]
+
+
 def lm_head(h: np.ndarray, wte: np.ndarray) -> np.ndarray:
     """Tied head: logit j = <h, E_j>, no bias ("第 25 章" §25.4; "GPT-1 学习笔记" §4.1)."""
     return np.asarray(h, np.float64) @ np.asarray(wte, np.float64).T
@@ -202,7 +210,7 @@ def forward(cfg: GPTConfig, w: dict, ids: np.ndarray, targets=None):
     ids = np.asarray(ids)
     if cfg.C % cfg.H != 0:
         raise ValueError("C must be divisible by H")
-    logits = lm_head(forward_hidden(cfg, w, ids), w["wte"])
+    logits = lm_head(forward_hidden(cfg, w, ids), head_matrix(cfg, w))
     loss = None if targets is None else cross_entropy(logits, targets)
     return loss, logits
 

@@ -35,6 +35,7 @@ VARIANTS = {
     "post": dict(norm_mode=POST_NORM, final_ln=0),
     "erf": dict(gelu=GELU_ERF),
     "noln_f": dict(final_ln=0),
+    "untied": dict(untied_head=1),
 }
 
 
@@ -50,6 +51,8 @@ def _model(cfg, seed, B=2, T=8, wstd=0.3):
 def _tensors(cfg, w):
     """(getter name, array) for every parameter tensor of the model."""
     out = [("wte", w["wte"]), ("wpe", w["wpe"])]
+    if "head" in w:
+        out.append(("head", w["head"]))
     if cfg.final_ln:
         out += [("lnf_g", w["lnf_g"]), ("lnf_b", w["lnf_b"])]
     for i, p in enumerate(w["layers"]):
@@ -358,3 +361,18 @@ def test_adamw_first_step_moves_each_weight_by_lr():
         gr = _grad_of(g, n)
         big = np.abs(gr) > 1e-6
         assert np.allclose((before[n] - a)[big], 1e-3 * np.sign(gr[big]), rtol=1e-5), n
+
+
+def test_untied_head_with_the_table_as_head_equals_tied():
+    # an untied head whose matrix equals E computes the tied model; its two gradients add to the tied one
+    from dataclasses import replace
+    cfg = _cfg()
+    w, ids, tg, _ = _model(cfg, seed=109)
+    cu = replace(cfg, untied_head=1)
+    wu = dict(w)
+    wu["head"] = w["wte"].copy()
+    lt, gt = oracle.backward(cfg, w, ids, tg)
+    lu, gu = oracle.backward(cu, wu, ids, tg)
+    assert abs(lt - lu) < 1e-14
+    assert np.allclose(gu["wte"] + gu["head"], gt["wte"], rtol=0, atol=1e-15)
+    assert go.param_count(cu) == go.param_count(cfg) + cfg.V * cfg.C

@@ -36,6 +36,7 @@ class GPTConfig:
     gelu: int = GELU_TANH
     dtype: int = DT_BF16
     ln_eps: float = 1e-5
+    untied_head: int = 0          # 1: the head has its own [V, C] matrix instead of reusing E
 
     @property
     def D(self) -> int:

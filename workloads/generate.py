@@ -44,7 +44,7 @@ def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
 
 def make_weights(cfg: GPTConfig, rng: np.random.Generator, scale_cproj: bool = False,
                  affine: str = "init", wstd: float = 0.02) -> Dict[str, object]:
-    """Draw a full weight set. Returns {'wte','wpe','layers':[{...}],'lnf_g','lnf_b'}."""
+    """Draw a full weight set. Returns {'wte','wpe','layers':[{...}],'lnf_g','lnf_b'} (+ 'head' when untied)."""
     V, C, L, ctx = cfg.V, cfg.C, cfg.L, cfg.ctx
     w: Dict[str, object] = {}
     w["wte"] = _normal(rng, (V, C), wstd)
@@ -71,9 +71,13 @@ def make_weights(cfg: GPTConfig, rng: np.random.Generator, scale_cproj: bool = F
     else:
         w["lnf_g"] = (1.0 + _normal(rng, (C,), 0.1)).astype(np.float32)
         w["lnf_b"] = _normal(rng, (C,), 0.02)
+    if cfg.untied_head:                      # drawn last, so tied models' draws are unchanged
+        w["head"] = _normal(rng, (V, C), wstd)
     if cfg.dtype == DT_BF16:
         w["wte"] = round_to_bf16(w["wte"])
         w["wpe"] = round_to_bf16(w["wpe"])
+        if cfg.untied_head:
+            w["head"] = round_to_bf16(w["head"])
         for p in layers:
             for k in ("attn_w", "proj_w", "fc_w", "mp_w"):
                 p[k] = round_to_bf16(p[k])
