@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libgpt_gb300.so")
 GPT_OK, GPT_EINVAL, GPT_ECONFIG, GPT_ESEQ, GPT_ETOKEN, GPT_ECUDA, GPT_ENOMEM, GPT_EDEVICE, GPT_EUNSUPPORTED = range(9)
 # parameters of gpt_grad, in the library's order; the per-block ones take a layer index
 GRAD_PARAMS = ("wte", "wpe", "lnf_g", "lnf_b", "ln1_g", "ln1_b", "attn_w", "attn_b", "proj_w", "proj_b",
-               "ln2_g", "ln2_b", "fc_w", "fc_b", "mp_w", "mp_b")
+               "ln2_g", "ln2_b", "fc_w", "fc_b", "mp_w", "mp_b", "head")
 EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESID, EPI_F32 = range(4)
 
 _fp = ctypes.POINTER(ctypes.c_float)
@@ -26,7 +26,7 @@ class GptConfig(ctypes.Structure):
     _fields_ = [("V", ctypes.c_int32), ("C", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32),
                 ("ctx", ctypes.c_int32), ("ffn", ctypes.c_int32), ("norm_mode", ctypes.c_int32),
                 ("final_ln", ctypes.c_int32), ("gelu", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("ln_eps", ctypes.c_float), ("max_tokens", ctypes.c_int64)]
+                ("ln_eps", ctypes.c_float), ("max_tokens", ctypes.c_int64), ("untied_head", ctypes.c_int32)]
 
 
 class GptLayerWeights(ctypes.Structure):
@@ -36,7 +36,7 @@ class GptLayerWeights(ctypes.Structure):
 
 class GptWeights(ctypes.Structure):
     _fields_ = [("wte", _fp), ("wpe", _fp), ("layers", ctypes.POINTER(GptLayerWeights)),
-                ("lnf_g", _fp), ("lnf_b", _fp)]
+                ("lnf_g", _fp), ("lnf_b", _fp), ("head", _fp)]
 
 
 class GptError(RuntimeError):
@@ -123,7 +123,7 @@ def _stream(stream) -> Optional[int]:
 def make_config(cfg, max_tokens: int) -> GptConfig:
     return GptConfig(V=cfg.V, C=cfg.C, H=cfg.H, L=cfg.L, ctx=cfg.ctx, ffn=cfg.ffn, norm_mode=cfg.norm_mode,
                      final_ln=cfg.final_ln, gelu=cfg.gelu, dtype=cfg.dtype, ln_eps=cfg.ln_eps,
-                     max_tokens=max_tokens)
+                     max_tokens=max_tokens, untied_head=getattr(cfg, "untied_head", 0))
 
 
 def param_count(cfg) -> int:
@@ -153,7 +153,8 @@ class GPTModel:
         for i, p in enumerate(weights["layers"]):
             layers[i] = GptLayerWeights(**{name: fp(p[name]) for name, _ in GptLayerWeights._fields_})
         w = GptWeights(wte=fp(weights["wte"]), wpe=fp(weights["wpe"]), layers=layers,
-                       lnf_g=fp(weights.get("lnf_g")), lnf_b=fp(weights.get("lnf_b")))
+                       lnf_g=fp(weights.get("lnf_g")), lnf_b=fp(weights.get("lnf_b")),
+                       head=fp(weights.get("head")))
         h = ctypes.c_void_p()
         _check(self.lib.gpt_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h)), "gpt_create")
         self.handle = h
@@ -216,7 +217,7 @@ class GPTModel:
         ptr, n = ctypes.c_void_p(), ctypes.c_int64()
         _check(self.lib.gpt_grad(self.handle, param, layer, ctypes.byref(ptr), ctypes.byref(n)), "gpt_grad")
         c = self.cfg
-        shapes = {"wte": (c.V, c.C), "wpe": (c.ctx, c.C), "attn_w": (3 * c.C, c.C), "attn_b": (3 * c.C,),
+        shapes = {"wte": (c.V, c.C), "head": (c.V, c.C), "wpe": (c.ctx, c.C), "attn_w": (3 * c.C, c.C), "attn_b": (3 * c.C,),
                   "proj_w": (c.C, c.C), "fc_w": (c.ffn, c.C), "fc_b": (c.ffn,), "mp_w": (c.C, c.ffn)}
         out = torch.empty(shapes.get(name, (c.C,)), dtype=torch.float32, device="cuda")
         assert out.numel() == n.value
@@ -239,7 +240,9 @@ class GPTModel:
     def grads(self, stream=None) -> dict:
         """Every gradient, keyed like the weight dict ("layers" a list of per-block dicts)."""
         g = {k: self.grad(k, -1, stream) for k in GRAD_PARAMS[:4]}
-        g["layers"] = [{k: self.grad(k, l, stream) for k in GRAD_PARAMS[4:]} for l in range(self.cfg.L)]
+        if getattr(self.cfg, "untied_head", 0):
+            g["head"] = self.grad("head", -1, stream)
+        g["layers"] = [{k: self.grad(k, l, stream) for k in GRAD_PARAMS[4:16]} for l in range(self.cfg.L)]
         return g
 
     def status(self, stream=None):

@@ -62,6 +62,7 @@ int validate_config(const gpt_config* c) {
   if (c->dtype != 0 && c->dtype != 1) return GPT_EINVAL;
   if (c->norm_mode != 0 && c->norm_mode != 1) return GPT_EINVAL;
   if (c->gelu != 0 && c->gelu != 1) return GPT_EINVAL;
+  if (c->untied_head != 0 && c->untied_head != 1) return GPT_EINVAL;
   if (c->C % c->H != 0) return GPT_ECONFIG;
   if (c->C % 8 != 0 || c->ffn % 8 != 0) return GPT_EINVAL;
   if (c->C > 2048) return GPT_ECONFIG;
@@ -133,7 +134,8 @@ int64_t gpt_param_count(const gpt_config* c) {
   if (!c) return -1;
   const int64_t C = c->C, F = c->ffn;
   const int64_t per_block = 4 * C + (3 * C * C + 3 * C) + (C * C + C) + (F * C + F) + (C * F + C);
-  return c->L * per_block + (int64_t)c->V * C + (int64_t)c->ctx * C + (c->final_ln ? 2 * C : 0);
+  return c->L * per_block + (int64_t)c->V * C * (c->untied_head ? 2 : 1) + (int64_t)c->ctx * C +
+         (c->final_ln ? 2 * C : 0);
 }
 
 int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
@@ -143,6 +145,7 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
   if (rc != GPT_OK) return rc;
   if (!w || !w->wte || !w->wpe || (cfg->L > 0 && !w->layers)) return GPT_EINVAL;
   if (cfg->final_ln && (!w->lnf_g || !w->lnf_b)) return GPT_EINVAL;
+  if (cfg->untied_head && !w->head) return GPT_EINVAL;
 
   gpt_model* m = new (std::nothrow) gpt_model();
   if (!m) return GPT_ENOMEM;
@@ -175,10 +178,16 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
     for (int k = 8; k < 12; ++k) lo[l * 12 + k] = wc.take(C * 4);
   }
   const size_t o_lnf = wc.take(2 * C * 4);
+  const size_t o_head = cfg->untied_head ? wc.take(V * C * es) : 0;
   if (cudaMalloc(&m->wbuf, wc.off) != cudaSuccess) { free_model(m); return GPT_ENOMEM; }
   m->wte = m->wbuf + o_wte;
   m->wpe = m->wbuf + o_wpe;
   rc = copy_matrix(m->wte, w->wte, V * C, m->bf16);
+  m->head = m->wte;
+  if (rc == GPT_OK && cfg->untied_head) {
+    m->head = m->wbuf + o_head;
+    rc = copy_matrix(m->head, w->head, V * C, m->bf16);
+  }
   if (rc == GPT_OK) rc = copy_matrix(m->wpe, w->wpe, ctx * C, m->bf16);
   m->layers.resize(L);
   for (size_t l = 0; l < L && rc == GPT_OK; ++l) {
@@ -225,6 +234,13 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
   if (rc == GPT_OK && m->bf16 && !make_tmap_2d_bf16(&m->tm_wte, m->wte, V, C, gemm_tc_bn())) {
     set_detail_text("token-table tensor map");
     rc = GPT_ECUDA;
+  }
+  if (rc == GPT_OK && m->bf16) {
+    m->tm_head = m->tm_wte;
+    if (cfg->untied_head && !make_tmap_2d_bf16(&m->tm_head, m->head, V, C, gemm_tc_bn())) {
+      set_detail_text("head tensor map");
+      rc = GPT_ECUDA;
+    }
   }
   if (rc != GPT_OK) { free_model(m); return rc; }
 

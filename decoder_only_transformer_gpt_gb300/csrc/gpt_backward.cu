@@ -52,10 +52,11 @@ struct gpt_train {
   size_t grad_floats = 0;
   float* gbuf = nullptr;         // all gradients, contiguous
   float *g_wte = nullptr, *g_wpe = nullptr, *g_lnf_g = nullptr, *g_lnf_b = nullptr;
+  float* g_head = nullptr;       // the untied head's gradient (nullptr when tied)
   std::vector<gpt_layer_grad> lg;
   std::vector<gpt_layer_act> la;
-  CUtensorMap tg_wte;
-  void* wteT = nullptr;          // [C][Vp] bf16
+  CUtensorMap tg_wte, tg_head;
+  void* wteT = nullptr;          // the head's matrix (E when tied) transposed: [C][Vp] bf16
   CUtensorMap tb_wteT;
   bool wT_ready = false;
   // gradients of activations
@@ -120,7 +121,8 @@ int alloc_train(gpt_model* m) {
   t->lg.resize(L);
   t->la.resize(L);
   const size_t per_layer_grad = 3 * C * C + 3 * C + C * C + C + F * C + F + C * F + C + 4 * C;
-  t->grad_floats = V * C + ctx * C + 2 * C + L * per_layer_grad;
+  const size_t head_grad = c.untied_head ? V * C : 0;
+  t->grad_floats = V * C + ctx * C + 2 * C + head_grad + L * per_layer_grad;
   // sizes, then one allocation
   auto layout = [&](Carve& cv) {
     t->gbuf = static_cast<float*>(cv.take(t->grad_floats * 4));
@@ -173,6 +175,7 @@ int alloc_train(gpt_model* m) {
   t->g_wpe = take(ctx * C);
   t->g_lnf_g = take(C);
   t->g_lnf_b = take(C);
+  if (head_grad) t->g_head = take(head_grad);
   for (size_t l = 0; l < L; ++l) {
     gpt_layer_grad& g = t->lg[l];
     g.ln1_g = take(C); g.ln1_b = take(C);
@@ -184,7 +187,8 @@ int alloc_train(gpt_model* m) {
   }
   // fixed descriptors: gradient reduce-add targets and transposed weights
   bool ok = make_tmap_2d(&t->tg_wte, t->g_wte, 4, V, C, 32, kEpiRows) &&
-            make_tmap_2d_bf16(&t->tb_wteT, t->wteT, C, V, gemm_tc_bn(), Vp);
+            make_tmap_2d_bf16(&t->tb_wteT, t->wteT, C, V, gemm_tc_bn(), Vp) &&
+            (!t->g_head || make_tmap_2d(&t->tg_head, t->g_head, 4, V, C, 32, kEpiRows));
   for (size_t l = 0; l < L && ok; ++l) {
     gpt_layer_grad& g = t->lg[l];
     ok = make_tmap_2d(&g.tg_attn_w, g.attn_w, 4, 3 * C, C, 32, kEpiRows) &&
@@ -302,7 +306,7 @@ int prepare_weights(gpt_model* m, gpt_train* t, cudaStream_t s) {
   if (t->wT_ready) return GPT_OK;
   const gpt_config& c = m->cfg;
   const int C = c.C, F = c.ffn, V = c.V;
-  BW(cu(launch_transpose_bf16(m->wte, V, C, C, t->wteT, t->Vp, s), "transpose wte"));
+  BW(cu(launch_transpose_bf16(m->head, V, C, C, t->wteT, t->Vp, s), "transpose head"));
   for (int l = 0; l < c.L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
     gpt_layer_grad& g = t->lg[l];
@@ -331,9 +335,12 @@ int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStre
   a.err = m->err;
   a.m_fastest = 1;
   a.b_const = 1;                          // the token table
-  BWS(GPT_STEP_B_DZ, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, t->C_dz, a, EPI_CE_GRAD, m->num_sms, s), "head grad"));
-  // dE += dz^T h (the head's share of the tied table)
-  BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->K_dz, t->K_h, t->tg_wte, t->g_wte, V, C, M, s));
+  BWS(GPT_STEP_B_DZ, -1, cu(launch_gemm_tc(m->tm_a, m->tm_head, t->C_dz, a, EPI_CE_GRAD, m->num_sms, s), "head grad"));
+  // dE += dz^T h (the head's share of the tied table), or the untied head's gradient
+  if (t->g_head)
+    BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->K_dz, t->K_h, t->tg_head, t->g_head, V, C, M, s));
+  else
+    BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->K_dz, t->K_h, t->tg_wte, t->g_wte, V, C, M, s));
   // dh = dz E (fp32 into da)
   GPT_CUDA(cudaMemsetAsync(t->da, 0, static_cast<size_t>(M) * C * sizeof(float), s));
   BWS(GPT_STEP_B_DH, -1, gemm_bf16(m, t->A_dz, t->tb_wteT, t->C_da, M, C, V, nullptr, t->da, EPI_BIAS_RESID, s));
@@ -409,7 +416,7 @@ int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t*
   a.err = m->err;
   a.m_fastest = 1;
   a.b_const = 1;
-  BW(cu(launch_gemm_tc(m->tm_a, m->tm_wte, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
+  BW(cu(launch_gemm_tc(m->tm_a, m->tm_head, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
   BW(cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, m->block_sums, M, gemm_tc_num_ntiles(c.V), c.V,
                           m->err, s),
         "ce_combine"));
@@ -527,12 +534,15 @@ int gpt_grad(const gpt_model* m, int param, int layer, float** d_grad, int64_t* 
   const gpt_train* t = m->tr;
   float* p = nullptr;
   int64_t n = 0;
-  if (param <= GPT_P_LNF_B) {
+  if (param <= GPT_P_LNF_B || param == GPT_P_HEAD) {
     switch (param) {
       case GPT_P_WTE: p = t->g_wte; n = static_cast<int64_t>(c.V) * C; break;
       case GPT_P_WPE: p = t->g_wpe; n = static_cast<int64_t>(c.ctx) * C; break;
       case GPT_P_LNF_G: p = t->g_lnf_g; n = C; break;
       case GPT_P_LNF_B: p = t->g_lnf_b; n = C; break;
+      case GPT_P_HEAD:
+        if (!t->g_head) return GPT_EINVAL;
+        p = t->g_head; n = static_cast<int64_t>(c.V) * C; break;
       default: return GPT_EINVAL;
     }
   } else {
@@ -593,6 +603,7 @@ int alloc_optimizer(gpt_model* m, gpt_train* t) {
   add(t->g_wpe, static_cast<long long>(c.ctx) * C, m->wpe, true);
   add(t->g_lnf_g, C, m->lnf_g, false);
   add(t->g_lnf_b, C, m->lnf_b, false);
+  if (t->g_head) add(t->g_head, static_cast<long long>(c.V) * C, m->head, true);
   for (int l = 0; l < c.L; ++l) {
     const gpt_layer_grad& g = t->lg[l];
     const gpt_layer_dev& w = m->layers[l];

@@ -163,7 +163,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     a.err = m->err;
     a.m_fastest = 1;
     a.b_const = 1;
-    GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_wte, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
+    GPT_STEP(GPT_STEP_HEAD, -1, cu(launch_gemm_tc(m->tm_a, m->tm_head, m->tm_a, a, EPI_CE, m->num_sms, s), "head"));
     GPT_STEP(GPT_STEP_CE, -1,
              cu(launch_ce_combine(m->pmax, m->psum, m->ztgt, tg, m->nll, m->block_sums, M, gemm_tc_num_ntiles(c.V),
                                   c.V, m->err, s),
@@ -171,7 +171,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     if (d_loss)
       GPT_STEP(GPT_STEP_MEAN, -1, cu(launch_mean(m->block_sums, ce_combine_blocks(M), M, d_loss, s), "mean"));
   } else if (d_logits) {
-    GPT_STEP(GPT_STEP_HEAD, -1, tc_gemm(m, m->tm_a, m->tm_wte, m->tm_a, M, c.V, C, nullptr, d_logits, EPI_F32, s));
+    GPT_STEP(GPT_STEP_HEAD, -1, tc_gemm(m, m->tm_a, m->tm_head, m->tm_a, M, c.V, C, nullptr, d_logits, EPI_F32, s));
   }
   return GPT_OK;
 }
@@ -225,12 +225,12 @@ int forward_f32(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int 
       GPT_STEP(GPT_STEP_LN_OUT, l, cu(launch_layernorm(m->x, w.ln2_g, w.ln2_b, a, 0, m->x, M, C, c.ln_eps, s), "ln"));
     }
   }
-  if (!pre && L == 0 && c.final_ln)
+  if (!pre && c.final_ln)                   // post-norm with a final LayerNorm: after the last block's ln_2
     GPT_STEP(GPT_STEP_LN_OUT, -1, cu(launch_layernorm(m->x, m->lnf_g, m->lnf_b, a, 0, nullptr, M, C, c.ln_eps, s), "ln"));
   if (!tg && !d_logits) return GPT_OK;
   float* z = d_logits ? d_logits : m->logits_ws;
   GPT_STEP(GPT_STEP_HEAD, -1,
-           cu(launch_gemm_simt(a, reinterpret_cast<const float*>(m->wte), nullptr, z, M, c.V, C, c.V, EPI_F32, 0, s),
+           cu(launch_gemm_simt(a, reinterpret_cast<const float*>(m->head), nullptr, z, M, c.V, C, c.V, EPI_F32, 0, s),
               "head"));
   if (tg) {
     GPT_STEP(GPT_STEP_CE, -1, cu(launch_ce_rows(z, tg, m->nll, M, c.V, m->err, s), "ce_rows"));
@@ -297,9 +297,9 @@ int decode_bf16(gpt_model* m, const int32_t* ids, int B, const int* pos_dev, flo
     GPT_DEC(launch_gemv(m->g, F, w.mp_w, w.mp_b, m->x, C, B, C, F, EPI_BIAS_RESID, c.gelu, s), "mlp_proj");
     GPT_DEC(launch_layernorm(m->x, out.g, out.b, m->a, 1, pre ? nullptr : m->x, B, C, c.ln_eps, s), "ln");
   }
-  if (!pre && L == 0 && c.final_ln)
+  if (!pre && c.final_ln)                   // post-norm with a final LayerNorm: after the last block's ln_2
     GPT_DEC(launch_layernorm(m->x, m->lnf_g, m->lnf_b, m->a, 1, nullptr, B, C, c.ln_eps, s), "ln");
-  GPT_DEC(launch_gemv(m->a, C, m->wte, nullptr, d_logits, c.V, B, c.V, C, EPI_F32, c.gelu, s), "head");
+  GPT_DEC(launch_gemv(m->a, C, m->head, nullptr, d_logits, c.V, B, c.V, C, EPI_F32, c.gelu, s), "head");
 #undef GPT_DEC
   return GPT_OK;
 }
@@ -465,7 +465,7 @@ int gpt_prefill(gpt_model* m, const int32_t* d_ids, int32_t B, int32_t T, float*
   if (rc != GPT_OK || !d_logits) return rc;
   // the head on each sequence's last row only (rows T-1, 2T-1, ... of the final activations)
   const gpt_config& c = m->cfg;
-  rc = cu(launch_gemv(static_cast<const uint8_t*>(m->a) + static_cast<size_t>(T - 1) * c.C * 2, T * c.C, m->wte,
+  rc = cu(launch_gemv(static_cast<const uint8_t*>(m->a) + static_cast<size_t>(T - 1) * c.C * 2, T * c.C, m->head,
                       nullptr, d_logits, c.V, B, c.V, c.C, EPI_F32, c.gelu, s),
           "head");
   if (rc == GPT_OK) ++m->launches;

@@ -27,6 +27,8 @@ struct gpt_model {
   float* lnf_g = nullptr;
   float* lnf_b = nullptr;
   CUtensorMap tm_wte;
+  void* head = nullptr;     // the head's [V, C] matrix: wte when tied, its own storage when untied
+  CUtensorMap tm_head;
   // workspace
   uint8_t* ws = nullptr;
   float* x = nullptr;       // residual stream fp32 [Mx, C]

@@ -60,6 +60,8 @@ typedef struct gpt_config {
   int32_t dtype;       /* 0 fp32 SIMT parity mode, 1 bf16 tensor-core path (fp32 accumulation) */
   float ln_eps;        /* LayerNorm eps inside the square root, 1e-5 */
   int64_t max_tokens;  /* workspace bound: the largest B*T a forward call may use */
+  int32_t untied_head; /* 0: the head is E itself (tied, "第 25 章" §25.4); 1: its own [V, C] matrix
+                          (the MiniGPT page's nn.Linear(C, V) without bias) */
 } gpt_config;
 
 /* One block's parameters, all fp32, HOST memory, nn.Linear orientation. */
@@ -73,11 +75,12 @@ typedef struct gpt_layer_weights {
 } gpt_layer_weights;
 
 typedef struct gpt_weights {
-  const float* wte;                  /* token table E [V, C]; also the tied head */
+  const float* wte;                  /* token table E [V, C]; also the head when tied */
   const float* wpe;                  /* position table P [ctx, C] */
   const gpt_layer_weights* layers;   /* L entries */
   const float* lnf_g;                /* [C]; may be NULL when final_ln == 0 */
   const float* lnf_b;
+  const float* head;                 /* [V, C] head matrix when untied_head == 1, else ignored */
 } gpt_weights;
 
 typedef struct gpt_model gpt_model;
@@ -250,7 +253,8 @@ enum {
   GPT_P_WTE = 0, GPT_P_WPE = 1, GPT_P_LNF_G = 2, GPT_P_LNF_B = 3,
   GPT_P_LN1_G = 4, GPT_P_LN1_B = 5, GPT_P_ATTN_W = 6, GPT_P_ATTN_B = 7,
   GPT_P_PROJ_W = 8, GPT_P_PROJ_B = 9, GPT_P_LN2_G = 10, GPT_P_LN2_B = 11,
-  GPT_P_FC_W = 12, GPT_P_FC_B = 13, GPT_P_MP_W = 14, GPT_P_MP_B = 15
+  GPT_P_FC_W = 12, GPT_P_FC_B = 13, GPT_P_MP_W = 14, GPT_P_MP_B = 15,
+  GPT_P_HEAD = 16                    /* the untied head's matrix (GPT_EINVAL on tied models) */
 };
 
 /*

@@ -43,6 +43,8 @@ def _gpu_grads(cfg, w, ids, tg):
 def _pairs(cfg, got, ref):
     yield "wte", got["wte"], ref["wte"]
     yield "wpe", got["wpe"], ref["wpe"]
+    if "head" in ref:
+        yield "head", got["head"], ref["head"]
     for k in ("lnf_g", "lnf_b"):
         yield k, got[k], ref.get(k, np.zeros(cfg.C))
     for i, (pg, pr) in enumerate(zip(got["layers"], ref["layers"])):
@@ -69,10 +71,10 @@ def _compare(cfg, w, ids, tg, rel=REL):
     return worst
 
 
-@pytest.mark.parametrize("variant", ["pre", "post", "post_lnf", "erf", "noln_f"])
+@pytest.mark.parametrize("variant", ["pre", "post", "post_lnf", "erf", "noln_f", "untied"])
 def test_backward_small_variants(gpt_lib, variant):
     kw = {"pre": {}, "post": dict(norm_mode=POST_NORM, final_ln=0), "post_lnf": dict(norm_mode=POST_NORM),
-          "erf": dict(gelu=GELU_ERF), "noln_f": dict(final_ln=0)}[variant]
+          "erf": dict(gelu=GELU_ERF), "noln_f": dict(final_ln=0), "untied": dict(untied_head=1)}[variant]
     cfg = GPTConfig(V=300, C=128, H=2, L=2, ctx=80, ffn=512, **kw)
     rng = np.random.Generator(np.random.PCG64(51))
     w = make_weights(cfg, rng, affine="random", wstd=0.05)

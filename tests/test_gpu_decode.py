@@ -43,10 +43,10 @@ def _decode_case(cfg, w, ids, T0, steps):
         assert err <= TZ, (k, t, err)
 
 
-@pytest.mark.parametrize("variant", ["pre", "post", "erf", "noln_f"])
+@pytest.mark.parametrize("variant", ["pre", "post", "erf", "noln_f", "untied", "post_lnf"])
 def test_decode_small_variants(gpt_lib, variant):
     kw = {"pre": {}, "post": dict(norm_mode=POST_NORM, final_ln=0), "erf": dict(gelu=GELU_ERF),
-          "noln_f": dict(final_ln=0)}[variant]
+          "noln_f": dict(final_ln=0), "untied": dict(untied_head=1), "post_lnf": dict(norm_mode=POST_NORM)}[variant]
     cfg = GPTConfig(V=300, C=128, H=2, L=2, ctx=80, ffn=512, **kw)
     rng = np.random.Generator(np.random.PCG64(31))
     w = make_weights(cfg, rng, affine="random", wstd=0.02)

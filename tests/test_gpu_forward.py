@@ -58,10 +58,11 @@ def test_toy_fp32_random_affine_and_stress(gpt_lib, affine):
     _check(wl.cfg, w, ids, tg)
 
 
-@pytest.mark.parametrize("variant", ["post", "erf", "noln_f"])
+@pytest.mark.parametrize("variant", ["post", "erf", "noln_f", "untied", "post_lnf"])
 def test_fp32_variants(gpt_lib, variant):
     kw = {"post": dict(norm_mode=POST_NORM, final_ln=0), "erf": dict(gelu=GELU_ERF),
-          "noln_f": dict(final_ln=0)}[variant]
+          "noln_f": dict(final_ln=0), "untied": dict(untied_head=1),
+          "post_lnf": dict(norm_mode=POST_NORM)}[variant]
     cfg = GPTConfig(V=29, C=24, H=3, L=3, ctx=10, ffn=96, dtype=DT_FP32, **kw)
     rng = np.random.Generator(np.random.PCG64(5))
     w = make_weights(cfg, rng, affine="random", wstd=0.25)
@@ -69,11 +70,12 @@ def test_fp32_variants(gpt_lib, variant):
     _check(cfg, w, ids, tg)
 
 
-@pytest.mark.parametrize("variant", ["post", "erf", "noln_f", "pre"])
+@pytest.mark.parametrize("variant", ["post", "erf", "noln_f", "pre", "untied", "post_lnf"])
 def test_bf16_variants(gpt_lib, variant):
-    """The tensor-core path for each norm / GELU / final-LayerNorm variant."""
+    """The tensor-core path for each norm / GELU / final-LayerNorm / head variant."""
     kw = {"post": dict(norm_mode=POST_NORM, final_ln=0), "erf": dict(gelu=GELU_ERF),
-          "noln_f": dict(final_ln=0), "pre": {}}[variant]
+          "noln_f": dict(final_ln=0), "pre": {}, "untied": dict(untied_head=1),
+          "post_lnf": dict(norm_mode=POST_NORM)}[variant]
     cfg = GPTConfig(V=300, C=128, H=2, L=2, ctx=80, ffn=512, dtype=DT_BF16, **kw)
     rng = np.random.Generator(np.random.PCG64(11))
     w = make_weights(cfg, rng, affine="random", wstd=0.02)     # GPT-2 initialisation scale
