@@ -2,9 +2,9 @@
 // with respect to every parameter of a bf16 model, the back-propagation step
 // of the training loop in "预训练一个 Mini GPT" (训练循环).
 //
-// Sequence (M = B*T tokens; every product is a tcgen05 GEMM of the form
-// out = A . B^T with both operands K-major, so the activations and weights a
-// product needs along another axis are transposed first):
+// Sequence (M = B*T tokens; every product is a tcgen05 GEMM out = A . B^T: the
+// input-gradient products read transposed copies of the weights, the
+// weight-gradient products read the stored activations as MN-major operands):
 //   forward + loss, keeping every block's input and activations (and c_fc's pre-activation)
 //   head: dz = (softmax(z) - onehot) / M in bf16 straight from the GEMM that
 //         recomputes z = h E^T (the row's log-sum-exp from the forward's loss);
@@ -300,8 +300,8 @@ namespace {
     }                                                                                 \
   } while (0)
 
-// The transposed weights the input-gradient products read (the weights do not change
-// after gpt_create, so once per model).
+// The transposed weights the input-gradient products read: made by the first backward and
+// again after each gpt_adamw_step (which changes the weights).
 int prepare_weights(gpt_model* m, gpt_train* t, cudaStream_t s) {
   if (t->wT_ready) return GPT_OK;
   const gpt_config& c = m->cfg;
@@ -323,7 +323,7 @@ int prepare_weights(gpt_model* m, gpt_train* t, cudaStream_t s) {
 int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStream_t s) {
   const gpt_config& c = m->cfg;
   const int C = c.C, V = c.V;
-  // dz = (softmax(h E^T) - onehot) / M, bf16 [M, V] (row stride Vp), and its transpose
+  // dz = (softmax(h E^T) - onehot) / M, bf16 [M, V] (row stride Vp)
   GemmArgs a{};
   a.M = M; a.N = V; a.K = C;
   a.out = t->dz;
@@ -497,7 +497,6 @@ int gpt_backward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, i
   int rc = shape_ok(m, B, T);
   if (rc != GPT_OK) return rc;
   const int M = B * T;
-  if (M % 8 != 0) return GPT_EINVAL;             // rows of the transposed activations: 16-byte multiples
   if (!m->tr) {
     rc = alloc_train(m);
     if (rc != GPT_OK) return rc;

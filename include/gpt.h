@@ -237,8 +237,7 @@ int gpt_sample(const float* d_logits, int32_t B, int32_t V, float temperature, i
  * gradient of that loss with respect to every parameter into model-owned fp32
  * buffers, overwriting the previous call's. The tied token table's gradient
  * is the sum of its embedding and head shares ("第 25 章 从小 GPT 到 GPT-2"
- * §25.4). B*T must be a multiple of 8 (GPT_EINVAL), T <= ctx (GPT_ESEQ),
- * B*T <= max_tokens. The first call allocates the workspace synchronously:
+ * §25.4). T <= ctx (GPT_ESEQ), B*T <= max_tokens (GPT_EINVAL). The first call allocates the workspace synchronously:
  * every block's activations at max_tokens, the gradients, transposed weights
  * and the head's dz (about 11 GB for GPT-2 small at 16384 tokens; GPT_ENOMEM
  * on failure); later

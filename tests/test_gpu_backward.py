@@ -82,6 +82,15 @@ def test_backward_small_variants(gpt_lib, variant):
     _compare(cfg, w, ids, tg)
 
 
+def test_backward_odd_token_count(gpt_lib):
+    # B * T = 39 tokens: partial row tiles, a partial last K slice of every weight-gradient product
+    cfg = GPTConfig(V=157, C=64, H=2, L=2, ctx=16, ffn=256)
+    rng = np.random.Generator(np.random.PCG64(57))
+    w = make_weights(cfg, rng, affine="random", wstd=0.05)
+    ids, tg = make_tokens(cfg.V, 3, 13, rng)
+    _compare(cfg, w, ids, tg)
+
+
 def test_backward_ragged_head_width_32(gpt_lib):
     # D = 32 heads, T = 40 (ragged against the 16-row fragments and 64-row blocks), 3 sequences
     cfg = GPTConfig(V=211, C=128, H=4, L=2, ctx=48, ffn=512)
@@ -137,10 +146,10 @@ def test_backward_errors(gpt_lib):
     with pytest.raises(binding.GptError) as e:            # no gradients before the first backward
         m.grad("wte")
     assert e.value.code == binding.GPT_EINVAL
-    bad = np.ascontiguousarray(ids[:, :3])                 # B * T = 6: not a multiple of 8
+    long_ids = np.zeros((2, cfg.ctx + 1), np.int32)        # longer than the position table
     with pytest.raises(binding.GptError) as e:
-        m.backward(dev_i32(bad), dev_i32(np.ascontiguousarray(tg[:, :3])))
-    assert e.value.code == binding.GPT_EINVAL
+        m.backward(dev_i32(long_ids), dev_i32(long_ids))
+    assert e.value.code == binding.GPT_ESEQ
     tg2 = tg.copy()
     tg2[1, 2] = cfg.V                                      # a target outside [0, V), found on the device
     with pytest.raises(binding.GptError) as e:
