@@ -376,3 +376,19 @@ def test_untied_head_with_the_table_as_head_equals_tied():
     assert abs(lt - lu) < 1e-14
     assert np.allclose(gu["wte"] + gu["head"], gt["wte"], rtol=0, atol=1e-15)
     assert go.param_count(cu) == go.param_count(cfg) + cfg.V * cfg.C
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+def test_gradient_matches_torch_autograd(variant):
+    # the whole gradient against autograd through torch.nn.functional routines (fp64, CPU)
+    pytest.importorskip("torch")
+    import torch_ref
+    cfg = _cfg(V=50, C=32, H=4, L=2, ctx=24, ffn=128, **VARIANTS[variant])
+    w, ids, tg, _ = _model(cfg, seed=110, B=2, T=24, wstd=0.2)
+    loss, grads = oracle.backward(cfg, w, ids, tg)
+    rloss, ref = torch_ref.grads(cfg, w, ids, tg)
+    assert abs(loss - rloss) < 1e-12
+    for name, a in _tensors(cfg, w):
+        r = ref[name] if not name.startswith("layers.") else ref["layers"][int(name.split(".")[1])][name.split(".")[2]]
+        g = _grad_of(grads, name)
+        assert np.max(np.abs(g - r)) <= 1e-10 * max(1.0, np.max(np.abs(r))), name

@@ -2,7 +2,8 @@
 
 Used only to pin the oracle: it shares no code with it (the oracle is numpy),
 and each step is a library routine (layer_norm, linear, gelu,
-scaled_dot_product_attention, cross_entropy) rather than a retyped formula.
+scaled_dot_product_attention, cross_entropy) rather than a retyped formula;
+its gradients come from torch's autograd.
 """
 import numpy as np
 import torch
@@ -16,6 +17,33 @@ def _t(a):
 
 
 def forward(cfg, w, ids, targets=None):
+    loss, logits = _forward(cfg, w, ids, targets, _t)
+    return (None if loss is None else float(loss)), logits.detach().numpy()
+
+
+def grads(cfg, w, ids, targets):
+    """(loss, gradients keyed like the weight dict) by torch autograd through the same functional model."""
+    leaves = {}
+
+    def leaf(a):
+        key = id(a)
+        if key not in leaves:
+            leaves[key] = (a, _t(a).clone().requires_grad_(True))
+        return leaves[key][1]
+
+    loss, _ = _forward(cfg, w, ids, targets, leaf)
+    loss.backward()
+
+    def g(a):
+        t = leaves.get(id(a))
+        return np.zeros(np.shape(a)) if t is None or t[1].grad is None else t[1].grad.numpy()
+
+    out = {k: g(w[k]) for k in ("wte", "wpe", "lnf_g", "lnf_b", "head") if k in w}
+    out["layers"] = [{k: g(v) for k, v in p.items()} for p in w["layers"]]
+    return float(loss.detach()), out
+
+
+def _forward(cfg, w, ids, targets, _t):
     E = _t(w["wte"])
     P = _t(w["wpe"])
     ids_t = torch.from_numpy(np.asarray(ids, np.int64))
@@ -51,9 +79,10 @@ def forward(cfg, w, ids, targets=None):
             x = ln(n + mlp(n, p), p["ln2_g"], p["ln2_b"])
     if cfg.final_ln:
         x = ln(x, w["lnf_g"], w["lnf_b"])
-    logits = x @ E.T
+    head = _t(w["head"]) if getattr(cfg, "untied_head", 0) else E
+    logits = x @ head.T
     loss = None
     if targets is not None:
         tg = torch.from_numpy(np.asarray(targets, np.int64)).reshape(-1)
-        loss = float(F.cross_entropy(logits.reshape(-1, logits.shape[-1]), tg))
-    return loss, logits.numpy()
+        loss = F.cross_entropy(logits.reshape(-1, logits.shape[-1]), tg)
+    return loss, logits
