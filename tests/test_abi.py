@@ -67,3 +67,13 @@ def test_product_path_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.replace("oracle-free", ""), f
+
+
+def test_gradient_parameter_ids_match_the_binding():
+    # gpt_grad's parameter ids (include/gpt.h) and the binding's names, in the same order
+    from decoder_only_transformer_gpt_gb300 import binding
+    text = open(os.path.join(ROOT, "include", "gpt.h")).read()
+    ids = {k.lower(): int(v) for k, v in re.findall(r"\bGPT_P_(\w+)\s*=\s*(\d+)", text)}
+    assert sorted(ids.values()) == list(range(len(binding.GRAD_PARAMS)))
+    for i, name in enumerate(binding.GRAD_PARAMS):
+        assert ids[name] == i, name
