@@ -515,14 +515,13 @@ int gpt_backward(gpt_model* m, const int32_t* d_ids, const int32_t* d_targets, i
   m->probe_hits = 0;
   rc = forward_maps(m, B, T);
   if (rc == GPT_OK) rc = train_forward(m, t, d_ids, d_targets, B, T, d_loss, s);
-  const int fwd_launches = 0;
   if (rc == GPT_OK) rc = head_backward(m, t, d_targets, M, s);
   for (int l = c.L - 1; l >= 0 && rc == GPT_OK; --l) rc = block_backward(m, t, l, B, T, s);
   if (rc == GPT_OK) rc = cu(launch_embed_bwd(t->dx, d_ids, t->g_wte, t->g_wpe, M, T, c.C, c.V, s), "embedding'");
   m->prof_ev0 = m->prof_ev1 = nullptr;            // a probe covers one call
   m->prof_step = m->prof_layer = -1;
   if (rc != GPT_OK) return rc;
-  m->launches = fwd_launches + t->launches + 1;
+  m->launches = t->launches + 1;                 // + the embedding derivative
   return GPT_OK;
 }
 

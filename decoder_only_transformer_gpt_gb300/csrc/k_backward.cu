@@ -17,7 +17,6 @@ namespace gptgb {
 
 namespace {
 
-constexpr int kTr = 32;                      // transpose tile edge
 
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 __device__ __forceinline__ uint16_t f2bf(float f) {
@@ -28,31 +27,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-// fp32 [rows, cols] -> bf16 copy (dst, nullable) and bf16 transpose (dstT [cols, rows], nullable).
-__global__ void __launch_bounds__(256) cast_transpose_kernel(const float* __restrict__ src, int rows, int cols,
-                                                             uint16_t* __restrict__ dst, uint16_t* __restrict__ dstT,
-                                                             int ldt) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ uint16_t t[kTr][kTr + 2];
-  const int c0 = blockIdx.x * kTr, r0 = blockIdx.y * kTr;
-  for (int i = threadIdx.y; i < kTr; i += 8) {
-    const int r = r0 + i, c = c0 + threadIdx.x;
-    uint16_t h = 0;
-    if (r < rows && c < cols) {
-      h = f2bf(src[static_cast<size_t>(r) * cols + c]);
-      if (dst) dst[static_cast<size_t>(r) * cols + c] = h;
-    }
-    t[i][threadIdx.x] = h;
-  }
-  __syncthreads();
-  if (dstT == nullptr) return;                // a plain cast (block-uniform)
-  for (int i = threadIdx.y; i < kTr; i += 8) {
-    const int c = c0 + i, r = r0 + threadIdx.x;
-    if (c < cols && r < rows) dstT[static_cast<size_t>(c) * ldt + r] = t[threadIdx.x][i];
-  }
 }
 
 // out[c] += sum over rows of src[r][c]: a block sums 32 columns over a range of rows
@@ -430,12 +404,6 @@ cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, 
 cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s,
                                   float* colsum) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  if (dstT == nullptr && colsum == nullptr) {              // a plain cast
-    const dim3 grid((cols + kTr - 1) / kTr, (rows + kTr - 1) / kTr), block(kTr, 8);
-    if (grid.y > 65535u) return cudaErrorInvalidValue;
-    return launch_k(cast_transpose_kernel, grid, block, 0, s, src, rows, cols, static_cast<uint16_t*>(dst),
-                    static_cast<uint16_t*>(nullptr), ldt);
-  }
   const dim3 grid((cols + kT64 - 1) / kT64, (rows + kT64 - 1) / kT64);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   const int vec = (cols % 8 == 0) && (dstT == nullptr || ldt % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
