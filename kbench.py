@@ -1,10 +1,10 @@
 """Time one step kernel of the library in isolation (CUDA events, warm-up, mean of N).
 
-    python -m decoder_only_transformer_gpt_gb300.kbench attention --B 16 --T 1024 --H 12 --D 64
-    python -m decoder_only_transformer_gpt_gb300.kbench gemm --M 16384 --N 768 --K 768 --epi 2
-    python -m decoder_only_transformer_gpt_gb300.kbench head --M 16384 --V 50257 --C 768
-    python -m decoder_only_transformer_gpt_gb300.kbench layernorm --M 16384 --C 768
-    python -m decoder_only_transformer_gpt_gb300.kbench train --B 16 --T 1024
+    python kbench.py attention --B 16 --T 1024 --H 12 --D 64
+    python kbench.py gemm --M 16384 --N 768 --K 768 --epi 2
+    python kbench.py head --M 16384 --V 50257 --C 768
+    python kbench.py layernorm --M 16384 --C 768
+    python kbench.py train --B 16 --T 1024
 
 (`train`: one gpt_backward call, forward + loss + every gradient, of GPT-2 small on
 seeded synthetic tokens.)
@@ -14,10 +14,14 @@ Inputs are random device tensors; the figure printed is algorithmic TFLOP/s
 """
 import argparse
 import json
+import os
+import sys
 
 import torch
 
-from . import binding
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from decoder_only_transformer_gpt_gb300 import binding  # noqa: E402
 
 
 def _time(fn, warmup, iters):
