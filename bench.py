@@ -407,7 +407,10 @@ def run_ours(args, rank, world, local_rank):
         return
     pk, pk_src = peaks()
     flops = step_flops(cfg, B, T)
-    peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    # every kernel here runs inside a step of a few ms, not a seconds-long loop under the power cap,
+    # so the burst figure is its denominator; the sustained one is reported beside it
+    peak_t = float(pk["bf16_tflops"])
+    peak_ts = float(pk.get("bf16_tflops_sustained", peak_t))
     peak_b = float(pk.get("hbm_gbs"))
 
     def rate(work, bound, ms):
@@ -417,11 +420,16 @@ def run_ours(args, rank, world, local_rank):
         a = work / (ms / 1e3) / 1e9
         return a, peak_b, "GB/s"
 
+    # The breakdown brackets each launch with events, which stops it from overlapping its neighbours
+    # (programmatic dependent launch): the bracketed times add up to more than a step. ms_per_step_scaled
+    # shares the measured step time out in proportion to them.
     total_ms = sum(v["ms_per_step"] for v in breakdown.values())
+    step_ms = ms_max / args.steps
     kernels = []
     for name, v in sorted(breakdown.items(), key=lambda kv: -kv[1]["ms_per_step"]):
         a, p, u = rate(v["work"], v["bound"], v["avg_ms"])
         kernels.append({"step": name, "launches_per_step": v["launches_per_step"], "avg_ms": v["avg_ms"],
+                        "ms_per_step_scaled": v["ms_per_step"] * step_ms / total_ms,
                         "share": v["ms_per_step"] / total_ms, "bound": v["bound"], "achieved": a, "unit": u,
                         "frac": a / p})
     dom_avg = statistics.mean(dom_ms)
@@ -455,9 +463,13 @@ def run_ours(args, rank, world, local_rank):
                      "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic,
                      "algorithmic": breakdown[dom]["work"],
-                     "peak_source": f"{pk_src} " + ("bf16 sustained" if unit == "TFLOP/s" else "HBM copy"),
+                     "peak_source": f"{pk_src} " + ("bf16 burst" if unit == "TFLOP/s" else "HBM copy"),
+                     "frac_of_sustained": (achieved / peak_ts) if unit == "TFLOP/s" else None,
                      "avg_launch_ms": dom_avg, "launches_timed": len(dom_ms)},
         "kernels": kernels,
+        "kernels_note": ("avg_ms: each launch bracketed by events outside the timed region (no overlap with "
+                         "its neighbours); sum of bracketed times per step %.3f ms against %.3f ms measured; "
+                         "ms_per_step_scaled rescales them to the step" % (total_ms, step_ms)),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -674,7 +686,8 @@ def run_train(args, rank, world, local_rank):
         model.close()
         return
     pk, pk_src = peaks()
-    peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    peak_t = float(pk["bf16_tflops"])          # a step of tens of ms: the burst figure
+    peak_ts = float(pk.get("bf16_tflops_sustained", peak_t))
     flops = 3.0 * step_flops(cfg, B, T)
     total_ms = ms / args.steps
     kernels = []
@@ -708,7 +721,8 @@ def run_train(args, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"kernel": dom_kernel, "step": dom, "bound": "tensor", "achieved": achieved, "peak": peak_t,
                      "unit": "TFLOP/s", "frac": achieved / peak_t, "traffic": traffic,
-                     "algorithmic": breakdown[dom]["work"], "peak_source": f"{pk_src} bf16 sustained",
+                     "algorithmic": breakdown[dom]["work"], "peak_source": f"{pk_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_ts,
                      "avg_launch_ms": dom_avg, "launches_timed": len(dom_ms)},
         "kernels": kernels,
         "cpu_baseline": cpu,
