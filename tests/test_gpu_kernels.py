@@ -74,6 +74,47 @@ def test_gemm_tc_stream_k(gpt_lib, M, N, K, epi):
     _gemm_case(gpt_lib, M, N, K, epi, seed=K + epi)
 
 
+@pytest.mark.parametrize("M,N,K,epi", [(16384, 768, 3072, 2), (16384, 2304, 768, 0), (16384, 3072, 768, 1),
+                                        (16384, 768, 768, 2), (32768, 768, 3072, 2), (12432, 768, 3072, 2)])
+def test_gemm_tc_full_size_sampled_rows(gpt_lib, M, N, K, epi):
+    """The projections at the token counts of the timed runs (16,384 = 16 x 1024, 32,768 and the ragged
+    12,432 = 16 x 777), whose tile schedules (the stream-K split region of mlp c_proj, several waves of
+    whole tiles) the small cases do not reach. Every output is computed on the GPU; 128-row blocks at
+    the start, inside and at the end of the split region and in the last wave are checked against the
+    oracle with the same bounds as the small cases."""
+    from decoder_only_transformer_gpt_gb300 import binding
+    rng = np.random.default_rng(M + N + K)
+    A = rand_bf16(rng, (M, K))
+    W = rand_bf16(rng, (N, K), 0.5)
+    b = rng.standard_normal(N).astype(np.float32)
+    if epi == binding.EPI_BIAS_RESID:
+        x0 = rng.standard_normal((M, N)).astype(np.float32)
+        out = dev_f32(x0)
+    else:
+        x0 = None
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    binding.gemm(dev_bf16(A), dev_bf16(W), dev_f32(b), out, epi)
+    binding.status()
+    got_all = out
+    MB = (M + 127) // 128
+    blocks = sorted({0, 1, MB // 4, MB // 2, (3 * MB) // 4, MB - 2, MB - 1})
+    for mb in blocks:
+        r0, r1 = 128 * mb, min(M, 128 * mb + 128)
+        ref_lin = oracle.linear(A[r0:r1], W, b)
+        acc_bound = K * EPS23 * (np.abs(A[r0:r1]).astype(np.float64) @ np.abs(W).astype(np.float64).T) + 1e-6
+        got = host(got_all[r0:r1])
+        if epi == binding.EPI_BIAS:
+            ref, tol = ref_lin, bf16_ulp(ref_lin) + acc_bound
+        elif epi == binding.EPI_BIAS_GELU:
+            ref = oracle.gelu(ref_lin)
+            tol = bf16_ulp(ref) + 1.2 * acc_bound + 0.5 * np.abs(ref_lin) * 6e-4
+        else:
+            ref = x0[r0:r1].astype(np.float64) + ref_lin
+            tol = acc_bound + 4 * EPS23 * np.abs(ref)
+        bad = np.abs(got - ref) > tol
+        assert not bad.any(), f"rows {r0}:{r1}: {bad.sum()} outside bound; worst {np.max(np.abs(got - ref) - tol)}"
+
+
 def test_gemm_tc_stream_k_deterministic(gpt_lib):
     from decoder_only_transformer_gpt_gb300 import binding
     rng = np.random.default_rng(5)
@@ -113,6 +154,29 @@ def _attn_case(B, T, H, D, seed=0, qk_scale=1.5, boost_keys=None):
                                      (2, 777, 2, 64), (1, 1024, 2, 64), (2, 300, 3, 32)])
 def test_attention_tc(gpt_lib, B, T, H, D):
     _attn_case(B, T, H, D, qk_scale=2.0)
+
+
+@pytest.mark.parametrize("B,T", [(16, 1024), (16, 777)])
+def test_attention_tc_full_size_sampled(gpt_lib, B, T):
+    """Attention at the timed shape (16 x 12 (sequence, head) pairs of 1024 tokens: 1,536 work items
+    dealt over the persistent CTAs, every CTA running several items) and its ragged variant; the
+    whole batch runs on the GPU and three sequences (all 12 heads) are checked against the oracle."""
+    from decoder_only_transformer_gpt_gb300 import binding
+    H, D = 12, 64
+    C = H * D
+    rng = np.random.default_rng(T)
+    qkv = rand_bf16(rng, (B, T, 3 * C))
+    qkv[..., :2 * C] *= 2.0
+    y = torch.empty((B, T, C), dtype=torch.bfloat16, device="cuda")
+    binding.attention(dev_bf16(qkv), y, H)
+    binding.status()
+    umax = np.abs(qkv[..., 2 * C:]).max()
+    for b in (0, B // 2 + 1, B - 1):
+        ref = oracle.causal_self_attention(qkv[b:b + 1].astype(np.float64), H)[0]
+        got = host(y[b])
+        tol = 2.0 ** -8 * umax + bf16_ulp(ref) + 1e-5
+        bad = np.abs(got - ref) > tol
+        assert not bad.any(), f"sequence {b}: {bad.sum()} outside bound; worst {np.max(np.abs(got - ref) - tol)}"
 
 
 @pytest.mark.parametrize("D", [64, 32])
