@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH):
         "gpt_time_step": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gpt_last_launch_count": (ctypes.c_int, [vp]),
         "gpt_last_probe_hits": (ctypes.c_int, [vp]),
+        "gpt_debug_expire_waits": (ctypes.c_int, [vp, i64]),
         "gpt_kv_reserve": (ctypes.c_int, [vp, i32]),
         "gpt_prefill": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
         "gpt_decode_step": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
@@ -247,6 +248,10 @@ class GPTModel:
 
     def status(self, stream=None):
         _check(self.lib.gpt_status(self.handle, _stream(stream)), "gpt_status")
+
+    def debug_expire_waits(self, limit_cycles: int) -> None:
+        """Arm the failure-detection check for the next forward (see gpt_debug_expire_waits)."""
+        _check(self.lib.gpt_debug_expire_waits(self.handle, limit_cycles), "gpt_debug_expire_waits")
 
     def close(self):
         if getattr(self, "handle", None):

@@ -100,6 +100,7 @@ void free_model(gpt_model* m) {
   cudaFree(m->stage_logits);
   cudaFree(m->kv);
   cudaFree(m->dec_pos);
+  cudaFree(m->dbg_flag);
   gptgb::free_train(m);
   if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);
   if (m->fwd_exec) cudaGraphExecDestroy(m->fwd_exec);

@@ -639,12 +639,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const float4* ppart = nullptr;                  // owner: the other CTA's partial rows
       if (SK && kTmaOut && owner) {
         // wait (bounded) for the writer's flag, then clear it for the next launch
-        int* flag = args.sk_flag + (blockIdx.x + 1) * 4 + sub;
+        const int fi = (blockIdx.x + 1) * 4 + sub;
+        int* flag = args.sk_wait_flag != nullptr ? const_cast<int*>(args.sk_wait_flag) + fi : args.sk_flag + fi;
+        const long long limit = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
         bool seen = ld_acquire_gpu(flag) != 0;
         if (!seen) {
           const long long t0 = clock64();
           while (!(seen = (ld_acquire_gpu(flag) != 0))) {
-            if (*abort_flag || clock64() - t0 > kWaitLimitCycles) break;
+            if (*abort_flag || clock64() - t0 > limit) break;
           }
         }
         if (!__all_sync(0xffffffffu, seen)) {

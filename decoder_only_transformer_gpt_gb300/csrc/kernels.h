@@ -46,6 +46,9 @@ struct GemmArgs {
   // CTA holding its first K blocks after adding the other's fp32 partial.
   float* sk_part;           // [grid + 1][BM x 256] fp32 partial tiles, or nullptr: whole tiles per CTA
   int* sk_flag;             // [grid + 1][4] per-warp "partial written" flags, zero between launches
+  const int* sk_wait_flag;  // nullptr, or flags the finishing CTAs wait on instead of sk_flag (set by nobody:
+                            //   the failure-detection check makes those bounded waits expire)
+  long long wait_limit;     // SM cycles a finishing CTA waits for its partner's flag (0: kWaitLimitCycles)
   // Split-K (EPI_BIAS_RESID without bias, whole-tile launches): ksplit > 1 deals (tile, K slice)
   // units, slice s covering K blocks [s KB / ksplit, (s + 1) KB / ksplit); each adds its partial
   // into the fp32 output with the reduce-add store.

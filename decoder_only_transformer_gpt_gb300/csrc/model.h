@@ -44,6 +44,11 @@ struct gpt_model {
   float* logits_ws = nullptr;   // fp32 path: [Mx, V]
   float* sk_part = nullptr;     // bf16 path: stream-K partial tiles of the block projections
   int* sk_flag = nullptr;       // and their flags (zero between launches)
+  // failure-detection check (gpt_debug_expire_waits): the next bf16 forward's finishing CTAs wait on
+  // these flags, which nothing sets, for at most dbg_wait_limit SM cycles
+  int* dbg_flag = nullptr;
+  long long dbg_wait_limit = 0;
+  bool dbg_armed = false;
   // key/value cache for incremental decoding: per layer [kv_batch][ctx][2C] bf16
   uint8_t* kv = nullptr;
   int kv_batch = 0;

@@ -176,6 +176,23 @@ int gpt_last_launch_count(const gpt_model* m);
 int gpt_last_probe_hits(const gpt_model* m);
 
 /*
+ * Failure-detection check of the bounded device waits (the pages have no
+ * counterpart: it tests the library's own error path). Arms the next bf16
+ * gpt_forward on m, which then runs with direct launches (no graph): in the
+ * long-K projections whose tiles are split between two CTAs (stream-K), each
+ * CTA that finishes a split tile waits on a partial-tile flag that nothing sets,
+ * for at most limit_cycles SM clock cycles (about limit_cycles / 2e9 seconds)
+ * instead of about 2 s. Every such wait expires: the kernel records a device
+ * error, raises its CTA's abort flag, drains its own copies and MMAs, frees its
+ * tensor memory and returns. The loss of that call is unspecified; the next
+ * gpt_status() returns GPT_EDEVICE and clears the flags the aborted launches
+ * left set, after which the handle computes correct results again. A forward
+ * with no split tiles is unaffected. The first call allocates a small flag
+ * buffer. GPT_ECONFIG for fp32 models, GPT_EINVAL for limit_cycles < 1.
+ */
+int gpt_debug_expire_waits(gpt_model* m, int64_t limit_cycles);
+
+/*
  * Incremental decoding with a key/value cache ("预训练一个 Mini GPT", the
  * sections on the KV cache and on prefill and decode: the keys and values of
  * every processed token are kept, so a new token costs one projection of its
