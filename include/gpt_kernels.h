@@ -86,8 +86,14 @@ int gptk_lmhead_ce(const void* h, const void* wte, const int32_t* targets, float
  * The first call on each device looks up that array's device address (with the
  * device current); make that first call before any stream capture. All calls
  * share the array, so calls whose GPU work overlaps race; order them on one
- * stream. d_err: caller-owned device int that receives a nonzero code if a
- * target is outside [0, V), or NULL; nll as in gptk_lmhead_ce. No logits.
+ * stream. The looked-up address is kept for the life of the process: do not
+ * use this entry after a reset of the device (cudaDeviceReset or a destroyed
+ * and recreated primary context), which invalidates it. d_err: caller-owned
+ * device int that receives a nonzero code (and keeps the first one) if a target
+ * is outside [0, V) or a bounded wait expired; the nll of a row whose target is
+ * out of range is then unspecified, the other rows are still correct. With
+ * d_err NULL such errors are not reported anywhere. nll as in gptk_lmhead_ce.
+ * No logits.
  */
 int gptk_lmhead_ce_noalloc(const void* h, const void* wte, const int32_t* targets, float* nll,
                            int32_t M, int32_t V, int32_t C, int32_t* d_err, void* stream);

@@ -65,3 +65,26 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(gpt_lib):
         binding.lmhead_ce_noalloc(h, E, tg, nll)
     assert e.value.code == binding.GPT_EINVAL
     assert "scratch" in str(e.value)
+
+
+def test_noalloc_reports_a_bad_target_and_runs_without_an_error_word(gpt_lib):
+    """A target equal to V reaches the caller's error word while every other row still matches
+    the allocating entry; with no error word (NULL) the result on valid inputs is the same."""
+    from decoder_only_transformer_gpt_gb300 import binding
+    V, C, M = 5000, 128, 300
+    h, E, tg = _inputs(77, M, V, C)
+    ref = _reference(h, E, tg)
+    bad = tg.clone()
+    bad[17] = V
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nll = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda")
+    binding.lmhead_ce_noalloc(h, E, bad, nll, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) != 0
+    keep = torch.ones(M, dtype=torch.bool, device="cuda")
+    keep[17] = False
+    assert (nll[keep] - ref[keep]).abs().max().item() <= TOL
+    nll2 = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda")
+    binding.lmhead_ce_noalloc(h, E, tg, nll2, None)
+    torch.cuda.synchronize()
+    assert (nll2 - ref).abs().max().item() <= TOL
