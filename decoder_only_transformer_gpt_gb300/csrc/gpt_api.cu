@@ -286,10 +286,11 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
   m->nll = reinterpret_cast<float*>(m->ws + o_nll);
   m->block_sums = reinterpret_cast<float*>(m->ws + o_bsum);
   m->err = reinterpret_cast<int*>(m->ws + o_err);
+  m->attn_sched = m->err + 16;
   m->stage_ids = reinterpret_cast<int32_t*>(m->ws + o_ids);
   m->stage_tg = reinterpret_cast<int32_t*>(m->ws + o_tg);
   m->stage_loss = reinterpret_cast<float*>(m->ws + o_loss);
-  if (cudaMemset(m->err, 0, sizeof(int)) != cudaSuccess) { free_model(m); return GPT_ECUDA; }
+  if (cudaMemset(m->err, 0, 256) != cudaSuccess) { free_model(m); return GPT_ECUDA; }
   if (cudaMallocHost(&m->h_pinned, 64) != cudaSuccess) { free_model(m); return GPT_ENOMEM; }
   *out = m;
   return GPT_OK;

@@ -133,7 +133,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
       rc = cu(launch_kv_store(m->qkv, kv_layer(m, l), B, T, C, c.ctx, s), "kv_store");
       if (rc != GPT_OK) return rc;
     }
-    GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_tc(m->tm_qkv, m->y, B, T, c.H, C / c.H, m->err, s), "attention"));
+    GPT_STEP(GPT_STEP_ATTN, l, cu(launch_attention_tc(m->tm_qkv, m->y, B, T, c.H, C / c.H, m->err, m->attn_sched, s), "attention"));
     // the LayerNorm after each residual add: ln_2 then the next block's ln_1 or ln_f
     // (pre-norm), ln_1 then ln_2 applied to x itself (post-norm)
     NextLN mid = pre ? NextLN{w.ln2_g, w.ln2_b} : NextLN{w.ln1_g, w.ln1_b};

@@ -107,7 +107,15 @@ int gptk_attention(const void* qkv, void* y, int32_t B, int32_t T, int32_t H, in
     set_detail_text("qkv tensor map");
     return GPT_ECUDA;
   }
-  GPT_CUDA(launch_attention_tc(tm, y, B, T, H, D, err, s));
+  int* sched = nullptr;                    // the kernel's work counter, zeroed, on the stream
+  GPT_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&sched), 2 * sizeof(int), s));
+  cudaError_t e = cudaMemsetAsync(sched, 0, 2 * sizeof(int), s);
+  if (e == cudaSuccess) e = launch_attention_tc(tm, y, B, T, H, D, err, sched, s);
+  cudaFreeAsync(sched, s);
+  if (e != cudaSuccess) {
+    set_detail("attention", e);
+    return GPT_ECUDA;
+  }
   return GPT_OK;
 }
 

@@ -11,35 +11,44 @@
 // never reach memory. Key tiles above the diagonal are never loaded; only the
 // diagonal tile is masked.
 //
-// A work item is one (b, h) and one 128-row query tile; the kernel is
-// persistent (one CTA per SM walks its items, heaviest first, snake-dealt) and
-// keeps its barriers, TMEM and K/U ring across items. Inside an item the score
-// tiles are triple-buffered so the tensor core and the softmax overlap:
-//   S(j)  = Q K_j^T   tcgen05.mma M=128 N=128 K=D  -> TMEM S[j % 3] (128 columns each)
-//   O_h  += P(j)_h U_j[64h:64h+64]                 -> TMEM O_h (h = 0, 1)
-// The softmax reads its 64 scores of S(j) into registers and writes P(j) back
-// as bf16 pairs over the first 32 columns of the same 64 (row = lane), so the
-// P U MMA takes its A operand straight from tensor memory: probabilities never
-// pass through shared memory. While the softmax turns S(j) into P(j), the
-// tensor core already holds S(j+1) and S(j+2); once P(j) is handed over it runs
-// P(j) U_j and then S(j+3) into the same buffer (one thread's MMAs execute in
-// issue order, so S(j+3) overwrites P(j) only after P(j) U_j has read it), which
-// leaves two softmax steps for that chain. The query tile is double-buffered
-// across items, so an item's first score tiles never wait for its Q load; the
-// next item's first P U waits only for the previous item's output to be read,
-// which the same softmax warps do before they produce that P. U_j is consumed
-// MN-major straight from its TMA tile. Two softmax threads share each query row
-// (= TMEM lane): one owns keys [0, 64) of every key tile, the other keys
-// [64, 128), each with its own running max, running sum and TMEM output
-// accumulator. The running max is raised lazily: a half's O and sum are
-// rescaled only when its max grows by more than 2^8. At the end of an item both
-// threads of a row exchange their (max, sum) and each writes half of the row's
-// D output columns.
-// Warp roles (320 threads, one persistent CTA per SM):
-//   warp 0      TMA producer: Q once per item (two buffers), then K_j, U_j into a five-stage ring
-//   warp 1      TMEM allocator (512 columns) and MMA issuer (the whole warp runs
-//               the loop, one elected lane issues)
-//   warps 2-5   softmax, keys [0, 64) of each tile; warps 6-9 keys [64, 128)
+// Work item: one (b, h) and a PAIR of consecutive 128-row query tiles
+// (2p, 2p + 1). Both read the same stream of 128-key K/U tiles, so each K/U
+// tile is loaded once for 256 query rows. Two softmax groups of four warps own
+// one query tile each (group 0 tile 2p, group 1 tile 2p + 1), one thread per
+// query row (= TMEM lane), and run out of phase: while one group turns its
+// scores into probabilities, the tensor core runs the other group's P U and the
+// next scores. Items are numbered heaviest pair first and taken from a global
+// counter by each CTA's producer as it needs them (longest-first list
+// scheduling over the persistent CTAs).
+//
+// The score tiles of both groups form ONE sequence in a fixed order: per item,
+// for key tile j, group 0's (if j <= 2p) then group 1's (if the tile 2p + 1
+// exists). Score number k goes to TMEM buffer k % 3 (three 128-column
+// buffers). Two MMA-issuing warps walk the sequence: one waits for the
+// probabilities P(k) (written by the owning group over the first 64 columns of
+// buffer k % 3, two bf16 per column, released in two 64-key halves) and issues
+// O_g += P(k) U_j with the A operand in tensor memory; the other issues
+// S(k + 3) = Q K^T into that buffer once the P U of number k has completed. Each
+// group therefore finds its next score tile issued while it still works on the
+// current one.
+//
+// Per row, one running (lazily raised) max and sum over all keys: a tile's
+// probabilities are taken against the running max without a maximum pass (for
+// an item's first tile the reference is the row's first score); only when a
+// half tile's sum passes 2^16 (every probability is at most the sum, and an
+// overflow shows as an infinite sum) is its exact maximum taken, and the
+// running output and sum are rescaled when the max grows by more than 2^8. An
+// item's output is normalised, staged in shared memory and stored by TMA (one
+// 32-row box per warp; rows past T are clipped by the copy) during the group's
+// next tile, just before that tile's first P U overwrites the accumulator.
+//
+// Tensor memory (512 columns): score buffers at 0, 128, 256; O_g at 384 + 64 g.
+// Warp roles (352 threads, one persistent CTA per SM):
+//   warp 0      TMA producer: takes work items, loads both query tiles of an item and then
+//               K_j, U_j into a four-stage ring
+//   warp 1      TMEM allocator; issues the P U MMAs (the whole warp runs the loop, one elected lane issues)
+//   warps 2-5   softmax group 0; warps 6-9 softmax group 1
+//   warp 10     issues the score MMAs
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.h"
@@ -52,48 +61,50 @@ namespace {
 
 constexpr int BQ = kAttnBQ;       // query rows per tile
 constexpr int BKV = 128;          // keys per tile
-constexpr int THREADS = 320;
+constexpr int THREADS = 352;
 constexpr int TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by more than this
-constexpr float kSumLimit = 65536.0f;   // off-diagonal tiles: recompute against the exact max past this sum
-constexpr int NS = 5;                   // K/U ring depth (key tiles in flight)
-constexpr uint32_t NSB = 3;             // score buffers: S(j+3) is issued while the softmax works on S(j+1)
-// TMEM columns
-constexpr uint32_t kColS = 0;           // S[k] at 128 k, k < NSB
-constexpr uint32_t kColO = 128 * NSB;   // O (half h at + 64 h): 384..511
+constexpr float kSumLimit = 65536.0f;   // recompute a tile against its exact max past this sum
+constexpr int NS = 4;                   // K/U ring depth; the MMA warp's look-ahead needs at least 4
+constexpr int NSB = 3;                  // score buffers
+constexpr uint32_t kColO = 128 * NSB;   // O_g at kColO + 64 g
+constexpr int SR = 8;                   // work items announced ahead by the producer (ring slots)
+constexpr int kConsumers = 10;          // warps that read each announced item: 2 MMA issuers + 8 softmax
 
 template <int D>
 struct AttnCfg {
   static constexpr int ROWB = D * 2;                               // bytes per row of a Q/K/U tile
   static constexpr uint32_t SWZ = (ROWB == 128) ? SWZ_128B : SWZ_64B;
   static constexpr int TILE = BQ * ROWB;
-  static constexpr int OFF_Q = 0;                                    // Q[0], Q[1]
-  static constexpr int OFF_K = 2 * TILE;                             // NS stages
+  static constexpr int STG = 32 * ROWB;                            // one warp's 32 output rows
+  static constexpr int OFF_Q = 0;                                    // [buffer][group] query tiles
+  static constexpr int OFF_K = 4 * TILE;                             // NS stages
   static constexpr int OFF_U = OFF_K + NS * TILE;                    // NS stages
-  static constexpr int OFF_ML = OFF_U + NS * TILE;                  // (max, sum) of both halves of every row
-  static constexpr int OFF_BAR = OFF_ML + 2 * BQ * 8;
+  static constexpr int OFF_STG = OFF_U + NS * TILE;                  // 8 warps' output staging
+  static constexpr int OFF_BAR = OFF_STG + 8 * STG;
   // at least 120 KB so that two CTAs (2 x 512 TMEM columns) never share an SM
-  static constexpr int SMEM = (OFF_BAR + 256 > 120 * 1024) ? OFF_BAR + 256 : 120 * 1024;
+  static constexpr int SMEM = (OFF_BAR + 512 > 120 * 1024) ? OFF_BAR + 512 : 120 * 1024;
   static_assert(D == 32 || D == 64, "head width");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct __align__(8) AttnBars {
-  uint64_t q_full[2];       // Q buffer r % 2 holds item r's query tile
   uint64_t q_empty[2];      // every S of the item that used Q buffer k has been computed
-  uint64_t kv_full[NS];
+  uint64_t kv_full[NS];     // ring stage holds K_j, U_j (and, for an item's first tile, its query tiles)
   uint64_t kv_empty[NS];
-  uint64_t s_full[NSB];     // score buffer b holds a new score tile
-  uint64_t p_full[NSB];     // buffer b holds a tile's probabilities (8 softmax warps)
-  uint64_t o_full[NSB];     // the P U of a step with buffer b has completed
-  uint64_t o_free;          // the output accumulator has been read out of TMEM (8 softmax warps)
-  uint64_t ml_full;         // both halves wrote their (max, sum) for the merge (8 softmax warps)
-  uint64_t drain;
+  uint64_t s_full[2][NSB];  // score buffer b holds a new score tile of group g (that group's uses of b, in order)
+  uint64_t p_full[NSB][2];  // score buffer b holds that tile's probabilities of keys [64 h, 64 h + 64) (4 warps)
+  uint64_t pv_done[NSB];    // the P U that read buffer b has completed (the buffer may take new scores)
+  uint64_t o_full[2][3];    // group g's P U number i (its own count) has completed: barrier i % 3
+  uint64_t drain[2];        // the issuing warps' own MMAs have completed (exit)
+  uint64_t sched_full[SR];  // slot r % SR holds this CTA's r-th work item (from the producer)
+  uint64_t sched_empty[SR]; // every consumer warp has read the slot
+  int sched_item[SR];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(AttnBars) <= 256, "barrier block");
+static_assert(sizeof(AttnBars) <= 512, "barrier block");
 
 // The start-address field is the low 14 bits of a descriptor (address >> 4), and
 // every operand here lies below 256 KB, so advancing an operand by `bytes` is a
@@ -108,49 +119,94 @@ __device__ __forceinline__ void issue_s(uint32_t tS, uint64_t q_desc, uint64_t k
     tc_mma_bf16_warp(tS, desc_add(q_desc, k * 32), desc_add(k_desc, k * 32), idesc, k > 0 ? 1u : 0u);
 }
 
-// O_h += P(j)_h U_h for both key halves h: P(j) lies in TMEM over the first 32
-// columns of each 64-column half of its score buffer (two bf16 per column, row =
-// lane), U_j is MN-major in shared memory (D contiguous per key).
+// O += P_h U_h for keys [64 h, 64 h + 64) of a tile: P lies in TMEM over the first 64
+// columns of its score buffer (two bf16 per column, row = lane; keys 64 h.. at column 32 h),
+// U is MN-major in shared memory (D contiguous per key).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint64_t u_desc, bool accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t tO, uint32_t tP, uint64_t u_desc, int h, bool accumulate) {
   using Cfg = AttnCfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(BQ, D, true);     // U is MN-major (D contiguous)
 #pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      // a K step of 16 keys is 8 TMEM columns of P and 16 rows of ROWB bytes of U
-      tc_mma_bf16_ts_warp(tO + 64 * hf, tP + 64 * hf + 8 * kk, desc_add(u_desc, (hf * 64 + kk * 16) * Cfg::ROWB),
-                          idesc, (accumulate || kk > 0) ? 1u : 0u);
-    }
-  }
+  for (int kk = 0; kk < 4; ++kk)            // a K step of 16 keys: 8 TMEM columns of P, 16 rows of U
+    tc_mma_bf16_ts_warp(tO, tP + 32 * h + 8 * kk, desc_add(u_desc, (64 * h + 16 * kk) * Cfg::ROWB), idesc,
+                        (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Work item `r` of this CTA's sequence: items are (query tile, b, h) with the
-// heaviest tiles first, dealt to the CTAs in a snake order (CTA c takes c,
-// 2G-1-c, 2G+c, ...) so long and short items even out across the grid.
-__device__ __forceinline__ int item_of(int r, int cta, int G) {
-  return (r & 1) ? r * G + (G - 1 - cta) : r * G + cta;
+// Work items are ((b, h), query-tile pair), numbered heaviest pair first. A CTA's producer
+// takes the next number from a global counter whenever it starts an item (so the work
+// evens out across the CTAs the way longest-first list scheduling does) and announces it to
+// the CTA's other warps through a ring of SR slots; a number >= the item count ends the list.
+__device__ __forceinline__ int next_item(AttnBars* bars, int r, volatile int* abort_flag, int* err, int lane) {
+  const int slot = r % SR;
+  if (!mbar_wait_warp(&bars->sched_full[slot], static_cast<uint32_t>(r / SR) & 1u, abort_flag, err)) return 0x7fffffff;
+  const int item = reinterpret_cast<volatile int*>(bars->sched_item)[slot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars->sched_empty[slot]);
+  return item;
 }
 
 struct Item {
-  int b, h, qt, n;          // n: key tiles 0..qt
+  int b, h, qt0;            // query tiles qt0 (group 0) and qt0 + 1 (group 1)
+  int n0, n1;               // key tiles of each group: qt + 1, or 0 for a tile past the sequence
+  int nkv;                  // key tiles the item loads: max(n0, n1)
 };
 
-__device__ __forceinline__ Item decode_item(int item, int BH, int H, int n_qtiles) {
+__device__ __forceinline__ Item decode_item(int item, int BH, int H, int n_qtiles, int n_pairs) {
   Item w;
-  w.qt = n_qtiles - 1 - item / BH;
+  const int p = n_pairs - 1 - item / BH;
   const int bh = item % BH;
   w.b = bh / H;
   w.h = bh % H;
-  w.n = w.qt + 1;
+  w.qt0 = 2 * p;
+  w.n0 = w.qt0 + 1;
+  w.n1 = (w.qt0 + 1 < n_qtiles) ? w.qt0 + 2 : 0;
+  w.nkv = w.n1 > w.n0 ? w.n1 : w.n0;
   return w;
+}
+
+// Walks the score-tile sequence of one CTA for the MMA warp: item r, key tile j, group g,
+// with the item's tile counts and the ring position of its key tile 0.
+struct Cursor {
+  int r, j, g, n0, n1, nkv;
+  uint32_t kvb;
+  bool valid;
+  __device__ __forceinline__ void load(AttnBars* bars, volatile int* abort_flag, int* err, int lane, int n_items, int BH,
+                                       int n_qtiles, int n_pairs) {
+    const int item = next_item(bars, r, abort_flag, err, lane);
+    valid = item < n_items;
+    if (valid) {
+      const int qt0 = 2 * (n_pairs - 1 - item / BH);
+      n0 = qt0 + 1;
+      n1 = (qt0 + 1 < n_qtiles) ? qt0 + 2 : 0;
+      nkv = n1 > n0 ? n1 : n0;
+    }
+  }
+  __device__ __forceinline__ void advance(AttnBars* bars, volatile int* abort_flag, int* err, int lane, int n_items,
+                                          int BH, int n_qtiles, int n_pairs) {
+    if (g == 0 && j < n1) { g = 1; return; }
+    if (++j < nkv) { g = (j < n0) ? 0 : 1; return; }
+    kvb += nkv;
+    ++r;
+    j = 0;
+    g = 0;
+    load(bars, abort_flag, err, lane, n_items, BH, n_qtiles, n_pairs);
+  }
+  __device__ __forceinline__ uint32_t pos() const { return kvb + j; }
+  // the element is the last MMA reader of its ring position / the item's last score tile
+  __device__ __forceinline__ bool last_of_pos() const { return g == 1 || j >= n1; }
+  __device__ __forceinline__ bool last_of_item() const { return j == nkv - 1 && last_of_pos(); }
+};
+
+// 16-byte unit u of row r of a staging box (rows of ROWB bytes) in the TMA swizzle of that width.
+template <int ROWB>
+__device__ __forceinline__ int swz_unit(int r, int u) {
+  return (ROWB == 128) ? (u ^ (r & 7)) : (u ^ ((r >> 1) & 3));
 }
 
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
-attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, int B, int T,
-                   int H, int n_qtiles, float scale_log2, int* err) {
+attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_y, int B,
+                   int T, int H, int n_qtiles, float scale_log2, int* err, int* sched) {
   using Cfg = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   AttnBars* bars = reinterpret_cast<AttnBars*>(smem_raw + Cfg::OFF_BAR);
@@ -167,31 +223,38 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
 
   const int BH = B * H;
   const int C = H * D;
-  const int n_items = n_qtiles * BH;
-  const int G = static_cast<int>(gridDim.x);
-  const int cta = static_cast<int>(blockIdx.x);
+  const int n_pairs = (n_qtiles + 1) / 2;
+  const int n_items = n_pairs * BH;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
+      for (int k = 0; k < 3; ++k) mbar_init(&bars->o_full[i][k], 1);
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->kv_empty[i], 2);                // K read by the score warp, U by the P U warp
     }
-    for (uint32_t i = 0; i < NSB; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 8);
-      mbar_init(&bars->o_full[i], 1);
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(&bars->s_full[0][i], 1);
+      mbar_init(&bars->s_full[1][i], 1);
+      mbar_init(&bars->p_full[i][0], 4);
+      mbar_init(&bars->p_full[i][1], 4);
+      mbar_init(&bars->pv_done[i], 1);
     }
-    mbar_init(&bars->o_free, 8);
-    mbar_init(&bars->ml_full, 8);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain[0], 1);
+    mbar_init(&bars->drain[1], 1);
+    for (int i = 0; i < SR; ++i) {
+      mbar_init(&bars->sched_full[i], 1);
+      mbar_init(&bars->sched_empty[i], kConsumers);
+    }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm);
+    tma_prefetch_desc(&tm_y);
+  }
   if (warp == 1) tmem_alloc(&bars->tmem_base, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -205,22 +268,26 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
     if (lane == 0) {
       uint32_t issued = 0, last_par = 0;
       uint32_t kv_it = 0;                            // K/U tiles loaded so far (ring position)
-      uint32_t q_loads = 0;                          // Q tiles loaded so far (q_full phases)
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int item = item_of(r, cta, G);
+        const int slot = r % SR;                     // announce the CTA's r-th item
+        if (r >= SR && !mbar_wait(&bars->sched_empty[slot], static_cast<uint32_t>(r / SR - 1) & 1u, abort_flag, err)) break;
+        const int item = atomicAdd(sched, 1);
+        reinterpret_cast<volatile int*>(bars->sched_item)[slot] = item;
+        mbar_arrive(&bars->sched_full[slot]);
         if (item >= n_items) break;
-        const Item w = decode_item(item, BH, H, n_qtiles);
+        const Item w = decode_item(item, BH, H, n_qtiles, n_pairs);
         const int qb = r & 1;                        // Q buffer of this item; its previous user was item r - 2
         if (r >= 2 && !mbar_wait(&bars->q_empty[qb], static_cast<uint32_t>((r >> 1) - 1) & 1u, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&bars->q_full[qb], Cfg::TILE);
-        tma_load_3d(sQ + qb * Cfg::TILE, &tm, &bars->q_full[qb], w.h * D, w.qt * BQ, w.b);
-        ++q_loads;
-        for (int j = 0; j < w.n; ++j, ++kv_it) {
+        for (int j = 0; j < w.nkv; ++j, ++kv_it) {
           const int s = kv_it % NS;
           const uint32_t use_par = (kv_it / NS) & 1u;
           if (!mbar_wait(&bars->kv_empty[s], use_par ^ 1u, abort_flag, err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->kv_full[s], 2 * Cfg::TILE);
+          // the item's query tiles complete on the barrier of its first K/U tile
+          const int nq = (j == 0) ? (w.n1 > 0 ? 2 : 1) : 0;
+          mbar_arrive_expect_tx(&bars->kv_full[s], (2 + nq) * Cfg::TILE);
+          if (nq > 0) tma_load_3d(sQ + (2 * qb) * Cfg::TILE, &tm, &bars->kv_full[s], w.h * D, w.qt0 * BQ, w.b);
+          if (nq > 1) tma_load_3d(sQ + (2 * qb + 1) * Cfg::TILE, &tm, &bars->kv_full[s], w.h * D, (w.qt0 + 1) * BQ, w.b);
           tma_load_3d(sK + s * Cfg::TILE, &tm, &bars->kv_full[s], C + w.h * D, j * BKV, w.b);
           tma_load_3d(sU + s * Cfg::TILE, &tm, &bars->kv_full[s], 2 * C + w.h * D, j * BKV, w.b);
           issued |= 1u << s;
@@ -228,256 +295,304 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
         }
       }
       // never leave with copies in flight into this CTA's shared memory
-      for (uint32_t k = q_loads > 2 ? q_loads - 2 : 0; k < q_loads; ++k)
-        mbar_wait_drain(&bars->q_full[k & 1u], (k >> 1) & 1u);
       for (int s = 0; s < NS; ++s)
         if (issued & (1u << s)) mbar_wait_drain(&bars->kv_full[s], (last_par >> s) & 1u);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer (whole warp; one elected lane issues)
+  } else if (warp == 1 || warp == 10) {
+    // ------------------------------------------------ MMA issuers (whole warp; one elected lane issues)
+    // Two warps on different sub-partitions share the issue work, each walking the same
+    // sequence of score numbers: warp 1 waits for P(k) and issues O_g += P(k) U_j; warp 10
+    // issues S(k) = Q K_j^T into buffer k % 3 once the P U of number k - 3 (which read that
+    // buffer) has completed. A ring stage is released after both the last S reading its K and
+    // the last P U reading its U; S(k) lies at most three ring positions past the oldest
+    // unreleased stage, so four stages never wait on each other.
     {
-      // base descriptors: Q and K K-major (8-row groups ROWB*8 apart), P K-major
-      // 128-byte swizzle, U MN-major (K-direction 8-row groups ROWB*8 apart)
+      const bool pv_warp = warp == 1;
+      // base descriptors: Q and K K-major (8-row groups ROWB*8 apart), U MN-major (K-direction
+      // 8-row groups ROWB*8 apart)
       const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 8 * Cfg::ROWB, Cfg::SWZ);
       const uint64_t du0 = smem_desc(smem_u32(sU), Cfg::TILE, 8 * Cfg::ROWB, Cfg::SWZ);
-      uint32_t kv_it = 0;                            // K/U tiles consumed so far (ring position)
-      uint32_t gs = 0;                               // score tiles so far: step g uses buffers g % 2
-      uint32_t items_done = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int item = item_of(r, cta, G);
-        if (item >= n_items) break;
-        const Item w = decode_item(item, BH, H, n_qtiles);
-        const int qb = r & 1;
-        if (!mbar_wait_warp(&bars->q_full[qb], static_cast<uint32_t>(r >> 1) & 1u, abort_flag, err)) break;
-        const uint64_t dq = desc_add(dq0, qb * Cfg::TILE);
-        const uint32_t tO = tmem_base + kColO;
-        // the first two score tiles (the softmax read both buffers' previous tiles before
-        // handing over the previous item's last probabilities)
-        for (int jj = 0; jj < static_cast<int>(NSB) && jj < w.n; ++jj) {
-          const uint32_t t = kv_it + jj;
-          const uint32_t b = (gs + jj) % NSB;
-          if (!mbar_wait_warp(&bars->kv_full[t % NS], (t / NS) & 1u, abort_flag, err)) { ok = false; break; }
+      Cursor c;
+      c.r = 0;
+      c.j = 0;
+      c.g = 0;
+      c.kvb = 0;
+      c.load(bars, abort_flag, err, lane, n_items, BH, n_qtiles, n_pairs);
+      uint32_t b = 0;                                // buffer of number k (k % 3)
+      uint32_t bits = 0;                             // phase per buffer of the barrier this warp waits on
+      if (pv_warp) {
+        uint32_t oi0 = 0, oi1 = 0;                   // next o_full barrier per group (P U count % 3)
+        while (c.valid) {
+          const uint32_t st = c.pos() % NS;
+          const uint32_t tOg = tmem_base + kColO + 64 * c.g;
+          // keys [0, 64) as soon as the group releases them, then keys [64, 128)
+          if (!mbar_wait_warp(&bars->p_full[b][0], (bits >> b) & 1u, abort_flag, err)) break;
           tc_fence_after();
-          issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t % NS) * Cfg::TILE));
-          tc_commit_warp(&bars->s_full[b]);
-        }
-        for (int j = 0; j < w.n && ok; ++j) {
-          const uint32_t g = gs + j;
-          const uint32_t b = g % NSB;
-          const uint32_t s = (kv_it + j) % NS;
-          if (!mbar_wait_warp(&bars->p_full[b], (g / NSB) & 1u, abort_flag, err)) { ok = false; break; }
-          // the previous item's output has been read out of the accumulator
-          if (j == 0 && items_done >= 1 &&
-              !mbar_wait_warp(&bars->o_free, (items_done - 1) & 1u, abort_flag, err)) { ok = false; break; }
+          issue_pv_half<D>(tOg, tmem_base + 128 * b, desc_add(du0, st * Cfg::TILE), 0, c.j > 0);
+          if (!mbar_wait_warp(&bars->p_full[b][1], (bits >> b) & 1u, abort_flag, err)) break;
+          bits ^= 1u << b;
           tc_fence_after();
-          issue_pv<D>(tO, tmem_base + kColS + 128 * b, desc_add(du0, s * Cfg::TILE), j > 0);
-          tc_commit_warp(&bars->o_full[b]);
-          tc_commit_warp(&bars->kv_empty[s]);        // K_j and U_j are consumed
-          // the score tile after next into buffer b: issued after P(j) U_j, which reads
-          // P(j) out of the same columns (one thread's MMAs run in issue order)
-          if (j + static_cast<int>(NSB) < w.n) {
-            const uint32_t t2 = kv_it + j + NSB;
-            if (!mbar_wait_warp(&bars->kv_full[t2 % NS], (t2 / NS) & 1u, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            issue_s<D>(tmem_base + kColS + 128 * b, dq, desc_add(dk0, (t2 % NS) * Cfg::TILE));
-            tc_commit_warp(&bars->s_full[b]);
+          issue_pv_half<D>(tOg, tmem_base + 128 * b, desc_add(du0, st * Cfg::TILE), 1, true);
+          tc_commit_warp(&bars->pv_done[b]);
+          if (c.g) {
+            tc_commit_warp(&bars->o_full[1][oi1]);
+            oi1 = oi1 == 2 ? 0 : oi1 + 1;
+          } else {
+            tc_commit_warp(&bars->o_full[0][oi0]);
+            oi0 = oi0 == 2 ? 0 : oi0 + 1;
           }
+          if (c.last_of_pos()) tc_commit_warp(&bars->kv_empty[st]);   // U_j is consumed
+          c.advance(bars, abort_flag, err, lane, n_items, BH, n_qtiles, n_pairs);
+          b = b == NSB - 1 ? 0 : b + 1;
         }
-        if (!ok) break;
-        tc_commit_warp(&bars->q_empty[qb]);          // every S of this item has read its Q
-        gs += w.n;
-        kv_it += w.n;
-        ++items_done;
+      } else {
+        uint32_t n = 0;                              // score number
+        uint32_t waited = 0xffffffffu;               // ring position whose K/U (and Q) was last waited for
+        while (c.valid) {
+          if (n >= NSB) {                            // the P U that read this buffer has completed
+            if (!mbar_wait_warp(&bars->pv_done[b], (bits >> b) & 1u, abort_flag, err)) break;
+            bits ^= 1u << b;
+          }
+          const uint32_t pos = c.pos();
+          const uint32_t st = pos % NS;
+          if (pos != waited) {
+            if (!mbar_wait_warp(&bars->kv_full[st], (pos / NS) & 1u, abort_flag, err)) break;
+            waited = pos;
+          }
+          tc_fence_after();
+          const uint32_t qb = static_cast<uint32_t>(c.r) & 1u;
+          issue_s<D>(tmem_base + 128 * b, desc_add(dq0, (2 * qb + c.g) * Cfg::TILE), desc_add(dk0, st * Cfg::TILE));
+          tc_commit_warp(c.g ? &bars->s_full[1][b] : &bars->s_full[0][b]);
+          if (c.last_of_pos()) tc_commit_warp(&bars->kv_empty[st]);   // K_j is consumed
+          if (c.last_of_item()) tc_commit_warp(&bars->q_empty[qb]);   // every S of the item has read its Q
+          c.advance(bars, abort_flag, err, lane, n_items, BH, n_qtiles, n_pairs);
+          b = b == NSB - 1 ? 0 : b + 1;
+          ++n;
+        }
       }
-      tc_commit_warp(&bars->drain);
-      mbar_wait_drain(&bars->drain, 0);
+      uint64_t* dr = &bars->drain[pv_warp ? 0 : 1];
+      tc_commit_warp(dr);
+      mbar_wait_drain(dr, 0);
     }
   } else {
-    // ------------------------------------------------ softmax
-    const int hf = (warp - 2) >> 2;                   // which 64 keys of every key tile
+    // ------------------------------------------------ softmax (group g owns query tile qt0 + g)
+    const int g = (warp - 2) >> 2;
     const int sub = warp & 3;
     const int r_row = sub * 32 + lane;                // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
-    float2* sML = reinterpret_cast<float2*>(smem_raw + Cfg::OFF_ML);   // [2 halves][BQ rows]
-    uint32_t gs = 0;
-    uint32_t items_done = 0;
+    const uint32_t tO = tmem_base + kColO + 64 * g + lane_off;
+    uint8_t* stg = smem_raw + Cfg::OFF_STG + (warp - 2) * Cfg::STG;
+    uint32_t kbase = 0;                               // score number of the item's first tile
+    uint32_t tiles = 0;                               // this group's tiles so far (its P U numbering)
+    uint32_t used0 = 0, used1 = 0, used2 = 0;         // this group's score tiles so far in buffers 0, 1, 2
     bool ok = true;
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
+    // An item's output is written during the group's next tile, just before that tile's first
+    // P U (which overwrites the accumulator) is released: by then the item's last P U has
+    // completed, so the group never idles on it.
+    bool pend = false;
+    float pl = 0.0f;                                  // the pending item's running sum
+    int pb = 0, ph = 0, pqt = 0;                      // its batch row, head and query tile
+    uint32_t plast = 0;                               // its last tile (this group's numbering)
+    auto write_out = [&]() -> bool {
+      if (!mbar_wait_warp(&bars->o_full[g][plast % 3], (plast / 3) & 1u, abort_flag, err)) return false;
+      tc_fence_after();
+      const float inv = 1.0f / pl;
+      uint32_t ov[D];
+      if constexpr (D == 64) {
+        uint32_t (&o64)[64] = *reinterpret_cast<uint32_t (*)[64]>(ov);
+        tmem_ld_32x32b_x64(tO, o64);
+      } else {
+        uint32_t (&o32)[32] = *reinterpret_cast<uint32_t (*)[32]>(ov);
+        tmem_ld_32x32b_x32(tO, o32);
+      }
+      tmem_ld_wait();
+      tc_fence_before();                        // the accumulator may be overwritten after this
+      if (lane == 0) bulk_wait_read_all();      // this warp's previous store has read its staging box
+      __syncwarp();
+      uint8_t* row = stg + lane * Cfg::ROWB;
+#pragma unroll
+      for (int u = 0; u < Cfg::ROWB / 16; ++u) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(ov[8 * u + 0]) * inv, __uint_as_float(ov[8 * u + 1]) * inv);
+        v.y = pack_bf16x2(__uint_as_float(ov[8 * u + 2]) * inv, __uint_as_float(ov[8 * u + 3]) * inv);
+        v.z = pack_bf16x2(__uint_as_float(ov[8 * u + 4]) * inv, __uint_as_float(ov[8 * u + 5]) * inv);
+        v.w = pack_bf16x2(__uint_as_float(ov[8 * u + 6]) * inv, __uint_as_float(ov[8 * u + 7]) * inv);
+        *reinterpret_cast<uint4*>(row + (swz_unit<Cfg::ROWB>(lane, u) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_y, stg, ph * D, pqt * BQ + sub * 32, pb);
+        bulk_commit();
+      }
+      pend = false;
+      return true;
+    };
     for (int r = 0; ok; ++r) {
-      const int item = item_of(r, cta, G);
+      const int item = next_item(bars, r, abort_flag, err, lane);
       if (item >= n_items) break;
-      const Item w = decode_item(item, BH, H, n_qtiles);
-      const int t = w.qt * BQ + r_row;                // query position
-      const uint32_t tO0 = tmem_base + kColO + lane_off;              // O of keys [0, 64)
-      const uint32_t tO = tO0 + 64 * hf;                                // this half's O
-      float m_run = -INFINITY;                        // running (lazily raised) max, log2 units
-      float l = 0.0f;                                 // running sum of 2^(s - m_run) over this half
-      for (int j = 0; j < w.n; ++j) {
-        const uint32_t g = gs + j;
-        const uint32_t b = g % NSB;
-        if (!mbar_wait_warp(&bars->s_full[b], (g / NSB) & 1u, abort_flag, err)) { ok = false; break; }
+      const Item w = decode_item(item, BH, H, n_qtiles, n_pairs);
+      const int n = g == 0 ? w.n0 : w.n1;
+      const uint32_t knext = kbase + w.n0 + w.n1;
+      if (n == 0) { kbase = knext; continue; }        // group 1 past the last query tile
+      const int qt = w.qt0 + g;
+      const int t = qt * BQ + r_row;                  // query position
+      float mr = -INFINITY;                           // running (lazily raised) max, log2 units
+      float l = 0.0f;                                 // running sum of 2^(s - mr)
+      for (int j = 0; j < n && ok; ++j) {
+        // this tile's score number and buffer
+        const uint32_t k = kbase + (g == 0 ? j + min(j, w.n1) : j + min(j + 1, w.n0));
+        const uint32_t b = k % NSB;
+        const uint32_t use = b == 0 ? used0++ : (b == 1 ? used1++ : used2++);
+        if (!mbar_wait_warp(&bars->s_full[g][b], use & 1u, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tS = tmem_base + kColS + 128 * b + 64 * hf + lane_off;
-        const bool diag = (j == w.n - 1);
-        const int kb = j * BKV + 64 * hf;             // first key of this half
-        // Raise this half's running max to m_new where `need`: scale its sum and output by
-        // 2^(m_run - m_new) (the output once every earlier P U has landed). Warp-uniform.
-        auto raise_max = [&](bool need, float m_new) -> bool {
-          if (j > 0) {                                // this half's O must hold all earlier P U
-            if (!mbar_wait_warp(&bars->o_full[(g - 1) % NSB], ((g - 1) / NSB) & 1u, abort_flag, err)) return false;
-            tc_fence_after();
-          }
-          const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-          if (need) m_run = m_new;
-          l *= alpha;
-          if (j > 0) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld_32x32b_x32(tO + c * 32, o);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st_32x32b_x32(tO + c * 32, o);
-            }
-            tmem_st_wait();
-          }
-          return true;
-        };
-        // Exact maximum of this half's allowed keys, eight independent chains.
-        auto tile_max = [&](const uint32_t (&v)[64]) -> float {
-          float mx8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = (!diag || kb + i <= t) ? __uint_as_float(v[i]) : -INFINITY;
-            const float bv = (!diag || kb + 32 + i <= t) ? __uint_as_float(v[32 + i]) : -INFINITY;
-            mx8[i & 7] = fmax3(mx8[i & 7], a, bv);
-          }
-          return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-        };
-        // pv = 2^(s*scale - m_run), two keys per f32x2 instruction; returns their sum
-        const float2 sc2 = make_float2(scale_log2, scale_log2);
-        auto probs = [&](const uint32_t (&v)[64], float (&p)[64]) -> float {
-          const float2 nm2 = make_float2(-m_run, -m_run);
+        const uint32_t tS = tmem_base + 128 * b + lane_off;
+        const bool diag = (j == n - 1);
+        const int kb = j * BKV;                       // first key of the tile
+        // pv = 2^(s*scale - mr) in place of the scores, two keys per f32x2 instruction;
+        // keys after t get 0 on the diagonal; returns the sum
+        auto probs = [&](uint32_t (&v)[64], int kb_half) -> float {
+          const float2 nm2 = make_float2(-mr, -mr);
 #pragma unroll
           for (int i = 0; i < 64; i += 2) {
             const float2 x = fma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc2, nm2);
-            p[i] = ex2_approx(x.x);
-            p[i + 1] = ex2_approx(x.y);
-          }
-          if (diag) {                                 // keys after t get probability 0
-#pragma unroll
-            for (int i = 0; i < 64; ++i) p[i] = (kb + i <= t) ? p[i] : 0.0f;
+            float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            if (diag) {
+              p0 = (kb_half + i <= t) ? p0 : 0.0f;
+              p1 = (kb_half + i + 1 <= t) ? p1 : 0.0f;
+            }
+            v[i] = __float_as_uint(p0);
+            v[i + 1] = __float_as_uint(p1);
           }
           float2 ls[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.0f, 0.0f);
+          for (int q = 0; q < 4; ++q) ls[q] = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int i = 0; i < 64; i += 2) ls[(i >> 1) & 3] = add2_rn(ls[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
+          for (int i = 0; i < 64; i += 2)
+            ls[(i >> 1) & 3] = add2_rn(ls[(i >> 1) & 3], make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
           const float2 l2 = add2_rn(add2_rn(ls[0], ls[1]), add2_rn(ls[2], ls[3]));
           return l2.x + l2.y;
         };
-        // this half's 64 scores (one 64-column TMEM load)
-        uint32_t sv[64];
-        tmem_ld_32x32b_x64(tS, sv);
-        tmem_ld_wait();
-        float pv[64];
-        float lt;                                     // this tile's sum of probabilities
-        if (!diag) {
-          // Off the diagonal no maximum pass: the probabilities are taken against the running
-          // max (for an item's first tile, against this row's first score), and only a tile
-          // whose sum passes 2^16 (every probability is at most its sum, and an overflow shows
-          // as an infinite sum) is recomputed against its exact maximum.
-          if (j == 0) m_run = __uint_as_float(sv[0]) * scale_log2;
-          lt = probs(sv, pv);
-          if (__any_sync(0xffffffffu, !(lt <= kSumLimit))) {
-            tmem_ld_32x32b_x64(tS, sv);               // the scores again (their registers were reused)
-            tmem_ld_wait();
-            const float m_new = fmaxf(m_run, tile_max(sv) * scale_log2);
-            if (!raise_max(m_new > m_run + kRescaleLog2, m_new)) { ok = false; break; }
-            tmem_ld_32x32b_x64(tS, sv);
-            tmem_ld_wait();
-            lt = probs(sv, pv);
-          }
-        } else {
-          // the diagonal tile: exact maximum first (a fully masked half leaves -inf: nothing to raise)
-          const float m_new = fmaxf(m_run, tile_max(sv) * scale_log2);
-          const bool need = m_new > m_run + kRescaleLog2;
-          if (__any_sync(0xffffffffu, need)) {
-            if (!raise_max(need, m_new)) { ok = false; break; }
-            tmem_ld_32x32b_x64(tS, sv);               // read the scores again rather than hold them
-            tmem_ld_wait();
-          }
-          lt = probs(sv, pv);
-        }
-        l += lt;
-        // P(j) as bf16 pairs over the first 32 columns of this half (its scores are in registers)
-        uint32_t pk[32];
+        // exact maximum of the allowed keys of one half, eight independent chains
+        auto half_max = [&](const uint32_t (&v)[64], int kb_half) -> float {
+          float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
-        tmem_st_32x32b_x32(tS, pk);
+          for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = (!diag || kb_half + i <= t) ? __uint_as_float(v[i]) : -INFINITY;
+            const float c = (!diag || kb_half + 32 + i <= t) ? __uint_as_float(v[32 + i]) : -INFINITY;
+            mx8[i & 7] = fmax3(mx8[i & 7], a, c);
+          }
+          return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        };
+        // The two 64-key halves in turn. A half's probabilities are final once its sum is checked
+        // (and, rarely, recomputed against a raised max); they are then stored as bf16 pairs over
+        // columns [32 hf, 32 hf + 32) of the buffer, whose scores are already in registers.
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t tSh = tS + 64 * hf;
+          const int kbh = kb + 64 * hf;
+          uint32_t sv[64];
+          tmem_ld_32x32b_x64(tSh, sv);
+          tmem_ld_wait();
+          if (j == 0 && hf == 0) mr = __uint_as_float(sv[0]) * scale_log2;   // key 0 is allowed for every row
+          float lt = probs(sv, kbh);
+          if (__any_sync(0xffffffffu, !(lt <= kSumLimit))) {
+            // rare: this half's exact maximum, a rescale of the running output and sum (and of
+            // the first half's stored probabilities) where the max grew by more than 2^8, and
+            // the half again against the new reference
+            tmem_ld_32x32b_x64(tSh, sv);
+            tmem_ld_wait();
+            const float m_new = fmaxf(mr, half_max(sv, kbh) * scale_log2);
+            const bool need = m_new > mr + kRescaleLog2;
+            if (__any_sync(0xffffffffu, need)) {
+              const float alpha = need ? ex2_approx(mr - m_new) : 1.0f;
+              if (need) mr = m_new;
+              l *= alpha;
+              if (j > 0) {
+                // every earlier P U of the group has completed (its own numbering, barrier i % 3)
+                const uint32_t last = tiles - 1;
+                if (!mbar_wait_warp(&bars->o_full[g][last % 3], (last / 3) & 1u, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                  uint32_t o[32];
+                  tmem_ld_32x32b_x32(tO + c * 32, o);
+                  tmem_ld_wait();
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st_32x32b_x32(tO + c * 32, o);
+                }
+              }
+              if (hf == 1) {                          // the first half's probabilities, already stored
+                tmem_st_wait();
+                uint32_t q[32];
+                tmem_ld_32x32b_x32(tS, q);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float2 f = unpack_bf16x2(q[i]);
+                  q[i] = pack_bf16x2(f.x * alpha, f.y * alpha);
+                }
+                tmem_st_32x32b_x32(tS, q);
+              }
+              tmem_st_wait();
+            }
+            tmem_ld_32x32b_x64(tSh, sv);
+            tmem_ld_wait();
+            lt = probs(sv, kbh);
+          }
+          l += lt;
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+          if (hf == 1) {
+            // the previous item's output leaves the accumulator before this item's first P U
+            if (j == 0 && pend && !write_out()) { ok = false; break; }
+            tmem_st_wait();                           // keys [0, 64) are final: hand them to the P U warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[b][0]);
+          }
+          tmem_st_32x32b_x32(tS + 32 * hf, pk);
+        }
+        if (!ok) break;
         tmem_st_wait();
         tc_fence_before();                      // our TMEM reads of S and writes of P precede the next MMA
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[b]);
+        if (lane == 0) mbar_arrive(&bars->p_full[b][1]);
+        ++tiles;
       }
       if (!ok) break;
-      // the item's output: both threads of a row exchange (max, sum); each writes D/2 columns
-      const uint32_t glast = gs + w.n - 1;
-      if (!mbar_wait_warp(&bars->o_full[glast % NSB], (glast / NSB) & 1u, abort_flag, err)) break;
-      tc_fence_after();
-      sML[hf * BQ + r_row] = make_float2(m_run, l);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ml_full);
-      if (!mbar_wait_warp(&bars->ml_full, items_done & 1u, abort_flag, err)) break;
-      const float2 other = sML[(hf ^ 1) * BQ + r_row];
-      const float m0 = hf == 0 ? m_run : other.x, l0 = hf == 0 ? l : other.y;
-      const float m1 = hf == 0 ? other.x : m_run, l1 = hf == 0 ? other.y : l;
-      const float m = fmaxf(m0, m1);                // finite: key 0 of tile 0 is always allowed
-      const float a0 = ex2_approx(m0 - m);
-      const float a1 = ex2_approx(m1 - m);          // 0 when the upper half never had an allowed key
-      const float inv = 1.0f / (a0 * l0 + a1 * l1);
-      const float w0 = a0 * inv, w1 = a1 * inv;
-      constexpr int DH = D / 2;                      // output columns per thread
-      const int c0 = hf * DH;
-      uint32_t v0[DH], v1[DH];
-      if constexpr (DH == 32) {
-        tmem_ld_32x32b_x32(tO0 + c0, v0);
-        tmem_ld_32x32b_x32(tO0 + 64 + c0, v1);
-      } else {
-        tmem_ld_32x32b_x16(tO0 + c0, v0);
-        tmem_ld_32x32b_x16(tO0 + 64 + c0, v1);
-      }
-      tmem_ld_wait();
-      tc_fence_before();                             // the accumulator may be overwritten after this
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_free);
-      if (t < T) {
-        uint4* dst = reinterpret_cast<uint4*>(y + ((size_t)w.b * T + t) * C + w.h * D + c0);
-#pragma unroll
-        for (int q = 0; q < DH / 8; ++q) {
-          float f[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = w0 * __uint_as_float(v0[8 * q + i]) + w1 * __uint_as_float(v1[8 * q + i]);
-          uint4 wv;
-          wv.x = pack_bf16x2(f[0], f[1]);
-          wv.y = pack_bf16x2(f[2], f[3]);
-          wv.z = pack_bf16x2(f[4], f[5]);
-          wv.w = pack_bf16x2(f[6], f[7]);
-          dst[q] = wv;
-        }
-      }
-      gs += w.n;
-      ++items_done;
+      // the item's output is written during the group's next tile (or after the last item)
+      pend = true;
+      pl = l;
+      pb = w.b;
+      ph = w.h;
+      pqt = qt;
+      plast = tiles - 1;
+      kbase = knext;
     }
+    if (ok && pend) write_out();
+    if (lane == 0) bulk_wait_all();              // stores complete before the CTA exits
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    // every CTA has taken its last number once all have arrived here: the last one resets the
+    // counter for the next launch
+    __threadfence();
+    if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      sched[0] = 0;
+      sched[1] = 0;
+      __threadfence();
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -485,7 +600,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __rest
 }
 
 template <int D>
-cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* err, cudaStream_t s) {
+cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* err, int* sched, cudaStream_t s) {
   using Cfg = AttnCfg<D>;
   static bool attr_set = false;
   static int num_sms = 0;
@@ -500,21 +615,24 @@ cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* e
     attr_set = true;
   }
   const int n_qtiles = (T + BQ - 1) / BQ;
-  const long long items = (long long)n_qtiles * B * H;
+  const long long items = (long long)((n_qtiles + 1) / 2) * B * H;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  CUtensorMap tm_y;
+  if (!make_tmap_attn_out(&tm_y, y, B, T, H * D, D)) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   const float scale_log2 = kLog2e / sqrtf(static_cast<float>(D));
-  return launch_k(attn_fwd_tc_kernel<D>, dim3(grid), dim3(THREADS), Cfg::SMEM, s, tm,
-                  reinterpret_cast<__nv_bfloat16*>(y), B, T, H, n_qtiles, scale_log2, err);
+  return launch_k(attn_fwd_tc_kernel<D>, dim3(grid), dim3(THREADS), Cfg::SMEM, s, tm, tm_y, B, T, H, n_qtiles,
+                  scale_log2, err, sched);
 }
 
 }  // namespace
 
 cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T, int H, int D, int* err,
-                                cudaStream_t s) {
-  if (D == 64) return launch_d<64>(tm_qkv, y, B, T, H, err, s);
-  if (D == 32) return launch_d<32>(tm_qkv, y, B, T, H, err, s);
+                                int* sched, cudaStream_t s) {
+  if (!sched) return cudaErrorInvalidValue;
+  if (D == 64) return launch_d<64>(tm_qkv, y, B, T, H, err, sched, s);
+  if (D == 32) return launch_d<32>(tm_qkv, y, B, T, H, err, sched, s);
   return cudaErrorInvalidValue;
 }
 

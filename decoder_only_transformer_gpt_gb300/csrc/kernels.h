@@ -79,8 +79,10 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            const GemmArgs& a, int epi, int grid_limit, cudaStream_t s);
 
 constexpr int kAttnBQ = 128;
+// sched: 2 device ints, zero before the launch; the kernel's CTAs take work items from it and the
+// last CTA to finish sets it back to zero. Launches sharing one sched must be ordered.
 cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T, int H, int D,
-                                int* err, cudaStream_t s);
+                                int* err, int* sched, cudaStream_t s);
 
 // ---- row-wise kernels (both paths)
 // Row m is token m of its sequence at position pos0 + m % T (pos0 read from pos_dev when non-null).
@@ -155,6 +157,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t r
                   uint32_t box_cols, uint32_t box_rows, uint64_t ld = 0);
 // qkv viewed as [B][T][3C] bf16 with a box of 128 rows x D columns (one batch).
 bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int D);
+// y viewed as [B][T][C] bf16 with a box of 32 rows x D columns (the attention kernel's output stores).
+bool make_tmap_attn_out(CUtensorMap* map, const void* base, int B, int T, int C, int D);
 
 // ---- incremental decoding (bf16)
 constexpr int kGemvMaxRows = 16;       // rows per matrix-vector launch

@@ -69,6 +69,7 @@ struct gpt_model {
   bool capturing = false;       // a forward or decode step is being captured into a graph
   gpt_train* tr = nullptr;      // allocated by the first gpt_backward
   int* err = nullptr;       // device error word
+  int* attn_sched = nullptr;   // attention work counter (2 ints, zero between launches)
   int32_t* stage_ids = nullptr;
   int32_t* stage_tg = nullptr;
   float* stage_loss = nullptr;

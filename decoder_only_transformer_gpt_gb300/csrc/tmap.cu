@@ -74,4 +74,20 @@ bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The attention output y viewed as [B][T][C] bf16 with a box of 32 rows x D columns (one batch),
+// for the TMA store of each warp's 32 query rows of one head: rows past T are clipped by the copy.
+bool make_tmap_attn_out(CUtensorMap* map, const void* base, int B, int T, int C, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || ((C * 2) & 15) || (D != 32 && D != 64))
+    return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2, static_cast<cuuint64_t>(C) * 2 * T};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = (D == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gptgb
