@@ -40,6 +40,7 @@ struct gpt_layer_act {
   void *a1, *qkv, *y, *a2, *u, *g;   // bf16: ln_1 output (post-norm: x itself), c_attn out, attention
                                      // out, ln_2 output (post-norm: n), c_fc pre- and post-GELU
   float *s1, *n, *s2;            // fp32: x + attention branch; post-norm: LN1(s1), n + MLP branch
+  float* lse2 = nullptr;         // the attention rows' base-2 log-sum-exp [B*H][T] (from the forward)
   CUtensorMap A_a1, A_y, A_a2, A_g;        // as GEMM A operands
   CUtensorMap K_a1, K_y, K_a2, K_g;        // as MN-major operands of the weight-gradient products
   CUtensorMap C_qkv, C_u, C_g, Q3;         // as epilogue outputs; qkv as the attention input
@@ -63,6 +64,8 @@ struct gpt_train {
   float *dx, *da;
   void *dxb, *dyb, *dqkv, *du;
   float *lse2, *dsum;
+  float* dqacc = nullptr;        // fp32 [M, C] dQ of the attention derivative (zero between calls)
+  CUtensorMap T_dy, T_dkv, T_dq; // dy, dqkv and dqacc as the attention derivative's TMA operands
   void* dz;
   // activation maps, for one (B, T)
   int mB = -1, mT = -1;
@@ -147,6 +150,7 @@ int alloc_train(gpt_model* m) {
       q.s1 = static_cast<float*>(cv.take(Mx * C * 4));
       q.n = post ? static_cast<float*>(cv.take(Mx * C * 4)) : nullptr;
       q.s2 = post ? static_cast<float*>(cv.take(Mx * C * 4)) : nullptr;
+      q.lse2 = static_cast<float*>(cv.take(Mx * c.H * 4));
     }
     t->dx = static_cast<float*>(cv.take(Mx * C * 4));
     t->da = static_cast<float*>(cv.take(Mx * C * 4));
@@ -156,6 +160,7 @@ int alloc_train(gpt_model* m) {
     t->du = cv.take(Mx * F * 2);
     t->lse2 = static_cast<float*>(cv.take(Mx * c.H * 4));
     t->dsum = static_cast<float*>(cv.take(Mx * c.H * 4));
+    t->dqacc = static_cast<float*>(cv.take(Mx * C * 4));
     t->dz = cv.take(Mx * Vp * 2);
   };
   Carve sizing;
@@ -168,6 +173,11 @@ int alloc_train(gpt_model* m) {
   Carve real;
   real.base = t->buf;
   layout(real);
+  if (cudaMemset(t->dqacc, 0, Mx * C * 4) != cudaSuccess) {
+    cudaFree(t->buf);
+    delete t;
+    return GPT_ECUDA;
+  }
   // gradient pointers in the order of the weights
   float* p = t->gbuf;
   auto take = [&](size_t n) { float* q = p; p += n; return q; };
@@ -230,7 +240,9 @@ int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
       make_tmap_2d_bf16(&t->K_dqkv, t->dqkv, M, 3 * C, BK) &&
       make_tmap_2d(&t->C_dz, t->dz, 2, M, V, 64, kEpiRows, Vp) &&
       make_tmap_2d(&t->C_du, t->du, 2, M, F, 64, kEpiRows) && make_tmap_2d(&t->C_dyb, t->dyb, 2, M, C, 64, kEpiRows) &&
-      make_tmap_2d(&t->C_da, t->da, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_dx, t->dx, 4, M, C, 32, kEpiRows);
+      make_tmap_2d(&t->C_da, t->da, 4, M, C, 32, kEpiRows) && make_tmap_2d(&t->C_dx, t->dx, 4, M, C, 32, kEpiRows) &&
+      make_tmap_qkv(&t->T_dy, t->dyb, B, T, C, C / c.H) && make_tmap_attn_out(&t->T_dkv, t->dqkv, B, T, 3 * C, C / c.H) &&
+      make_tmap_bt_f32(&t->T_dq, t->dqacc, B, T, C);
   for (size_t l = 0; l < t->la.size() && ok; ++l) {
     gpt_layer_act& q = t->la[l];
     ok = make_tmap_2d_bf16(&q.A_a1, q.a1, M, C, BA) && make_tmap_2d_bf16(&q.A_y, q.y, M, C, BA) &&
@@ -380,7 +392,7 @@ int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t*
     void* next_a = (l + 1 < L) ? t->la[l + 1].a1 : m->a;
     GPT_CUDA(cudaMemcpyAsync(q.x, m->x, MC4, cudaMemcpyDeviceToDevice, s));
     BW(gemm_bf16(m, q.A_a1, w.tm_attn_w, q.C_qkv, M, 3 * C, C, w.attn_b, q.qkv, EPI_BIAS_OUT, s));
-    BW(cu(launch_attention_tc(q.Q3, q.y, B, T, c.H, C / c.H, m->err, m->attn_sched, s), "attention"));
+    BW(cu(launch_attention_tc(q.Q3, q.y, B, T, c.H, C / c.H, m->err, m->attn_sched, s, q.lse2), "attention"));
     BW(gemm_bf16(m, q.A_y, w.tm_proj_w, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
     GPT_CUDA(cudaMemcpyAsync(q.s1, m->x, MC4, cudaMemcpyDeviceToDevice, s));
     if (pre) {
@@ -471,8 +483,10 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
   BWS(GPT_STEP_B_PROJ_W, l, grad_gemm(m, t->K_dxb, q.K_y, g.tg_proj_w, g.proj_w, C, C, M, s));
   BWS(GPT_STEP_B_DY, l, gemm_bf16(m, t->A_dxb, g.tb_proj_wT, t->C_dyb, M, C, C, nullptr, t->dyb, EPI_BIAS_OUT, s));
   BWS(GPT_STEP_B_ATTN, l,
-      cu(launch_attention_bwd(q.qkv, q.y, t->dyb, t->dqkv, t->lse2, t->dsum, B, T, H, C / H, s), "attention'"));
-  ++t->launches;                                                                                   // two kernels
+      cu(launch_attention_bwd_tc(q.Q3, t->T_dy, t->T_dkv, t->T_dq, q.y, t->dyb, q.lse2, t->dsum, t->dqacc, t->dqkv, B,
+                                 T, H, C / H, m->err, m->attn_sched, s),
+         "attention'"));
+  t->launches += 2;                                          // three kernels: Dsum, the derivative, dQ to bf16
   BW(cu(launch_colsum(t->dqkv, 1, M, 3 * C, 3 * C, g.attn_b, m->num_sms, s), "db_attn"));
   BWS(GPT_STEP_B_ATTN_W, l, grad_gemm(m, t->K_dqkv, q.K_a1, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
   if (pre) {

@@ -206,7 +206,7 @@ __device__ __forceinline__ int swz_unit(int r, int u) {
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_y, int B,
-                   int T, int H, int n_qtiles, float scale_log2, int* err, int* sched) {
+                   int T, int H, int n_qtiles, float scale_log2, int* err, int* sched, float* lse2) {
   using Cfg = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   AttnBars* bars = reinterpret_cast<AttnBars*>(smem_raw + Cfg::OFF_BAR);
@@ -393,6 +393,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant
     // completed, so the group never idles on it.
     bool pend = false;
     float pl = 0.0f;                                  // the pending item's running sum
+    float pm = 0.0f;                                  // and its running max (log2 units)
     int pb = 0, ph = 0, pqt = 0;                      // its batch row, head and query tile
     uint32_t plast = 0;                               // its last tile (this group's numbering)
     auto write_out = [&]() -> bool {
@@ -426,6 +427,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant
       if (lane == 0) {
         tma_store_3d(&tm_y, stg, ph * D, pqt * BQ + sub * 32, pb);
         bulk_commit();
+      }
+      if (lse2 != nullptr) {                      // the row's base-2 log-sum-exp of the scaled scores
+        const int t = pqt * BQ + r_row;
+        if (t < T) lse2[(static_cast<size_t>(pb) * H + ph) * T + t] = pm + log2f(pl);
       }
       pend = false;
       return true;
@@ -570,6 +575,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant
       // the item's output is written during the group's next tile (or after the last item)
       pend = true;
       pl = l;
+      pm = mr;
       pb = w.b;
       ph = w.h;
       pqt = qt;
@@ -600,7 +606,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant
 }
 
 template <int D>
-cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* err, int* sched, cudaStream_t s) {
+cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* err, int* sched, float* lse2,
+                     cudaStream_t s) {
   using Cfg = AttnCfg<D>;
   static bool attr_set = false;
   static int num_sms = 0;
@@ -623,16 +630,16 @@ cudaError_t launch_d(const CUtensorMap& tm, void* y, int B, int T, int H, int* e
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   const float scale_log2 = kLog2e / sqrtf(static_cast<float>(D));
   return launch_k(attn_fwd_tc_kernel<D>, dim3(grid), dim3(THREADS), Cfg::SMEM, s, tm, tm_y, B, T, H, n_qtiles,
-                  scale_log2, err, sched);
+                  scale_log2, err, sched, lse2);
 }
 
 }  // namespace
 
 cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T, int H, int D, int* err,
-                                int* sched, cudaStream_t s) {
+                                int* sched, cudaStream_t s, float* lse2) {
   if (!sched) return cudaErrorInvalidValue;
-  if (D == 64) return launch_d<64>(tm_qkv, y, B, T, H, err, sched, s);
-  if (D == 32) return launch_d<32>(tm_qkv, y, B, T, H, err, sched, s);
+  if (D == 64) return launch_d<64>(tm_qkv, y, B, T, H, err, sched, lse2, s);
+  if (D == 32) return launch_d<32>(tm_qkv, y, B, T, H, err, sched, lse2, s);
   return cudaErrorInvalidValue;
 }
 

@@ -81,8 +81,10 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 constexpr int kAttnBQ = 128;
 // sched: 2 device ints, zero before the launch; the kernel's CTAs take work items from it and the
 // last CTA to finish sets it back to zero. Launches sharing one sched must be ordered.
+// lse2 (nullable): fp32 [B*H][T] receives each query row's base-2 log-sum-exp of its scaled scores
+// (log2 of the softmax denominator in units where the probabilities are 2^(s log2(e)/sqrt(D) - lse2)).
 cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, void* y, int B, int T, int H, int D,
-                                int* err, int* sched, cudaStream_t s);
+                                int* err, int* sched, cudaStream_t s, float* lse2 = nullptr);
 
 // ---- row-wise kernels (both paths)
 // Row m is token m of its sequence at position pos0 + m % T (pos0 read from pos_dev when non-null).
@@ -132,6 +134,15 @@ cudaError_t launch_embed_bwd(const float* dx0, const int32_t* ids, float* dE, fl
 // scaled scores and sum of dy * y. D = 32 or 64.
 cudaError_t launch_attention_bwd(const void* qkv, const void* y, const void* dy, void* dqkv, float* lse2, float* dsum,
                                  int B, int T, int H, int D, cudaStream_t s);
+// The same derivative on tcgen05 from the forward's row log-sum-exp (lse2 [B*H][T], base 2): tm_qkv is the
+// qkv map of make_tmap_qkv (128-row boxes), tm_dy the same over dy [B][T][C], tm_dkv make_tmap_attn_out
+// over dqkv [B][T][3C] (dK and dU are stored there), tm_dq make_tmap_bt_f32 over dqacc [B][T][C] fp32, which
+// must hold zeros and holds zeros again after the call (its dQ goes to dqkv's first third). dsum: fp32
+// [B*H][T] scratch. sched: 2 ints as for launch_attention_tc. D = 32 or 64.
+cudaError_t launch_attention_bwd_tc(const CUtensorMap& tm_qkv, const CUtensorMap& tm_dy, const CUtensorMap& tm_dkv,
+                                    const CUtensorMap& tm_dq, const void* y, const void* dy, const float* lse2,
+                                    float* dsum, float* dqacc, void* dqkv, int B, int T, int H, int D, int* err,
+                                    int* sched, cudaStream_t s);
 
 // One parameter tensor for the optimiser: values [off, off + n) of the flat gradient, master and
 // moment arrays, stored at dst (bf16 when bf16 != 0, else fp32); decay: decoupled weight decay applies.
@@ -159,6 +170,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t r
 bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int D);
 // y viewed as [B][T][C] bf16 with a box of 32 rows x D columns (the attention kernel's output stores).
 bool make_tmap_attn_out(CUtensorMap* map, const void* base, int B, int T, int C, int D);
+// fp32 [B][T][C] with a box of 32 rows x 32 columns (the attention derivative's dQ reduce-adds).
+bool make_tmap_bt_f32(CUtensorMap* map, const void* base, int B, int T, int C);
 
 // ---- incremental decoding (bf16)
 constexpr int kGemvMaxRows = 16;       // rows per matrix-vector launch

@@ -74,6 +74,20 @@ bool make_tmap_qkv(CUtensorMap* map, const void* base, int B, int T, int C3, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An fp32 [B][T][C] tensor with a box of 32 rows x 32 columns (128 bytes, 128-byte swizzle; one batch):
+// the attention derivative adds its dQ tiles into it with TMA reduce-adds. Rows past T are clipped.
+bool make_tmap_bt_f32(CUtensorMap* map, const void* base, int B, int T, int C) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || ((C * 4) & 15)) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 4, static_cast<cuuint64_t>(C) * 4 * T};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The attention output y viewed as [B][T][C] bf16 with a box of 32 rows x D columns (one batch),
 // for the TMA store of each warp's 32 query rows of one head: rows past T are clipped by the copy.
 bool make_tmap_attn_out(CUtensorMap* map, const void* base, int B, int T, int C, int D) {
