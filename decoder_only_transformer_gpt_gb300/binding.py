@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH):
         "gpt_master_copy": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
+        "gptk_attention_lse": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp]),
+        "gptk_attention_bwd": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
         "gptk_layernorm": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp]),
         "gptk_embed": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_lmhead_ce": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
@@ -290,6 +292,23 @@ def attention(qkv, y, H: int, stream=None):
     D = C3 // 3 // H
     dtype = 1 if qkv.element_size() == 2 else 0
     _check(lib.gptk_attention(_ptr(qkv), _ptr(y), B, T, H, D, dtype, _stream(stream)), "gptk_attention")
+
+
+def attention_lse(qkv, y, lse2, H: int, stream=None):
+    """bf16 attention that also writes each query row's base-2 log-sum-exp, lse2 fp32 [B*H*T]."""
+    lib = load()
+    B, T, C3 = qkv.shape
+    D = C3 // 3 // H
+    _check(lib.gptk_attention_lse(_ptr(qkv), _ptr(y), _ptr(lse2), B, T, H, D, _stream(stream)), "gptk_attention_lse")
+
+
+def attention_bwd(qkv, y, dy, lse2, dqkv, H: int, stream=None):
+    """dqkv [B, T, 3C] bf16 from qkv, the attention output y, its gradient dy and lse2 of attention_lse."""
+    lib = load()
+    B, T, C3 = qkv.shape
+    D = C3 // 3 // H
+    _check(lib.gptk_attention_bwd(_ptr(qkv), _ptr(y), _ptr(dy), _ptr(lse2), _ptr(dqkv), B, T, H, D,
+                                  _stream(stream)), "gptk_attention_bwd")
 
 
 def layernorm(x, g, b, out, out_f32=None, eps: float = 1e-5, stream=None):

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgpt_gb300.so")
 
 SOURCES = ["k_gemm_tc.cu", "k_attn_tc.cu", "k_rowwise.cu", "k_simt.cu", "k_decode.cu", "tmap.cu", "gpt_api.cu",
-           "gpt_forward.cu", "gptk.cu", "gptk_noalloc.cu", "k_backward.cu", "k_attn_bwd.cu", "k_attn_bwd_tc.cu", "gpt_backward.cu"]
+           "gpt_forward.cu", "gptk.cu", "gptk_noalloc.cu", "k_backward.cu", "k_attn_bwd_tc.cu", "gpt_backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]

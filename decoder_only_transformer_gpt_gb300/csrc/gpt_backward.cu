@@ -64,7 +64,7 @@ struct gpt_train {
   float *dx, *da;
   void *dxb, *dyb, *dqkv, *du;
   float *lse2, *dsum;
-  float* dqacc = nullptr;        // fp32 [M, C] dQ of the attention derivative (zero between calls)
+  float* dqacc = nullptr;        // fp32 [M, C] dQ accumulator of the attention derivative (scratch)
   CUtensorMap T_dy, T_dkv, T_dq; // dy, dqkv and dqacc as the attention derivative's TMA operands
   void* dz;
   // activation maps, for one (B, T)
@@ -173,11 +173,6 @@ int alloc_train(gpt_model* m) {
   Carve real;
   real.base = t->buf;
   layout(real);
-  if (cudaMemset(t->dqacc, 0, Mx * C * 4) != cudaSuccess) {
-    cudaFree(t->buf);
-    delete t;
-    return GPT_ECUDA;
-  }
   // gradient pointers in the order of the weights
   float* p = t->gbuf;
   auto take = [&](size_t n) { float* q = p; p += n; return q; };

@@ -119,6 +119,66 @@ int gptk_attention(const void* qkv, void* y, int32_t B, int32_t T, int32_t H, in
   return GPT_OK;
 }
 
+int gptk_attention_lse(const void* qkv, void* y, float* lse2, int32_t B, int32_t T, int32_t H, int32_t D,
+                       void* stream) {
+  if (!qkv || !y || !lse2 || B < 1 || T < 1 || H < 1 || D < 1) return GPT_EINVAL;
+  if ((D != 32 && D != 64) || !aligned16(qkv) || !aligned16(y)) return GPT_ECONFIG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* err = err_word();
+  if (!err) return GPT_ENOMEM;
+  CUtensorMap tm;
+  if (!make_tmap_qkv(&tm, qkv, B, T, 3 * H * D, D)) {
+    set_detail_text("qkv tensor map");
+    return GPT_ECUDA;
+  }
+  int* sched = nullptr;
+  GPT_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&sched), 2 * sizeof(int), s));
+  cudaError_t e = cudaMemsetAsync(sched, 0, 2 * sizeof(int), s);
+  if (e == cudaSuccess) e = launch_attention_tc(tm, y, B, T, H, D, err, sched, s, lse2);
+  cudaFreeAsync(sched, s);
+  if (e != cudaSuccess) {
+    set_detail("attention", e);
+    return GPT_ECUDA;
+  }
+  return GPT_OK;
+}
+
+int gptk_attention_bwd(const void* qkv, const void* y, const void* dy, const float* lse2, void* dqkv, int32_t B,
+                       int32_t T, int32_t H, int32_t D, void* stream) {
+  if (!qkv || !y || !dy || !lse2 || !dqkv || B < 1 || T < 1 || H < 1 || D < 1) return GPT_EINVAL;
+  if ((D != 32 && D != 64) || !aligned16(qkv) || !aligned16(y) || !aligned16(dy) || !aligned16(dqkv))
+    return GPT_ECONFIG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* err = err_word();
+  if (!err) return GPT_ENOMEM;
+  const int C = H * D;
+  const size_t M = static_cast<size_t>(B) * T;
+  // scratch on the stream: dQ accumulator, Dsum and the work counter (zeroed)
+  const size_t acc_b = M * C * sizeof(float), dsum_b = M * H * sizeof(float), cnt_b = 2 * sizeof(int);
+  uint8_t* ws = nullptr;
+  GPT_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&ws), acc_b + dsum_b + cnt_b, s));
+  float* dqacc = reinterpret_cast<float*>(ws);
+  float* dsum = reinterpret_cast<float*>(ws + acc_b);
+  int* sched = reinterpret_cast<int*>(ws + acc_b + dsum_b);
+  CUtensorMap tq, tdy, tdkv, tdq;
+  cudaError_t e = cudaMemsetAsync(sched, 0, cnt_b, s);
+  if (e == cudaSuccess &&
+      !(make_tmap_qkv(&tq, qkv, B, T, 3 * C, D) && make_tmap_qkv(&tdy, dy, B, T, C, D) &&
+        make_tmap_attn_out(&tdkv, dqkv, B, T, 3 * C, D) && make_tmap_bt_f32(&tdq, dqacc, B, T, C))) {
+    cudaFreeAsync(ws, s);
+    set_detail_text("attention derivative tensor maps");
+    return GPT_ECUDA;
+  }
+  if (e == cudaSuccess)
+    e = launch_attention_bwd_tc(tq, tdy, tdkv, tdq, y, dy, lse2, dsum, dqacc, dqkv, B, T, H, D, err, sched, s);
+  cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) {
+    set_detail("attention derivative", e);
+    return GPT_ECUDA;
+  }
+  return GPT_OK;
+}
+
 int gptk_layernorm(const float* x, const float* g, const float* b, void* out, float* out_f32, int32_t M, int32_t C,
                    float eps, int32_t dtype, void* stream) {
   if (!x || !g || !b || !out || M < 0 || C <= 0 || (C % 8) || C > 2048) return GPT_EINVAL;

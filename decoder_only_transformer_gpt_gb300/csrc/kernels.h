@@ -129,16 +129,13 @@ cudaError_t launch_layernorm_bwd(const float* x, const float* g, const float* dy
 // dE[id[m]] += dx0[m], dP[m % T] += dx0[m].
 cudaError_t launch_embed_bwd(const float* dx0, const int32_t* ids, float* dE, float* dP, int M, int T, int C, int V,
                              cudaStream_t s);
-// Causal attention derivative: dqkv [B*T, 3C] bf16 from qkv [B*T, 3C], the output y and its gradient dy
-// ([B*T, C] bf16); lse2 and dsum ([B*H*T] fp32) receive each query row's base-2 log-sum-exp of the
-// scaled scores and sum of dy * y. D = 32 or 64.
-cudaError_t launch_attention_bwd(const void* qkv, const void* y, const void* dy, void* dqkv, float* lse2, float* dsum,
-                                 int B, int T, int H, int D, cudaStream_t s);
-// The same derivative on tcgen05 from the forward's row log-sum-exp (lse2 [B*H][T], base 2): tm_qkv is the
-// qkv map of make_tmap_qkv (128-row boxes), tm_dy the same over dy [B][T][C], tm_dkv make_tmap_attn_out
-// over dqkv [B][T][3C] (dK and dU are stored there), tm_dq make_tmap_bt_f32 over dqacc [B][T][C] fp32, which
-// must hold zeros and holds zeros again after the call (its dQ goes to dqkv's first third). dsum: fp32
-// [B*H][T] scratch. sched: 2 ints as for launch_attention_tc. D = 32 or 64.
+// Causal attention derivative on tcgen05, from the forward's row log-sum-exp (lse2 [B*H][T], base 2 of the
+// scaled scores): dqkv [B*T, 3C] bf16 from qkv [B*T, 3C], the output y and its gradient dy ([B*T, C] bf16).
+// tm_qkv is the qkv map of make_tmap_qkv (128-row boxes), tm_dy the same over dy [B][T][C], tm_dkv
+// make_tmap_attn_out over dqkv [B][T][3C] (dK and dU are stored there), tm_dq make_tmap_bt_f32 over dqacc
+// [B][T][C] fp32 scratch (cleared by the call; dQ goes to dqkv's first third). dsum: fp32 [B*H][T]
+// scratch. sched: 2 ints as for launch_attention_tc. D = 32 or 64. A memset and three kernels: Dsum, the
+// derivative, dQ to bf16.
 cudaError_t launch_attention_bwd_tc(const CUtensorMap& tm_qkv, const CUtensorMap& tm_dy, const CUtensorMap& tm_dkv,
                                     const CUtensorMap& tm_dq, const void* y, const void* dy, const float* lse2,
                                     float* dsum, float* dqacc, void* dqkv, int B, int T, int H, int D, int* err,

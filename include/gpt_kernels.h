@@ -50,6 +50,25 @@ int gptk_attention(const void* qkv, void* y, int32_t B, int32_t T, int32_t H, in
                    int32_t dtype, void* stream);
 
 /*
+ * gptk_attention on the bf16 path that also writes, for every query row, the base-2
+ * log-sum-exp of its scaled scores: lse2[(b H + h) T + t] = log2 sum_{s <= t} 2^(q_t . k_s log2(e) / sqrt(D))
+ * (fp32, [B*H*T]); the softmax normaliser of "第 25 章" §25.2 that the derivative below reuses.
+ */
+int gptk_attention_lse(const void* qkv, void* y, float* lse2, int32_t B, int32_t T, int32_t H, int32_t D,
+                       void* stream);
+
+/*
+ * Derivative of the causal self-attention of one layer (bf16 path; the chain rule through the
+ * definitions of §25.2, as the training loop of "预训练一个 Mini GPT" needs it): from qkv [B, T, 3C],
+ * the output y [B, T, C] and lse2 of gptk_attention_lse, and dy [B, T, C] (the loss gradient with
+ * respect to y), writes dqkv [B, T, 3C] bf16: dQ, dK and dU in the thirds of qkv's layout. D in {32, 64};
+ * all four bf16 arrays 16-byte aligned. Its fp32 dQ accumulator (B*T*C*4 bytes) and Dsum scratch are
+ * allocated on the stream and freed there after the launches.
+ */
+int gptk_attention_bwd(const void* qkv, const void* y, const void* dy, const float* lse2, void* dqkv, int32_t B,
+                       int32_t T, int32_t H, int32_t D, void* stream);
+
+/*
  * LayerNorm over rows of x [M, C] fp32 ("预训练一个 Mini GPT" 第4步; "GPT-1 学习笔记" §3.2):
  * out (dtype) = (x - mean)/sqrt(var + eps) * g + b; out_f32 (fp32, may alias x, may be NULL)
  * receives the same values in fp32. C must be a multiple of 8 and at most 2048.

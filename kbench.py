@@ -1,13 +1,15 @@
 """Time one step kernel of the library in isolation (CUDA events, warm-up, mean of N).
 
     python kbench.py attention --B 16 --T 1024 --H 12 --D 64
+    python kbench.py attention_bwd --B 16 --T 1024 --H 12 --D 64
     python kbench.py gemm --M 16384 --N 768 --K 768 --epi 2
     python kbench.py head --M 16384 --V 50257 --C 768
     python kbench.py layernorm --M 16384 --C 768
     python kbench.py train --B 16 --T 1024
 
 (`train`: one gpt_backward call, forward + loss + every gradient, of GPT-2 small on
-seeded synthetic tokens.)
+seeded synthetic tokens. `attention_bwd`: one gptk_attention_bwd call, the attention
+derivative's memset and three kernels, after one gptk_attention_lse for its inputs.)
 
 Inputs are random device tensors; the figure printed is algorithmic TFLOP/s
 (or GB/s for the row-wise kernels) over the mean launch time.
@@ -40,7 +42,7 @@ def _time(fn, warmup, iters):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["attention", "gemm", "head", "layernorm", "train"])
+    ap.add_argument("kernel", choices=["attention", "attention_bwd", "gemm", "head", "layernorm", "train"])
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=1024)
     ap.add_argument("--H", type=int, default=12)
@@ -64,6 +66,17 @@ def main():
         ms = _time(lambda: binding.attention(qkv, y, a.H), a.warmup, a.iters)
         flop = 2.0 * C * a.T * (a.T + 1) * a.B
         out = {"kernel": "attention", "shape": [a.B, a.T, a.H, a.D], "ms": ms, "tflops": flop / ms / 1e9}
+    elif a.kernel == "attention_bwd":
+        C = a.H * a.D
+        qkv = torch.randn(a.B, a.T, 3 * C, device=dev).to(torch.bfloat16)
+        dy = (0.25 * torch.randn(a.B, a.T, C, device=dev)).to(torch.bfloat16)
+        y = torch.empty(a.B, a.T, C, device=dev, dtype=torch.bfloat16)
+        lse2 = torch.empty(a.B * a.H * a.T, device=dev)
+        binding.attention_lse(qkv, y, lse2, a.H)
+        dqkv = torch.empty(a.B, a.T, 3 * C, device=dev, dtype=torch.bfloat16)
+        ms = _time(lambda: binding.attention_bwd(qkv, y, dy, lse2, dqkv, a.H), a.warmup, a.iters)
+        flop = 4.0 * C * a.T * (a.T + 1) * a.B         # dP, dU, dK, dQ over the causal half
+        out = {"kernel": "attention_bwd", "shape": [a.B, a.T, a.H, a.D], "ms": ms, "tflops": flop / ms / 1e9}
     elif a.kernel == "gemm":
         A = torch.randn(a.M, a.K, device=dev).to(torch.bfloat16)
         W = (0.05 * torch.randn(a.N, a.K, device=dev)).to(torch.bfloat16)

@@ -100,6 +100,16 @@ def test_backward_ragged_head_width_32(gpt_lib):
     _compare(cfg, w, ids, tg)
 
 
+def test_backward_ragged_multi_tile(gpt_lib):
+    # T = 300: three 128-query tiles, the last with 44 rows (a half tile partly and one wholly past T),
+    # so the attention derivative's key tiles 0..2 all add into query tile 2 and its slabs past T stay empty
+    cfg = GPTConfig(V=199, C=128, H=2, L=1, ctx=320, ffn=512)
+    rng = np.random.Generator(np.random.PCG64(58))
+    w = make_weights(cfg, rng, affine="random", wstd=0.05)
+    ids, tg = make_tokens(cfg.V, 2, 300, rng)
+    _compare(cfg, w, ids, tg)
+
+
 def test_backward_gpt2_width_two_blocks(gpt_lib):
     # GPT-2 small widths and vocabulary (V = 50257: the padded dz rows), two blocks, 2 x 1024 tokens:
     # split-K weight products, stream-K head-table product, attention over 1024 positions
@@ -113,7 +123,12 @@ def test_backward_gpt2_width_two_blocks(gpt_lib):
 
 def test_backward_full_size_properties(gpt_lib):
     # the bench workload (GPT-2 small, B = 16, T = 1024): the loss equals the forward's, every
-    # gradient is finite and a second run agrees to fp32 atomics' reordering
+    # gradient is finite and a second run agrees up to the reordering of fp32 sums. The attention
+    # derivative adds each query tile's dQ from up to 8 key tiles in the order the CTAs finish (a few
+    # 2^-24 relative per element), which flips some bf16 roundings of dqkv; every later bf16 rounding
+    # of a quantity that depends on it (dx, dz, dg, ... through 12 blocks) can flip in turn, so the
+    # gradients of the first layers and the embeddings differ by about 1e-3 of their norm between runs
+    # (the step-level test of the attention derivative bounds the first stage to one bf16 ulp)
     from decoder_only_transformer_gpt_gb300 import binding
     wl = workload("gpt2_small")
     w, ids, tg = generate(wl)
@@ -132,7 +147,7 @@ def test_backward_full_size_properties(gpt_lib):
                           ("fc_b", 3)), g1.values()):
         v2 = m.grad(k, l)
         assert torch.isfinite(v).all() and v.abs().sum() > 0, k
-        assert float((v - v2).norm() / v.norm()) < 1e-3, k
+        assert float((v - v2).norm() / v.norm()) < 3e-3, k
     m.close()
 
 
