@@ -58,18 +58,18 @@ STEP_KINDS = [("embed", 0, False), ("c_attn", 1, True), ("attention", 2, True), 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the same
 # launch configuration, valid only while the kernel's sources hash to the digest recorded with it.
 NCU_TRAFFIC = {
-    "attention": {"bytes": 76.583680e6 + 4.296960e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
+    "attention": {"bytes": 76.483840e6 + 3.919360e6, "profile": "profiles/attention_b16_t1024_h12_d64.md",
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                  "digest": "0af4f6d02833eafb4f4600f81d8d7eeb92bbb9e9"},
-    "head": {"bytes": 102.547968e6 + 17.449984e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+                  "digest": "1458438068a7e65286a8c275768f49580badcdc5"},
+    "head": {"bytes": 102.547712e6 + 17.439744e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "252d74110154ffa50a3e9d33dfcb2ab56b8a0873"},
-    "mlp_proj": {"bytes": 163.266816e6 + 25.031936e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+             "digest": "cec56c43b5b204774fa6ba2985407178ea08ed0d"},
+    "mlp_proj": {"bytes": 164.021504e6 + 24.960256e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                 "digest": "252d74110154ffa50a3e9d33dfcb2ab56b8a0873"},
+                 "digest": "cec56c43b5b204774fa6ba2985407178ea08ed0d"},
 }
 
 # The same for the training step's dominant step at B = 16, T = 1024: the attention derivative (Dsum,
