@@ -268,27 +268,26 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const void* __restrict
 }
 
 // LayerNorm derivative with the row held in registers: C = 32 NPL, lane j-th column lane + 32 j
-// (128-byte coalesced), gain and shift gradients accumulated per lane across the warp's rows and
-// added once per warp (shared memory) and once per block (global). x and dy are read once.
+// (128-byte coalesced). The gain and its per-warp gain and shift gradient partials live in shared memory
+// (each lane owns its columns, so no atomics within a warp), summed over the block's four warps and
+// added once per block (global). Holding them in registers took 168 registers (12 resident warps per
+// SM, latency-bound); this form takes 72 (28 warps). x and dy are read once.
 template <int NPL>
-__global__ void __launch_bounds__(256) layernorm_bwd_reg_kernel(const float* __restrict__ x, const float* __restrict__ g,
+__global__ void __launch_bounds__(128) layernorm_bwd_reg_kernel(const float* __restrict__ x, const float* __restrict__ g,
                                                                 const float* dy, float* dx_io, int add,
                                                                 float* __restrict__ dg, float* __restrict__ db, int M,
                                                                 float eps) {
   pdl_wait();
   pdl_trigger();
   constexpr int C = 32 * NPL;
-  __shared__ float sg[C], sb[C];
-  for (int i = threadIdx.x; i < C; i += blockDim.x) sg[i] = sb[i] = 0.0f;
-  __syncthreads();
+  constexpr int W = 4;
+  __shared__ float sgam[C];
+  __shared__ float wacc[W][2][C];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  for (int i = threadIdx.x; i < C; i += blockDim.x) sgam[i] = g[i];
+  for (int i = lane; i < C; i += 32) { wacc[warp][0][i] = 0.0f; wacc[warp][1][i] = 0.0f; }
+  __syncthreads();
   constexpr float invC = 1.0f / static_cast<float>(C);
-  float gam[NPL], ag[NPL], ab[NPL];
-#pragma unroll
-  for (int j = 0; j < NPL; ++j) {
-    gam[j] = g[lane + 32 * j];
-    ag[j] = ab[j] = 0.0f;
-  }
   for (int row = blockIdx.x * wpb + warp; row < M; row += gridDim.x * wpb) {
     const float* xr = x + static_cast<size_t>(row) * C;
     const float* dr = dy + static_cast<size_t>(row) * C;
@@ -311,30 +310,28 @@ __global__ void __launch_bounds__(256) layernorm_bwd_reg_kernel(const float* __r
     float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
-      xv[j] *= r;                                          // xh
-      const float dxh = dv[j] * gam[j];
+      xv[j] *= r;
+      const float dxh = dv[j] * sgam[lane + 32 * j];
       s1 += dxh;
       s2 += dxh * xv[j];
-      ag[j] += dv[j] * xv[j];
-      ab[j] += dv[j];
+      wacc[warp][0][lane + 32 * j] += dv[j] * xv[j];
+      wacc[warp][1][lane + 32 * j] += dv[j];
     }
     const float m1 = warp_sum(s1) * invC, m2 = warp_sum(s2) * invC;
     float* o = dx_io + static_cast<size_t>(row) * C;
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
-      const float val = r * (dv[j] * gam[j] - m1 - xv[j] * m2);
+      const float val = r * (dv[j] * sgam[lane + 32 * j] - m1 - xv[j] * m2);
       o[lane + 32 * j] = add ? o[lane + 32 * j] + val : val;
     }
   }
-#pragma unroll
-  for (int j = 0; j < NPL; ++j) {
-    atomicAdd(sg + lane + 32 * j, ag[j]);
-    atomicAdd(sb + lane + 32 * j, ab[j]);
-  }
   __syncthreads();
   for (int i = threadIdx.x; i < C; i += blockDim.x) {
-    atomicAdd(dg + i, sg[i]);
-    atomicAdd(db + i, sb[i]);
+    float ag = 0.0f, ab = 0.0f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) { ag += wacc[w][0][i]; ab += wacc[w][1][i]; }
+    atomicAdd(dg + i, ag);
+    atomicAdd(db + i, ab);
   }
 }
 
@@ -436,9 +433,9 @@ cudaError_t launch_colsum(const void* src, int bf16, int rows, int cols, int lds
 cudaError_t launch_layernorm_bwd(const float* x, const float* g, const float* dy, float* dx_io, int add, float* dg,
                                  float* db, int M, int C, float eps, int num_sms, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  int wpb = 4;                                  // 128-thread blocks: several per SM at the kernel's registers
+  int wpb = 4;                                  // 128-thread blocks (the kernel assumes four warps)
   int grid = (M + wpb - 1) / wpb;
-  if (grid > 4 * num_sms) grid = 4 * num_sms;
+  if (grid > 8 * num_sms) grid = 8 * num_sms;
 #define GPT_LNB(NPL)                                                                                          \
   if (C == 32 * NPL)                                                                                          \
     return launch_k(layernorm_bwd_reg_kernel<NPL>, dim3(grid), dim3(wpb * 32), 0, s, x, g, dy, dx_io, add, dg, \
