@@ -57,8 +57,9 @@ __global__ void __launch_bounds__(256) colsum_kernel(const void* __restrict__ sr
   }
 }
 
-// The same for bf16 rows with 16-byte loads: a thread sums 8 consecutive columns (one uint4 per row),
-// a block covers 256 columns over its range of rows with 8 row lanes, then one atomic per column.
+// The same for bf16 rows with 16-byte loads: a thread sums 8 consecutive columns (one uint4 per row, four
+// rows' loads in flight at a time, added in row order), a block covers 256 columns over its range of rows
+// with 8 row lanes, then one atomic per column.
 __global__ void __launch_bounds__(256) colsum8_bf16_kernel(const uint16_t* __restrict__ src, int rows, int cols,
                                                            int lds, float* __restrict__ out) {
   pdl_wait();
@@ -68,17 +69,25 @@ __global__ void __launch_bounds__(256) colsum8_bf16_kernel(const uint16_t* __res
   const int per = (rows + gridDim.y - 1) / gridDim.y;
   const int rb = blockIdx.y * per, re = min(rows, rb + per);
   float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-  if (c0 < cols) {
-    for (int r = rb + threadIdx.y; r < re; r += 8) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * lds + c0);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  auto add8 = [&](const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = unpack_bf16x2(w[k]);
-        acc[2 * k] += f.x;
-        acc[2 * k + 1] += f.y;
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = unpack_bf16x2(w[k]);
+      acc[2 * k] += f.x;
+      acc[2 * k + 1] += f.y;
     }
+  };
+  if (c0 < cols) {
+    int r = rb + threadIdx.y;
+    for (; r + 24 < re; r += 32) {                  // four rows' loads in flight per thread
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(r + 8 * i) * lds + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) add8(v[i]);
+    }
+    for (; r < re; r += 8) add8(*reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * lds + c0));
   }
 #pragma unroll
   for (int k = 0; k < 8; ++k) part[threadIdx.y][threadIdx.x * 8 + k] = acc[k];
