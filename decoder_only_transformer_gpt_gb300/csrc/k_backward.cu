@@ -102,6 +102,57 @@ __global__ void __launch_bounds__(256) colsum8_bf16_kernel(const uint16_t* __res
   }
 }
 
+// dst (bf16) = src (fp32), rows of `cols` values, and colsum[c] += the column sums (the bias gradient of the
+// product that produced src): the shape of colsum8_bf16_kernel, a thread taking 8 consecutive columns of
+// every 8th row of its block's range with four rows' loads in flight, so each warp access covers 1 KB of
+// fp32 and 512 contiguous bytes of bf16. cols % 8 == 0, 16-byte aligned rows.
+__global__ void __launch_bounds__(256) cast_colsum_kernel(const float* __restrict__ src, int rows, int cols,
+                                                          uint16_t* __restrict__ dst, float* __restrict__ colsum) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float part[8][256 + 4];
+  const int c0 = blockIdx.x * 256 + threadIdx.x * 8;
+  const int per = (rows + gridDim.y - 1) / gridDim.y;
+  const int rb = blockIdx.y * per, re = min(rows, rb + per);
+  float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+  auto row8 = [&](int r, const float4 a, const float4 b) {
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * cols + c0) =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  };
+  if (c0 < cols) {
+    int r = rb + threadIdx.y;
+    for (; r + 24 < re; r += 32) {
+      float4 va[4], vb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4* p = reinterpret_cast<const float4*>(src + static_cast<size_t>(r + 8 * i) * cols + c0);
+        va[i] = p[0];
+        vb[i] = p[1];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) row8(r + 8 * i, va[i], vb[i]);
+    }
+    for (; r < re; r += 8) {
+      const float4* p = reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * cols + c0);
+      row8(r, p[0], p[1]);
+    }
+  }
+  if (colsum == nullptr) return;                           // block-uniform
+#pragma unroll
+  for (int k = 0; k < 8; ++k) part[threadIdx.y][threadIdx.x * 8 + k] = acc[k];
+  __syncthreads();
+  const int t = threadIdx.y * 32 + threadIdx.x;
+  const int c = blockIdx.x * 256 + t;
+  if (c < cols) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += part[i][t];
+    atomicAdd(colsum + c, sum);
+  }
+}
+
 // LayerNorm derivative, one warp per row ("预训练一个 Mini GPT" 第4步 defines the forward:
 // xh = (x - mean) r, r = 1 / sqrt(var + eps), y = g xh + b). With dxh = dy g:
 // dx = r (dxh - mean(dxh) - xh mean(dxh xh)); dg = sum over rows of dy xh; db = sum of dy.
@@ -410,6 +461,22 @@ cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int lds, 
 cudaError_t launch_cast_transpose(const float* src, int rows, int cols, void* dst, void* dstT, int ldt, cudaStream_t s,
                                   float* colsum) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (dstT == nullptr && dst != nullptr && cols % 8 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(dst) % 16 == 0) {          // a cast (+ column sums): the streaming kernel
+    static int num_sms = 0;
+    if (num_sms == 0) {
+      int dev = 0;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+    }
+    const int gx = (cols + 255) / 256;
+    int gy = (4 * num_sms + gx - 1) / gx;
+    const int max_gy = (rows + 63) / 64;
+    gy = gy > max_gy ? max_gy : (gy < 1 ? 1 : gy);
+    return launch_k(cast_colsum_kernel, dim3(gx, gy), dim3(32, 8), 0, s, src, rows, cols, static_cast<uint16_t*>(dst),
+                    colsum);
+  }
   const dim3 grid((cols + kT64 - 1) / kT64, (rows + kT64 - 1) / kT64);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   const int vec = (cols % 8 == 0) && (dstT == nullptr || ldt % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
