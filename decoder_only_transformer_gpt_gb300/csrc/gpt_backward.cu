@@ -257,9 +257,32 @@ int ensure_bwd_maps(gpt_model* m, gpt_train* t, int B, int T) {
   return GPT_OK;
 }
 
+// Slices along the token axis for a weight-gradient product of `tiles` output tiles: the count whose
+// (tile, slice) units fill one or two waves of the grid best, the fewest slices among equally full ones
+// (a slice's partial tile costs one reduce-add of the tile), at least 4 K blocks per slice. Dealing
+// about two units per CTA regardless of the wave fill left a third wave of 2 units for the 18-tile
+// attention projection (306 units on 152 CTAs) and 2.4 waves for the 72-tile MLP products.
+int grad_ksplit(int tiles, int KB, int grid) {
+  if (tiles >= grid) return 1;
+  const int ks_max = KB / 4 > 1 ? KB / 4 : 1;
+  int best_ks = 1;
+  double best = -1.0;
+  for (int ks = 1; ks <= ks_max; ++ks) {
+    const long long units = static_cast<long long>(tiles) * ks;
+    if (units > 2LL * grid) break;
+    const long long waves = (units + grid - 1) / grid;
+    const double fill = static_cast<double>(units) / static_cast<double>(waves * grid);
+    if (fill > best + 0.02) {
+      best = fill;
+      best_ks = ks;
+    }
+  }
+  return best_ks;
+}
+
 // A weight-gradient product: out [N0, N1] fp32 += A^T B summed over the M tokens, A [M, N0] and
 // B [M, N1] the activations as stored (MN-major operands, maps with 64-row boxes), split along M
-// so that about two units per CTA are in flight.
+// (grad_ksplit).
 int grad_gemm(gpt_model* m, const CUtensorMap& A, const CUtensorMap& Bm, const CUtensorMap& out_map, float* out,
               int N0, int N1, int M, cudaStream_t s) {
   GemmArgs a{};
@@ -271,9 +294,7 @@ int grad_gemm(gpt_model* m, const CUtensorMap& A, const CUtensorMap& Bm, const C
   a.mn_major = 1;
   const int tiles = ((N0 + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(N1);
   const int KB = (M + kGemmBK - 1) / kGemmBK;
-  int ks = (2 * m->num_sms + tiles - 1) / tiles;
-  if (ks > KB / 4) ks = KB / 4;          // at least 4 K blocks per unit
-  if (ks < 1) ks = 1;
+  const int ks = grad_ksplit(tiles, KB, m->num_sms);
   a.ksplit = ks;
   if (ks == 1) {                          // enough tiles: whole tiles (stream-K where it applies)
     a.sk_part = m->sk_part;
