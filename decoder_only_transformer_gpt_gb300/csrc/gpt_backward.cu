@@ -417,8 +417,7 @@ int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t*
       BW(cu(launch_layernorm(m->x, w.ln1_g, w.ln1_b, q.a2, 1, m->x, M, C, eps, s), "ln1"));
       GPT_CUDA(cudaMemcpyAsync(q.n, m->x, MC4, cudaMemcpyDeviceToDevice, s));
     }
-    BW(gemm_bf16(m, q.A_a2, w.tm_fc_w, q.C_u, M, F, C, w.fc_b, q.u, EPI_BIAS_OUT, s));
-    BW(gemm_bf16(m, q.A_a2, w.tm_fc_w, q.C_g, M, F, C, w.fc_b, q.g, EPI_BIAS_GELU_OUT, s));
+    BW(gemm_bf16_gelu_u(m, q.A_a2, w.tm_fc_w, q.C_g, q.C_u, M, F, C, w.fc_b, q.g, s));   // g and u in one product
     BW(gemm_bf16(m, q.A_g, w.tm_mp_w, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
     if (pre) {
       const float* g = nullptr;

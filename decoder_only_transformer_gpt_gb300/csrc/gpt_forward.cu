@@ -75,7 +75,7 @@ int ensure_act_maps(gpt_model* m, int B, int T) {
 }
 
 int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
-            int K, const float* bias, void* out, int epi, cudaStream_t s) {
+            int K, const float* bias, void* out, int epi, cudaStream_t s, const CUtensorMap* tmC2 = nullptr) {
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K;
   a.bias = bias;
@@ -91,7 +91,7 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
     a.wait_limit = m->dbg_wait_limit;
   }
   a.b_const = 1;                        // every caller's B is a weight (or a transposed copy made earlier)
-  GPT_CUDA(launch_gemm_tc(tmA, tmB, tmC, a, epi, m->num_sms, s));
+  GPT_CUDA(launch_gemm_tc2(tmA, tmB, tmC, tmC2 != nullptr ? *tmC2 : tmC, a, epi, m->num_sms, s));
   return GPT_OK;
 }
 
@@ -413,6 +413,11 @@ int forward_maps(gpt_model* m, int B, int T) { return ensure_act_maps(m, B, T); 
 int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
               int K, const float* bias, void* out, int epi, cudaStream_t s) {
   return tc_gemm(m, tmA, tmB, tmC, M, N, K, bias, out, epi, s);
+}
+
+int gemm_bf16_gelu_u(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tm_g,
+                     const CUtensorMap& tm_u, int M, int N, int K, const float* bias, void* g, cudaStream_t s) {
+  return tc_gemm(m, tmA, tmB, tm_g, M, N, K, bias, g, EPI_BIAS_GELU_UOUT, s, &tm_u);
 }
 
 int shape_ok(const gpt_model* m, int B, int T) { return check_shape(m, B, T); }

@@ -42,7 +42,7 @@ template <int EPI>
 struct Layout {
   static constexpr bool kTmaOut =
       (EPI == EPI_BIAS_OUT || EPI == EPI_BIAS_GELU_OUT || EPI == EPI_BIAS_RESID || EPI == EPI_CE_GRAD ||
-       EPI == EPI_F32_OUT || EPI == EPI_GELU_GRAD);
+       EPI == EPI_F32_OUT || EPI == EPI_GELU_GRAD || EPI == EPI_BIAS_GELU_UOUT);
   static constexpr int STAGES = 4;
   static constexpr int STAGING = STAGES * STAGE_BYTES;
   static constexpr int BIAS = STAGING + (kTmaOut ? EPI_WARPS * EPI_NBUF * EPI_BUF : 0);   // each warp's copy of the tile's bias
@@ -429,7 +429,8 @@ __device__ __forceinline__ SegIter make_seg_iter(bool sk, bool ks, int num_tiles
 template <int EPI, int MODE, bool MN = false>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
+               const GemmArgs args) {
   using LY = Layout<EPI>;
   constexpr int STAGES = LY::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -463,6 +464,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (kTmaOut) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_BIAS_GELU_UOUT) tma_prefetch_desc(&tmC2);
   }
   if (warp == 1) tmem_alloc(&bars->tmem_base, TMEM_COLS);
   tc_fence_before();
@@ -715,26 +717,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int n0 = nb * BN + c * CW;
             if (n0 >= args.N) continue;                  // the whole chunk is past N (warp-uniform)
             uint32_t w[32];
-            if (EPI == EPI_CE_GRAD)
+            // the chunk through the warp's staging box to the map (a TMA store, or the reduce-add into x)
+            auto stage_store = [&](const CUtensorMap* map) {
+              uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
+              ++n_staged;
+              if (lane == 0) bulk_wait_read<EPI_NBUF - 1>();   // the store that last used this box has read it
+              __syncwarp();
+              stage_row(buf, lane, w);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (EPI == EPI_BIAS_RESID) tma_reduce_add_2d(map, buf, n0, m0);   // x += tile, in L2
+                else tma_store_2d(map, buf, n0, m0);
+                bulk_commit();
+              }
+            };
+            if (EPI == EPI_CE_GRAD) {
               ce_grad_chunk(r + h * CW, row_lse, row_tgt - n0, args.scale, w);
-            else if (EPI == EPI_GELU_GRAD)
+            } else if (EPI == EPI_GELU_GRAD) {
               gelu_grad_chunk(r + h * CW,
                               static_cast<const __nv_bfloat16*>(args.aux) + static_cast<size_t>(row_ok ? grow : 0) * args.N + n0,
                               row_ok ? args.N - n0 : 0, args.gelu_erf, w);
-            else
+            } else if (EPI == EPI_BIAS_GELU_UOUT) {          // u = acc + bias first, then gelu(u)
+              finish_chunk<EPI_BIAS_OUT, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
+              stage_store(&tmC2);
+              finish_chunk<EPI_BIAS_GELU_OUT, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
+            } else {
               finish_chunk<EPI, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
-            uint8_t* buf = my_stage + (n_staged % EPI_NBUF) * EPI_BUF;
-            ++n_staged;
-            if (lane == 0) bulk_wait_read<EPI_NBUF - 1>();   // the store that last used this box has read it
-            __syncwarp();
-            stage_row(buf, lane, w);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              if (EPI == EPI_BIAS_RESID) tma_reduce_add_2d(&tmC, buf, n0, m0);   // x += tile, in L2
-              else tma_store_2d(&tmC, buf, n0, m0);
-              bulk_commit();
             }
+            stage_store(&tmC);
           }
         }
       } else {
@@ -771,8 +782,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 template <int EPI, int MODE, bool MN = false>
-cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmC2,
+                        const GemmArgs& a, int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, MODE, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -780,12 +791,13 @@ cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(gemm_tc_kernel<EPI, MODE, MN>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, a);
+  return launch_k(gemm_tc_kernel<EPI, MODE, MN>, dim3(grid), dim3(THREADS), Layout<EPI>::SMEM, s, tmA, tmB, tmC, tmC2,
+                  a);
 }
 
 template <int EPI>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
-                       int grid_limit, cudaStream_t s) {
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmC2,
+                       const GemmArgs& a, int grid_limit, cudaStream_t s) {
   const int MB = (a.M + BM - 1) / BM;
   const int NB = (a.N + BN - 1) / BN;
   const int tiles = MB * NB;
@@ -799,11 +811,11 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
         if (a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;
         const long long units = static_cast<long long>(tiles) * a.ksplit;
         const int g2 = units < grid_limit ? static_cast<int>(units) : grid_limit;
-        return launch_inst<EPI, 2, true>(tmA, tmB, tmC, a, g2, s);
+        return launch_inst<EPI, 2, true>(tmA, tmB, tmC, tmC2, a, g2, s);
       }
       if (a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
-        return launch_inst<EPI, 1, true>(tmA, tmB, tmC, a, grid, s);
-      return launch_inst<EPI, 0, true>(tmA, tmB, tmC, a, grid, s);
+        return launch_inst<EPI, 1, true>(tmA, tmB, tmC, tmC2, a, grid, s);
+      return launch_inst<EPI, 0, true>(tmA, tmB, tmC, tmC2, a, grid, s);
     } else {
       return cudaErrorInvalidValue;
     }
@@ -813,16 +825,16 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
       if (a.bias != nullptr || a.ksplit > (a.K + BK - 1) / BK) return cudaErrorInvalidValue;
       const long long units = static_cast<long long>(tiles) * a.ksplit;
       const int g2 = units < grid_limit ? static_cast<int>(units) : grid_limit;
-      return launch_inst<EPI, 2>(tmA, tmB, tmC, a, g2, s);
+      return launch_inst<EPI, 2>(tmA, tmB, tmC, tmC2, a, g2, s);
     } else {
       return cudaErrorInvalidValue;
     }
   }
   if constexpr (kSplit) {
     if (a.sk_part != nullptr && a.sk_flag != nullptr && gemm_tc_stream_k(a.M, a.N, a.K, EPI, grid_limit))
-      return launch_inst<EPI, 1>(tmA, tmB, tmC, a, grid, s);
+      return launch_inst<EPI, 1>(tmA, tmB, tmC, tmC2, a, grid, s);
   }
-  return launch_inst<EPI, 0>(tmA, tmB, tmC, a, grid, s);
+  return launch_inst<EPI, 0>(tmA, tmB, tmC, tmC2, a, grid, s);
 }
 
 }  // namespace
@@ -843,19 +855,26 @@ size_t gemm_sk_part_floats(int grid) { return static_cast<size_t>(grid + 1) * BM
 size_t gemm_sk_flag_ints(int grid) { return static_cast<size_t>(grid + 1) * 4; }
 int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
 
-cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
-                           int epi, int grid_limit, cudaStream_t s) {
+cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                            const CUtensorMap& tmC2, const GemmArgs& a, int epi, int grid_limit, cudaStream_t s) {
   switch (epi) {
-    case EPI_BIAS_OUT: return launch_one<EPI_BIAS_OUT>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_BIAS_GELU_OUT: return launch_one<EPI_BIAS_GELU_OUT>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_BIAS_RESID: return launch_one<EPI_BIAS_RESID>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_CE_GRAD: return launch_one<EPI_CE_GRAD>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_F32_OUT: return launch_one<EPI_F32_OUT>(tmA, tmB, tmC, a, grid_limit, s);
-    case EPI_GELU_GRAD: return launch_one<EPI_GELU_GRAD>(tmA, tmB, tmC, a, grid_limit, s);
+    case EPI_BIAS_OUT: return launch_one<EPI_BIAS_OUT>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_BIAS_GELU_OUT: return launch_one<EPI_BIAS_GELU_OUT>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_BIAS_RESID: return launch_one<EPI_BIAS_RESID>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_F32: return launch_one<EPI_F32>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_CE: return launch_one<EPI_CE>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_CE_GRAD: return launch_one<EPI_CE_GRAD>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_F32_OUT: return launch_one<EPI_F32_OUT>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_GELU_GRAD: return launch_one<EPI_GELU_GRAD>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
+    case EPI_BIAS_GELU_UOUT: return launch_one<EPI_BIAS_GELU_UOUT>(tmA, tmB, tmC, tmC2, a, grid_limit, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                           int epi, int grid_limit, cudaStream_t s) {
+  if (epi == EPI_BIAS_GELU_UOUT) return cudaErrorInvalidValue;   // needs the second map
+  return launch_gemm_tc2(tmA, tmB, tmC, tmC, a, epi, grid_limit, s);
 }
 
 }  // namespace gptgb

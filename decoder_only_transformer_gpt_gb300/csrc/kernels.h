@@ -25,6 +25,7 @@ enum Epilogue : int {
   EPI_CE_GRAD = 5,        // out bf16 = (exp(z - lse) - [col == target]) * scale, lse = nll + ztgt per row
   EPI_F32_OUT = 6,        // out fp32 = acc (+ bias) through the TMA store (fp32 [M,N] box 32x32)
   EPI_GELU_GRAD = 7,      // out bf16 = acc * gelu'(u), u = aux bf16 [M, N] (the GELU's input)
+  EPI_BIAS_GELU_UOUT = 8, // out bf16 = gelu(acc + bias) through tmC and u = acc + bias (bf16) through tmC2
 };
 
 struct GemmArgs {
@@ -77,6 +78,9 @@ int gemm_tc_num_ntiles(int N);
 constexpr int kEpiRows = 32;
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const GemmArgs& a, int epi, int grid_limit, cudaStream_t s);
+// The same with a second output map (EPI_BIAS_GELU_UOUT: tmC2 receives the GELU's input).
+cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                            const CUtensorMap& tmC2, const GemmArgs& a, int epi, int grid_limit, cudaStream_t s);
 
 constexpr int kAttnBQ = 128;
 // sched: 2 device ints, zero before the launch; the kernel's CTAs take work items from it and the

@@ -94,6 +94,9 @@ void free_train(gpt_model* m);     // releases m->tr (gpt_backward.cu)
 int forward_maps(gpt_model* m, int B, int T);
 int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
               int K, const float* bias, void* out, int epi, cudaStream_t s);
+// c_fc of the training forward: g = gelu(a W^T + b) through tm_g and the GELU's input u through tm_u.
+int gemm_bf16_gelu_u(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tm_g,
+                     const CUtensorMap& tm_u, int M, int N, int K, const float* bias, void* g, cudaStream_t s);
 int shape_ok(const gpt_model* m, int B, int T);
 // thread-local text of the last failing CUDA call
 void set_detail(const char* what, cudaError_t e);
