@@ -335,22 +335,37 @@ __device__ __forceinline__ void gelu_grad_chunk(const uint32_t* r, const __nv_bf
     }
   }
   constexpr float c0 = 0.7978845608028654f;
+  if (erf_form) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float2 x = unpack_bf16x2(uw[i]);
+      float d[2];
+      const float xs[2] = {x.x, x.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float xv = xs[e];
+        d[e] = 0.5f * (1.0f + erff(xv * 0.70710678118654752f)) + xv * 0.39894228040143268f * __expf(-0.5f * xv * xv);
+      }
+      w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * d[0], __uint_as_float(r[2 * i + 1]) * d[1]);
+    }
+    return;
+  }
+  // tanh form, on element pairs with the packed f32x2 instructions:
+  // gelu'(x) = (1 + t) / 2 + (x / 2) (1 - t^2) c0 (1 + 3 * 0.044715 x^2), t = tanh(c0 x (1 + 0.044715 x^2))
+  const float2 one = make_float2(1.0f, 1.0f), half = make_float2(0.5f, 0.5f), mone = make_float2(-1.0f, -1.0f);
+  const float2 k1 = make_float2(0.044715f, 0.044715f), k3 = make_float2(3.0f * 0.044715f, 3.0f * 0.044715f);
+  const float2 c0v = make_float2(c0, c0), hc0 = make_float2(0.5f * c0, 0.5f * c0);
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const float2 x = unpack_bf16x2(uw[i]);
-    float d[2];
-    const float xs[2] = {x.x, x.y};
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float xv = xs[e];
-      if (erf_form) {
-        d[e] = 0.5f * (1.0f + erff(xv * 0.70710678118654752f)) + xv * 0.39894228040143268f * __expf(-0.5f * xv * xv);
-      } else {
-        const float t = tanh_approx(c0 * xv * fmaf(0.044715f, xv * xv, 1.0f));
-        d[e] = 0.5f * (1.0f + t) + 0.5f * xv * (1.0f - t * t) * c0 * fmaf(3.0f * 0.044715f, xv * xv, 1.0f);
-      }
-    }
-    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * d[0], __uint_as_float(r[2 * i + 1]) * d[1]);
+    const float2 x2 = mul2_rn(x, x);
+    const float2 arg = mul2_rn(mul2_rn(x, c0v), fma2_rn(x2, k1, one));
+    const float2 t = make_float2(tanh_approx(arg.x), tanh_approx(arg.y));
+    const float2 omt2 = fma2_rn(mul2_rn(t, mone), t, one);                       // 1 - t^2
+    const float2 b = mul2_rn(mul2_rn(x, hc0), mul2_rn(omt2, fma2_rn(x2, k3, one)));
+    const float2 d = add2_rn(fma2_rn(t, half, half), b);
+    const float2 o = mul2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), d);
+    w[i] = pack_bf16x2(o.x, o.y);
   }
 }
 
