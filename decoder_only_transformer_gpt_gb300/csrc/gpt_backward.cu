@@ -280,6 +280,27 @@ int grad_ksplit(int tiles, int KB, int grid) {
   return best_ks;
 }
 
+// Slices along K for a long product added into an fp32 output zeroed before it (dh = dz E, K = V): the
+// count, at most 8 and at least 48 K blocks per slice, whose (tile, slice) units fill the waves best, the
+// fewest among equally full ones. Dealt tile by tile, the units of one wave hold the three N tiles of the
+// same rows at the same K slice, so each A slice comes from DRAM once and is reused from L2; stream-K's
+// contiguous ranges put those three tiles at different K offsets, and with K = V the A rows in use
+// (12.9 MB per 128-row block) do not stay in L2 between them.
+int long_k_split(int tiles, int KB, int grid) {
+  int best_ks = 1;
+  double best = -1.0;
+  for (int ks = 1; ks <= 8 && KB / ks >= 48; ++ks) {
+    const long long units = static_cast<long long>(tiles) * ks;
+    const long long waves = (units + grid - 1) / grid;
+    const double fill = static_cast<double>(units) / static_cast<double>(waves * grid);
+    if (fill > best + 0.02) {
+      best = fill;
+      best_ks = ks;
+    }
+  }
+  return best_ks;
+}
+
 // A weight-gradient product: out [N0, N1] fp32 += A^T B summed over the M tokens, A [M, N0] and
 // B [M, N1] the activations as stored (MN-major operands, maps with 64-row boxes), split along M
 // (grad_ksplit).
@@ -371,7 +392,21 @@ int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStre
     BWS(GPT_STEP_B_DE, -1, grad_gemm(m, t->K_dz, t->K_h, t->tg_wte, t->g_wte, V, C, M, s));
   // dh = dz E (fp32 into da)
   GPT_CUDA(cudaMemsetAsync(t->da, 0, static_cast<size_t>(M) * C * sizeof(float), s));
-  BWS(GPT_STEP_B_DH, -1, gemm_bf16(m, t->A_dz, t->tb_wteT, t->C_da, M, C, V, nullptr, t->da, EPI_BIAS_RESID, s));
+  {
+    GemmArgs a{};
+    a.M = M; a.N = C; a.K = V;
+    a.out = t->da;
+    a.ldo = C;
+    a.err = m->err;
+    a.b_const = 1;
+    const int tiles = ((M + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(C);
+    a.ksplit = long_k_split(tiles, (V + kGemmBK - 1) / kGemmBK, m->num_sms);
+    if (a.ksplit == 1) {
+      a.sk_part = m->sk_part;
+      a.sk_flag = m->sk_flag;
+    }
+    BWS(GPT_STEP_B_DH, -1, cu(launch_gemm_tc(t->A_dz, t->tb_wteT, t->C_da, a, EPI_BIAS_RESID, m->num_sms, s), "dh"));
+  }
   if (c.final_ln) {
     BW(cu(launch_layernorm_bwd(m->x, m->lnf_g, t->da, t->dx, 0, t->g_lnf_g, t->g_lnf_b, M, C, c.ln_eps, m->num_sms, s),
           "ln_f backward"));

@@ -65,6 +65,11 @@ struct __align__(8) Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
+// Fetch the 128-byte line holding p into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 __device__ __forceinline__ void tile_coords(int tile, int MB, int NB, int m_fastest, int& mb, int& nb) {
   if (m_fastest) { mb = tile % MB; nb = tile / MB; }
   else           { nb = tile % NB; mb = tile / NB; }
@@ -620,6 +625,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < BN / 32; ++i)
           my_bias[lane * (BN / 32) + i] = (nbase + i < args.N) ? __ldg(args.bias + nbase + i) : 0.0f;
         __syncwarp();
+      }
+      if (EPI == EPI_GELU_GRAD && mb * BM + row < args.M) {
+        // this row's GELU inputs for the tile into L2 while the tile's main loop runs: the chunks
+        // below then wait on L2, not on DRAM, for them
+        const __nv_bfloat16* urow = static_cast<const __nv_bfloat16*>(args.aux) + static_cast<size_t>(mb * BM + row) * args.N;
+#pragma unroll
+        for (int q = 0; q < BN / 64; ++q)
+          if (nb * BN + q * 64 < args.N) prefetch_l2(urow + nb * BN + q * 64);
       }
       if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, args.err)) break;
       tc_fence_after();
