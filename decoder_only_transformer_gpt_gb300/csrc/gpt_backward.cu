@@ -453,7 +453,7 @@ int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t*
       GPT_CUDA(cudaMemcpyAsync(q.n, m->x, MC4, cudaMemcpyDeviceToDevice, s));
     }
     BW(gemm_bf16_gelu_u(m, q.A_a2, w.tm_fc_w, q.C_g, q.C_u, M, F, C, w.fc_b, q.g, s));   // g and u in one product
-    BW(gemm_bf16(m, q.A_g, w.tm_mp_w, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
+    BW(gemm_bf16_resid(m, q.A_g, w.tm_mp_w, w.tm_mp_w_pair, m->tm_x_out, M, C, F, w.mp_b, m->x, s));
     if (pre) {
       const float* g = nullptr;
       const float* b = nullptr;

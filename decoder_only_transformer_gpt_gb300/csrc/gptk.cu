@@ -91,6 +91,52 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
   return GPT_OK;
 }
 
+int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
+                   int32_t ksplit, void* stream) {
+  if (!A || !W || !out || M < 0 || N <= 0 || K <= 0) return GPT_EINVAL;
+  if ((K % 8) || (N % 8) || !aligned16(A) || !aligned16(W) || !aligned16(out)) return GPT_EINVAL;
+  if (ksplit > 1 && (bias != nullptr || ksplit > (K + kGemmBK - 1) / kGemmBK)) return GPT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) return GPT_OK;
+  if (gemm_pair_capacity() <= 0) return GPT_ECONFIG;
+  int* err = err_word();
+  if (!err) return GPT_ENOMEM;
+  CUtensorMap tmA, tmB, tmC;
+  if (!make_tmap_2d_bf16(&tmA, A, M, K, kGemmBM) || !make_tmap_2d_bf16(&tmB, W, N, K, kGemmBM) ||
+      !make_tmap_2d(&tmC, out, 4, M, N, 32, kEpiRows)) {
+    set_detail_text("gemm tensor map");
+    return GPT_ECUDA;
+  }
+  GemmArgs a{};
+  a.M = M; a.N = N; a.K = K;
+  a.bias = bias; a.out = out; a.ldo = N;
+  a.err = err;
+  a.m_fastest = N > M ? 1 : 0;
+  a.ksplit = ksplit > 1 ? ksplit : 0;
+  const int grid = num_sms();
+  uint8_t* skws = nullptr;                 // stream-K partial tiles + flags, on the stream
+  if (ksplit <= 1) {
+    const size_t pbytes = gemm_sk_part_floats(grid) * sizeof(float);
+    const size_t fbytes = gemm_sk_flag_ints(grid) * sizeof(int);
+    GPT_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&skws), pbytes + fbytes, s));
+    a.sk_part = reinterpret_cast<float*>(skws);
+    a.sk_flag = reinterpret_cast<int*>(skws + pbytes);
+    const cudaError_t e = cudaMemsetAsync(a.sk_flag, 0, fbytes, s);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(skws, s);
+      set_detail("cudaMemsetAsync", e);
+      return GPT_ECUDA;
+    }
+  }
+  const cudaError_t e = launch_gemm_pair(tmA, tmB, tmC, a, grid / 2, s);
+  if (skws) cudaFreeAsync(skws, s);
+  if (e != cudaSuccess) {
+    set_detail("launch_gemm_pair", e);
+    return GPT_ECUDA;
+  }
+  return GPT_OK;
+}
+
 int gptk_attention(const void* qkv, void* y, int32_t B, int32_t T, int32_t H, int32_t D, int32_t dtype,
                    void* stream) {
   if (!qkv || !y || B < 1 || T < 1 || H < 1 || D < 1) return GPT_EINVAL;

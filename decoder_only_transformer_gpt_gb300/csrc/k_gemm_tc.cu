@@ -420,19 +420,23 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ SegIter make_seg_iter(bool sk, bool ks, int num_tiles, int KB, int ksplit) {
-  const int G = gridDim.x;
+// The work of worker `idx` of G (a CTA, or a CTA pair).
+__device__ __forceinline__ SegIter make_seg_iter_of(bool sk, bool ks, int num_tiles, int KB, int ksplit, int G, int idx) {
   const int S = !sk ? 0 : (num_tiles >= 2 * G ? G + num_tiles % G : num_tiles);
   SegIter it;
   it.KB = KB;
   const long long units = static_cast<long long>(S) * KB;
-  it.k = units * blockIdx.x / G;
-  it.kend = units * (blockIdx.x + 1) / G;
-  it.t = S + blockIdx.x;
+  it.k = units * idx / G;
+  it.kend = units * (idx + 1) / G;
+  it.t = S + idx;
   it.stride = G;
   it.ksplit = (ks && ksplit > 1) ? ksplit : 1;
   it.count = num_tiles * it.ksplit;
   return it;
+}
+
+__device__ __forceinline__ SegIter make_seg_iter(bool sk, bool ks, int num_tiles, int KB, int ksplit) {
+  return make_seg_iter_of(sk, ks, num_tiles, KB, ksplit, gridDim.x, blockIdx.x);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -809,6 +813,403 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel (cta_group::2)
+
+// The residual product (EPI_BIAS_RESID: x += A W^T + bias) on a pair of CTAs in a cluster of two:
+// one tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), issued by the even CTA, reads the pair's
+// 256 A rows from both CTAs' shared memory (128 each) and the 256 W rows likewise (128 each), and
+// leaves rows 0-127 of the 256 x 256 accumulator in the even CTA's TMEM and rows 128-255 in the odd
+// one's. Each CTA therefore stages 32 KB per K block instead of 48 KB (A 16 KB and half of W), and
+// the same shared memory holds a six-stage ring (2 us of MMA work at the measured peak) instead of
+// four. Each CTA's TMA copies land in its own shared memory and count towards the even CTA's "full"
+// barrier; the even CTA's commits arrive on both CTAs' barriers at once (multicast). Warp roles as
+// in gemm_tc_kernel; the odd CTA's warp 1 only allocates and frees TMEM.
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * BK * 2;            // this CTA's 128 of the pair's 256 A rows
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;      // this CTA's 128 of the tile's 256 W rows
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+struct PairLayout {
+  static constexpr int STAGING = P_STAGES * P_STAGE_BYTES;
+  static constexpr int BIAS = STAGING + EPI_WARPS * EPI_BUF;
+  static constexpr int BAR = BIAS + EPI_WARPS * BN * 4;
+  static constexpr int SMEM = BAR + 256 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct __align__(8) PairBars {
+  uint64_t full[P_STAGES];    // even CTA: both CTAs' copies of the stage have landed (2 x 32 KB)
+  uint64_t empty[P_STAGES];   // each CTA: the pair's MMAs have read its copy of the stage
+  uint64_t tfull[2];          // each CTA: its half of the accumulator is complete
+  uint64_t tempty[2];         // even CTA: both CTAs' epilogue warps (8) have read the accumulator
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(PairBars) <= 256, "barrier block");
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the variable at shared::cta address `saddr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+
+// Every thread of both CTAs: release this CTA's earlier writes, wait for the other CTA's.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+
+// A tiled copy into this CTA's shared memory whose bytes count towards a barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t cluster_bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// TMEM allocation for the pair: one warp of each CTA executes it (the whole warp).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// The pair's MMA, issued by one elected lane of the even CTA's converged warp.
+__device__ __forceinline__ void tc_mma_pair_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// One arrival on the barrier at this shared-memory offset in both CTAs once the pair's earlier MMAs
+// have completed.
+__device__ __forceinline__ void tc_commit_pair_both_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}\n"
+      :: "r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3)) : "memory");
+}
+
+// The same on this CTA's barrier only.
+__device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n"
+      :: "r"(smem_u32(bar)) : "memory");
+}
+
+// MODE as gemm_tc_kernel (0 whole tiles, 1 stream-K, 2 split-K), over pair tiles of 256 x 256 and
+// pairs of CTAs: pair p = blockIdx.x / 2 takes the work gemm_tc_kernel gives CTA p of gridDim.x / 2.
+// A stream-K partial is handed between the CTAs of equal rank in neighbouring pairs (slot blockIdx.x,
+// taken from slot blockIdx.x + 2).
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;   // the same in both CTAs
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * P_A_BYTES;
+  uint8_t* sE = smem + PairLayout::STAGING;
+  float* sBias = reinterpret_cast<float*>(smem + PairLayout::BIAS);
+  PairBars* bars = reinterpret_cast<PairBars*>(smem + PairLayout::BAR);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+  const int MB = (args.M + 2 * BM - 1) / (2 * BM);
+  const int NB = (args.N + BN - 1) / BN;
+  const int KB = (args.K + BK - 1) / BK;
+  const int num_tiles = MB * NB;
+  constexpr bool SK = MODE == 1, KS = MODE == 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) { mbar_init(&bars->full[s], 1); mbar_init(&bars->empty[s], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bars->tfull[i], 1); mbar_init(&bars->tempty[i], 2 * EPI_WARPS); }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  cluster_sync_all();               // the other CTA runs, and both CTAs' barriers exist before anything crosses over
+  if (warp == 1) tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);   // with the other CTA's warp 1
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (each CTA its own halves)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_par = 0;
+      bool ok = true;
+      auto load_a = [&](int st, int kb, int mb) {
+        tma_load_2d_pair(sA + st * P_A_BYTES, &tmA, cluster_addr(smem_u32(&bars->full[st]), 0), kb * BK,
+                         mb * 2 * BM + static_cast<int>(rank) * BM);
+      };
+      auto load_b = [&](int st, int kb, int nb) {
+        tma_load_2d_pair(sB + st * P_B_BYTES, &tmB, cluster_addr(smem_u32(&bars->full[st]), 0), kb * BK,
+                         nb * BN + static_cast<int>(rank) * (BN / 2));
+      };
+      int pre = 0;
+      SegIter it = make_seg_iter_of(SK, KS, num_tiles, KB, args.ksplit, npairs, pair);
+      if (args.b_const) {
+        SegIter it0 = it;
+        int tile0, kb00, kb10;
+        if (it0.template next<KS>(tile0, kb00, kb10)) {
+          int mb0, nb0;
+          tile_coords(tile0, MB, NB, args.m_fastest, mb0, nb0);
+          pre = (kb10 - kb00) < P_STAGES ? (kb10 - kb00) : P_STAGES;
+          for (int i = 0; i < pre; ++i) {
+            if (leader) mbar_arrive_expect_tx(&bars->full[i], 2 * P_STAGE_BYTES);
+            load_b(i, kb00 + i, nb0);
+          }
+        }
+      }
+      pdl_wait();
+      int tile, kb0, kb1;
+      while (ok && it.template next<KS>(tile, kb0, kb1)) {
+        int mb, nb;
+        tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (pre > 0) {
+            --pre;
+            load_a(stage, kb, mb);
+          } else {
+            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+            if (leader) mbar_arrive_expect_tx(&bars->full[stage], 2 * P_STAGE_BYTES);
+            load_a(stage, kb, mb);
+            load_b(stage, kb, nb);
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // the copies this CTA issued have landed once the pair's MMAs have read them (or the wait ran out)
+      for (int s = 0; s < P_STAGES; ++s)
+        if (issued & (1u << s)) mbar_wait_drain(&bars->empty[s], (last_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (even CTA; whole warp, one elected lane issues)
+    if (leader) {
+      const uint32_t idesc = idesc_bf16_f32(2 * BM, BN, false);
+      const uint64_t da0 = smem_desc(smem_u32(sA), 16, 1024, SWZ_128B);
+      const uint64_t db0 = smem_desc(smem_u32(sB), 16, 1024, SWZ_128B);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      SegIter it = make_seg_iter_of(SK, KS, num_tiles, KB, args.ksplit, npairs, pair);
+      int tile, kb0, kb1;
+      while (ok && it.template next<KS>(tile, kb0, kb1)) {
+        if (!mbar_wait_warp(&bars->tempty[acc], acc_phase ^ 1u, abort_flag, args.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_warp(&bars->full[stage], phase, abort_flag, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = da0 + static_cast<uint64_t>((stage * P_A_BYTES) >> 4);
+          const uint64_t db = db0 + static_cast<uint64_t>((stage * P_B_BYTES) >> 4);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_pair_warp(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+          tc_commit_pair_both_warp(&bars->empty[stage]);
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_both_warp(&bars->tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      tc_commit_pair_warp(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps (each CTA its 128 rows)
+    const int sub = warp & 3;
+    const int row = sub * 32 + lane;
+    uint8_t* my_stage = sE + sub * EPI_BUF;
+    float* my_bias = sBias + sub * BN;
+    pdl_wait();
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    SegIter it = make_seg_iter_of(SK, KS, num_tiles, KB, args.ksplit, npairs, pair);
+    int tile, kb0, kb1;
+    while (it.template next<KS>(tile, kb0, kb1)) {
+      int mb, nb;
+      tile_coords(tile, MB, NB, args.m_fastest, mb, nb);
+      const bool writer = kb0 > 0;
+      const bool owner = kb0 == 0 && kb1 < KB;
+      if (args.bias != nullptr && !writer) {
+        const int nbase = nb * BN + lane * (BN / 32);
+#pragma unroll
+        for (int i = 0; i < BN / 32; ++i)
+          my_bias[lane * (BN / 32) + i] = (nbase + i < args.N) ? __ldg(args.bias + nbase + i) : 0.0f;
+        __syncwarp();
+      }
+      if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, args.err)) break;
+      tc_fence_after();
+      const int m0 = mb * 2 * BM + static_cast<int>(rank) * BM + sub * 32;   // this warp's first output row
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      // the accumulator is read: one arrival of this warp on the even CTA's barrier
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(cluster_addr(smem_u32(&bars->tempty[acc]), 0));
+      };
+      if (SK && writer) {
+        float4* pw = reinterpret_cast<float4*>(args.sk_part) + ((size_t)blockIdx.x * 4 + sub) * (BN / 64) * 16 * 32 + lane;
+#pragma unroll 1
+        for (int c2 = 0; c2 < BN / 64; ++c2) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x64(tbase + c2 * 64, r);
+          tmem_ld_wait();
+          if (c2 == BN / 64 - 1) release_acc();
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            pw[(c2 * 16 + q) * 32] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(args.sk_flag + blockIdx.x * 4 + sub, 1);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
+      const float4* ppart = nullptr;
+      if (SK && owner) {
+        const int fi = (blockIdx.x + 2) * 4 + sub;
+        int* flag = args.sk_wait_flag != nullptr ? const_cast<int*>(args.sk_wait_flag) + fi : args.sk_flag + fi;
+        const long long limit = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
+        bool seen = ld_acquire_gpu(flag) != 0;
+        if (!seen) {
+          const long long t0 = clock64();
+          while (!(seen = (ld_acquire_gpu(flag) != 0))) {
+            if (*abort_flag || clock64() - t0 > limit) break;
+          }
+        }
+        if (!__all_sync(0xffffffffu, seen)) {
+          if (lane == 0) { record_error(args.err, GPT_DEV_ETIMEOUT); *abort_flag = 1; }
+        } else if (lane == 0) {
+          *flag = 0;
+        }
+        ppart = reinterpret_cast<const float4*>(args.sk_part) + ((size_t)(blockIdx.x + 2) * 4 + sub) * (BN / 64) * 16 * 32 + lane;
+      }
+#pragma unroll 1
+      for (int c2 = 0; c2 < BN / 64; ++c2) {
+        uint32_t r[64];
+        tmem_ld_32x32b_x64(tbase + c2 * 64, r);
+        tmem_ld_wait();
+        if (c2 == BN / 64 - 1) release_acc();
+        if (SK && ppart != nullptr) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float4 p4 = ppart[(c2 * 16 + q) * 32];
+            r[4 * q + 0] = __float_as_uint(__uint_as_float(r[4 * q + 0]) + p4.x);
+            r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + p4.y);
+            r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + p4.z);
+            r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + p4.w);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = c2 * 2 + h;                    // 32-column chunk within the tile
+          const int n0 = nb * BN + c * 32;
+          if (n0 >= args.N) continue;
+          uint32_t w[32];
+          finish_chunk<EPI_BIAS_RESID, 32>(args, r + h * 32, args.bias != nullptr ? my_bias + c * 32 : nullptr, w);
+          if (lane == 0) bulk_wait_read<0>();          // the previous reduce-add has read the box
+          __syncwarp();
+          stage_row(my_stage, lane, w);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tmC, my_stage, n0, m0);
+            bulk_commit();
+          }
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  // Neither CTA leaves while the pair's MMAs, copies or arrivals may still touch it, and the TMEM is
+  // freed by both CTAs' warps 1 together while both are still running.
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+  cluster_sync_all();
+}
+
+template <int MODE>
+cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                             int pairs, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               PairLayout::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = PairLayout::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MODE>, tmA, tmB, tmC, a);
+}
+
 template <int EPI, int MODE, bool MN = false>
 cudaError_t launch_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmC2,
                         const GemmArgs& a, int grid, cudaStream_t s) {
@@ -879,8 +1280,55 @@ bool gemm_tc_stream_k(int M, int N, int K, int epi, int grid_limit) {
   const int KB = (K + BK - 1) / BK;
   return KB >= kSplitMinKB && grid_limit > 0 && tiles > grid_limit && tiles % grid_limit != 0;
 }
-size_t gemm_sk_part_floats(int grid) { return static_cast<size_t>(grid + 1) * BM * BN; }
-size_t gemm_sk_flag_ints(int grid) { return static_cast<size_t>(grid + 1) * 4; }
+// Slots 0 .. grid + 1: a CTA pair's partial goes from slot blockIdx.x + 2 to blockIdx.x.
+size_t gemm_sk_part_floats(int grid) { return static_cast<size_t>(grid + 2) * BM * BN; }
+size_t gemm_sk_flag_ints(int grid) { return static_cast<size_t>(grid + 2) * 4; }
+
+int gemm_pair_capacity() {
+  static int cap = -1;
+  if (cap < 0) {
+    int n = 0;
+    if (cudaFuncSetAttribute(gemm_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::SMEM) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(THREADS);
+      cfg.dynamicSmemBytes = PairLayout::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<1>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();                    // a refused query leaves no error behind
+    cap = n;
+  }
+  return cap;
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                             int max_pairs, cudaStream_t s) {
+  if (a.mn_major) return cudaErrorInvalidValue;
+  const int cap0 = gemm_pair_capacity();
+  const int cap = cap0 < max_pairs ? cap0 : max_pairs;
+  if (cap <= 0) return cudaErrorNotSupported;
+  const int MB = (a.M + 2 * BM - 1) / (2 * BM);
+  const int NB = (a.N + BN - 1) / BN;
+  const int tiles = MB * NB;
+  if (tiles == 0) return cudaSuccess;
+  const int KB = (a.K + BK - 1) / BK;
+  if (a.ksplit > 1) {                      // split-K: (pair tile, K slice) units, each reduce-added
+    if (a.bias != nullptr || a.ksplit > KB) return cudaErrorInvalidValue;
+    const long long units = static_cast<long long>(tiles) * a.ksplit;
+    return launch_pair_inst<2>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
+  }
+  if (a.sk_part != nullptr && a.sk_flag != nullptr && KB >= kSplitMinKB && tiles > cap && tiles % cap != 0)
+    return launch_pair_inst<1>(tmA, tmB, tmC, a, cap, s);
+  return launch_pair_inst<0>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
+}
 int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
 
 cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

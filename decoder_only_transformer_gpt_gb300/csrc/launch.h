@@ -23,6 +23,16 @@ inline bool pdl_enabled() {
   return on;
 }
 
+// The CTA-pair (cluster of two) kernels where a product has one; GPT_GB300_NO_PAIR=1 uses the
+// single-CTA kernels everywhere.
+inline bool pair_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GPT_GB300_NO_PAIR");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};

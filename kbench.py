@@ -3,6 +3,7 @@
     python kbench.py attention --B 16 --T 1024 --H 12 --D 64
     python kbench.py attention_bwd --B 16 --T 1024 --H 12 --D 64
     python kbench.py gemm --M 16384 --N 768 --K 768 --epi 2
+    python kbench.py gemm --M 16384 --N 768 --K 3072 --pair
     python kbench.py head --M 16384 --V 50257 --C 768
     python kbench.py layernorm --M 16384 --C 768
     python kbench.py train --B 16 --T 1024
@@ -53,6 +54,8 @@ def main():
     ap.add_argument("--V", type=int, default=50257)
     ap.add_argument("--C", type=int, default=768)
     ap.add_argument("--epi", type=int, default=0)
+    ap.add_argument("--pair", action="store_true", help="gemm: the residual product on CTA pairs (gptk_gemm_pair)")
+    ap.add_argument("--ksplit", type=int, default=0, help="gemm --pair: K slices (no bias when > 1)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--iters", type=int, default=10)
     a = ap.parse_args()
@@ -83,9 +86,15 @@ def main():
         bias = torch.randn(a.N, device=dev)
         odt = torch.bfloat16 if a.epi in (0, 1) else torch.float32
         out_t = torch.zeros(a.M, a.N, device=dev, dtype=odt)
-        ms = _time(lambda: binding.gemm(A, W, bias, out_t, a.epi), a.warmup, a.iters)
+        if a.pair:
+            out_t = torch.zeros(a.M, a.N, device=dev, dtype=torch.float32)
+            pb = bias if a.ksplit <= 1 else None
+            ms = _time(lambda: binding.gemm_pair(A, W, pb, out_t, a.ksplit), a.warmup, a.iters)
+        else:
+            ms = _time(lambda: binding.gemm(A, W, bias, out_t, a.epi), a.warmup, a.iters)
         flop = 2.0 * a.M * a.N * a.K
-        out = {"kernel": f"gemm_epi{a.epi}", "shape": [a.M, a.N, a.K], "ms": ms, "tflops": flop / ms / 1e9}
+        name = f"gemm_pair_ks{a.ksplit}" if a.pair else f"gemm_epi{a.epi}"
+        out = {"kernel": name, "shape": [a.M, a.N, a.K], "ms": ms, "tflops": flop / ms / 1e9}
     elif a.kernel == "head":
         h = torch.randn(a.M, a.C, device=dev).to(torch.bfloat16)
         E = (0.02 * torch.randn(a.V, a.C, device=dev)).to(torch.bfloat16)
