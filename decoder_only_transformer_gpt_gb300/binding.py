@@ -88,7 +88,7 @@ def load(path: str = LIB_PATH):
                                           ctypes.c_float, vp]),
         "gpt_master_copy": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp]),
         "gptk_gemm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
-        "gptk_gemm_pair": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, vp]),
+        "gptk_gemm_pair": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, i32, vp]),
         "gptk_attention_lse": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp]),
         "gptk_attention_bwd": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
@@ -287,11 +287,11 @@ def gemm(A, W, bias, out, epilogue: int, stream=None):
            "gptk_gemm")
 
 
-def gemm_pair(A, W, bias, out, ksplit: int = 0, stream=None):
+def gemm_pair(A, W, bias, out, ksplit: int = 0, epilogue: int = EPI_BIAS_RESID, stream=None):
     lib = load()
     M, K = A.shape
     N = W.shape[0]
-    _check(lib.gptk_gemm_pair(_ptr(A), _ptr(W), _ptr(bias), _ptr(out), M, N, K, ksplit, _stream(stream)),
+    _check(lib.gptk_gemm_pair(_ptr(A), _ptr(W), _ptr(bias), _ptr(out), M, N, K, epilogue, ksplit, _stream(stream)),
            "gptk_gemm_pair")
 
 

@@ -17,6 +17,7 @@
 //   embedding: dE[id] += dx_0, dP[t] += dx_0.
 // Weight gradients with few output tiles split K (the token axis) and add their
 // partials with reduce-add stores into the zeroed fp32 gradient.
+#include "launch.h"
 #include "model.h"
 
 #include <cuda_runtime.h>
@@ -32,6 +33,7 @@ struct gpt_layer_grad {
   CUtensorMap tg_attn_w, tg_proj_w, tg_fc_w, tg_mp_w;      // fp32 reduce-add targets
   void *attn_wT, *proj_wT, *fc_wT, *mp_wT;                  // bf16 transposed weights [in, out]
   CUtensorMap tb_attn_wT, tb_proj_wT, tb_fc_wT, tb_mp_wT;  // as B operands
+  CUtensorMap tb_attn_wT_pair, tb_fc_wT_pair;                // the same with 128-row boxes (CTA pairs)
 };
 
 // One block's activations from the training forward (kept for its backward).
@@ -59,6 +61,7 @@ struct gpt_train {
   CUtensorMap tg_wte, tg_head;
   void* wteT = nullptr;          // the head's matrix (E when tied) transposed: [C][Vp] bf16
   CUtensorMap tb_wteT;
+  CUtensorMap tb_wteT_pair;      // the same with 128-row boxes (CTA pairs)
   bool wT_ready = false;
   // gradients of activations
   float *dx, *da;
@@ -193,6 +196,7 @@ int alloc_train(gpt_model* m) {
   // fixed descriptors: gradient reduce-add targets and transposed weights
   bool ok = make_tmap_2d(&t->tg_wte, t->g_wte, 4, V, C, 32, kEpiRows) &&
             make_tmap_2d_bf16(&t->tb_wteT, t->wteT, C, V, gemm_tc_bn(), Vp) &&
+            make_tmap_2d_bf16(&t->tb_wteT_pair, t->wteT, C, V, kGemmBM, Vp) &&
             (!t->g_head || make_tmap_2d(&t->tg_head, t->g_head, 4, V, C, 32, kEpiRows));
   for (size_t l = 0; l < L && ok; ++l) {
     gpt_layer_grad& g = t->lg[l];
@@ -203,7 +207,9 @@ int alloc_train(gpt_model* m) {
          make_tmap_2d_bf16(&g.tb_attn_wT, g.attn_wT, C, 3 * C, gemm_tc_bn()) &&
          make_tmap_2d_bf16(&g.tb_proj_wT, g.proj_wT, C, C, gemm_tc_bn()) &&
          make_tmap_2d_bf16(&g.tb_fc_wT, g.fc_wT, C, F, gemm_tc_bn()) &&
-         make_tmap_2d_bf16(&g.tb_mp_wT, g.mp_wT, F, C, gemm_tc_bn());
+         make_tmap_2d_bf16(&g.tb_mp_wT, g.mp_wT, F, C, gemm_tc_bn()) &&
+         make_tmap_2d_bf16(&g.tb_attn_wT_pair, g.attn_wT, C, 3 * C, kGemmBM) &&
+         make_tmap_2d_bf16(&g.tb_fc_wT_pair, g.fc_wT, C, F, kGemmBM);
   }
   if (!ok) {
     cudaFree(t->buf);
@@ -399,13 +405,24 @@ int head_backward(gpt_model* m, gpt_train* t, const int32_t* tg, int M, cudaStre
     a.ldo = C;
     a.err = m->err;
     a.b_const = 1;
-    const int tiles = ((M + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(C);
-    a.ksplit = long_k_split(tiles, (V + kGemmBK - 1) / kGemmBK, m->num_sms);
+    const int KB = (V + kGemmBK - 1) / kGemmBK;
+    const int pairs = pair_enabled() ? gemm_pair_capacity() : 0;
+    if (pairs > 0) {                       // CTA pairs: 256 x 256 tiles
+      const int tiles = ((M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * gemm_tc_num_ntiles(C);
+      a.ksplit = long_k_split(tiles, KB, pairs < m->num_sms / 2 ? pairs : m->num_sms / 2);
+    } else {
+      const int tiles = ((M + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(C);
+      a.ksplit = long_k_split(tiles, KB, m->num_sms);
+    }
     if (a.ksplit == 1) {
       a.sk_part = m->sk_part;
       a.sk_flag = m->sk_flag;
     }
-    BWS(GPT_STEP_B_DH, -1, cu(launch_gemm_tc(t->A_dz, t->tb_wteT, t->C_da, a, EPI_BIAS_RESID, m->num_sms, s), "dh"));
+    if (pairs > 0)
+      BWS(GPT_STEP_B_DH, -1,
+          cu(launch_gemm_pair(t->A_dz, t->tb_wteT_pair, t->C_da, a, EPI_BIAS_RESID, m->num_sms / 2, s), "dh"));
+    else
+      BWS(GPT_STEP_B_DH, -1, cu(launch_gemm_tc(t->A_dz, t->tb_wteT, t->C_da, a, EPI_BIAS_RESID, m->num_sms, s), "dh"));
   }
   if (c.final_ln) {
     BW(cu(launch_layernorm_bwd(m->x, m->lnf_g, t->da, t->dx, 0, t->g_lnf_g, t->g_lnf_b, M, C, c.ln_eps, m->num_sms, s),
@@ -453,7 +470,7 @@ int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t*
       GPT_CUDA(cudaMemcpyAsync(q.n, m->x, MC4, cudaMemcpyDeviceToDevice, s));
     }
     BW(gemm_bf16_gelu_u(m, q.A_a2, w.tm_fc_w, q.C_g, q.C_u, M, F, C, w.fc_b, q.g, s));   // g and u in one product
-    BW(gemm_bf16_resid(m, q.A_g, w.tm_mp_w, w.tm_mp_w_pair, m->tm_x_out, M, C, F, w.mp_b, m->x, s));
+    BW(gemm_bf16_long(m, q.A_g, w.tm_mp_w, w.tm_mp_w_pair, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
     if (pre) {
       const float* g = nullptr;
       const float* b = nullptr;
@@ -521,11 +538,13 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
   BWS(GPT_STEP_B_FC_W, l, grad_gemm(m, t->K_du, q.K_a2, g.tg_fc_w, g.fc_w, F, C, M, s));
   if (pre) {
     // da2 = du W_fc; s1 -> LN2 -> a2: dx += LN2'(da2)
-    BWS(GPT_STEP_B_DA2, l, gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_da, M, C, F, nullptr, t->da, EPI_F32_OUT, s));
+    BWS(GPT_STEP_B_DA2, l, gemm_bf16_long(m, t->A_du, g.tb_fc_wT, g.tb_fc_wT_pair, t->C_da, M, C, F, nullptr, t->da,
+                                          EPI_F32_OUT, s));
     BW(cu(launch_layernorm_bwd(q.s1, w.ln2_g, t->da, t->dx, 1, g.ln2_g, g.ln2_b, M, C, eps, m->num_sms, s), "ln2'"));
   } else {
     // dn = ds2 + du W_fc; n = LN1(s1): d loss / d s1 in place
-    BWS(GPT_STEP_B_DA2, l, gemm_bf16(m, t->A_du, g.tb_fc_wT, t->C_dx, M, C, F, nullptr, t->dx, EPI_BIAS_RESID, s));
+    BWS(GPT_STEP_B_DA2, l, gemm_bf16_long(m, t->A_du, g.tb_fc_wT, g.tb_fc_wT_pair, t->C_dx, M, C, F, nullptr, t->dx,
+                                          EPI_BIAS_RESID, s));
     BW(cu(launch_layernorm_bwd(q.s1, w.ln1_g, t->dx, t->dx, 0, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
   }
   // attention: s1 = x + y W_proj^T + b_proj, y = attention(qkv), qkv = a1 W_attn^T + b_attn
@@ -541,11 +560,13 @@ int block_backward(gpt_model* m, gpt_train* t, int l, int B, int T, cudaStream_t
   BWS(GPT_STEP_B_ATTN_W, l, grad_gemm(m, t->K_dqkv, q.K_a1, g.tg_attn_w, g.attn_w, 3 * C, C, M, s));
   if (pre) {
     // da1 = dqkv W_attn; x -> LN1 -> a1: dx += LN1'(da1)
-    BWS(GPT_STEP_B_DA1, l, gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_da, M, C, 3 * C, nullptr, t->da, EPI_F32_OUT, s));
+    BWS(GPT_STEP_B_DA1, l, gemm_bf16_long(m, t->A_dqkv, g.tb_attn_wT, g.tb_attn_wT_pair, t->C_da, M, C, 3 * C, nullptr,
+                                          t->da, EPI_F32_OUT, s));
     BW(cu(launch_layernorm_bwd(xl, w.ln1_g, t->da, t->dx, 1, g.ln1_g, g.ln1_b, M, C, eps, m->num_sms, s), "ln1'"));
   } else {
     // a1 = x: dx += dqkv W_attn
-    BWS(GPT_STEP_B_DA1, l, gemm_bf16(m, t->A_dqkv, g.tb_attn_wT, t->C_dx, M, C, 3 * C, nullptr, t->dx, EPI_BIAS_RESID, s));
+    BWS(GPT_STEP_B_DA1, l, gemm_bf16_long(m, t->A_dqkv, g.tb_attn_wT, g.tb_attn_wT_pair, t->C_dx, M, C, 3 * C, nullptr,
+                                          t->dx, EPI_BIAS_RESID, s));
   }
   return GPT_OK;
 }

@@ -101,17 +101,18 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   return GPT_OK;
 }
 
-// The residual product x += A W^T + bias. Long K (at least 1536: the MLP down-projection) runs on CTA
-// pairs (256 x 256 tiles, a six-stage ring of 32 KB per CTA); shorter products, or a device where
-// clusters of two cannot be resident, take the single-CTA kernel.
-int tc_gemm_resid(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
-                  const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* x, cudaStream_t s) {
+// An fp32 product (EPI_BIAS_RESID: x += A W^T + bias, or EPI_F32_OUT: out = A W^T + bias). Long K (at
+// least 1536: the MLP down-projection, the input gradients through W_fc and W_attn) runs on CTA pairs
+// (256 x 256 tiles, a six-stage ring of 32 KB per CTA; tmB_pair has 128-row boxes); shorter products,
+// or a device where clusters of two cannot be resident, take the single-CTA kernel.
+int tc_gemm_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
+                 const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* out, int epi, cudaStream_t s) {
   if (pair_enabled() && K >= 1536 && gemm_pair_capacity() > 0) {
-    const GemmArgs a = tc_args(m, M, N, K, bias, x);
-    GPT_CUDA(launch_gemm_pair(tmA, tmB_pair, tmC, a, m->num_sms / 2, s));
+    const GemmArgs a = tc_args(m, M, N, K, bias, out);
+    GPT_CUDA(launch_gemm_pair(tmA, tmB_pair, tmC, a, epi, m->num_sms / 2, s));
     return GPT_OK;
   }
-  return tc_gemm(m, tmA, tmB, tmC, M, N, K, bias, x, EPI_BIAS_RESID, s);
+  return tc_gemm(m, tmA, tmB, tmC, M, N, K, bias, out, epi, s);
 }
 
 // Layer l's key/value cache: [kv_batch][ctx][2C] bf16.
@@ -166,7 +167,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
     GPT_STEP(GPT_STEP_LN_MID, l,
              cu(launch_layernorm(m->x, mid.g, mid.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
     GPT_STEP(GPT_STEP_C_FC, l, tc_gemm(m, m->tm_a, w.tm_fc_w, m->tm_g_out, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
-    GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm_resid(m, m->tm_g, w.tm_mp_w, w.tm_mp_w_pair, m->tm_x_out, M, C, F, w.mp_b, m->x, s));
+    GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm_long(m, m->tm_g, w.tm_mp_w, w.tm_mp_w_pair, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
     GPT_STEP(GPT_STEP_LN_OUT, l,
              cu(launch_layernorm(m->x, out.g, out.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
   }
@@ -434,9 +435,9 @@ int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, cons
   return tc_gemm(m, tmA, tmB, tmC, M, N, K, bias, out, epi, s);
 }
 
-int gemm_bf16_resid(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
-                    const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* x, cudaStream_t s) {
-  return tc_gemm_resid(m, tmA, tmB, tmB_pair, tmC, M, N, K, bias, x, s);
+int gemm_bf16_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
+                   const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* out, int epi, cudaStream_t s) {
+  return tc_gemm_long(m, tmA, tmB, tmB_pair, tmC, M, N, K, bias, out, epi, s);
 }
 
 int gemm_bf16_gelu_u(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tm_g,

@@ -92,8 +92,10 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
 }
 
 int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
-                   int32_t ksplit, void* stream) {
+                   int32_t epilogue, int32_t ksplit, void* stream) {
   if (!A || !W || !out || M < 0 || N <= 0 || K <= 0) return GPT_EINVAL;
+  if (epilogue != GPTK_EPI_BIAS_RESID && epilogue != GPTK_EPI_F32) return GPT_EINVAL;
+  if (ksplit > 1 && epilogue != GPTK_EPI_BIAS_RESID) return GPT_EINVAL;
   if ((K % 8) || (N % 8) || !aligned16(A) || !aligned16(W) || !aligned16(out)) return GPT_EINVAL;
   if (ksplit > 1 && (bias != nullptr || ksplit > (K + kGemmBK - 1) / kGemmBK)) return GPT_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -128,7 +130,8 @@ int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, 
       return GPT_ECUDA;
     }
   }
-  const cudaError_t e = launch_gemm_pair(tmA, tmB, tmC, a, grid / 2, s);
+  const cudaError_t e =
+      launch_gemm_pair(tmA, tmB, tmC, a, epilogue == GPTK_EPI_F32 ? EPI_F32_OUT : EPI_BIAS_RESID, grid / 2, s);
   if (skws) cudaFreeAsync(skws, s);
   if (e != cudaSuccess) {
     set_detail("launch_gemm_pair", e);

@@ -815,7 +815,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ---------------------------------------------------------------- CTA-pair kernel (cta_group::2)
 
-// The residual product (EPI_BIAS_RESID: x += A W^T + bias) on a pair of CTAs in a cluster of two:
+// The fp32 products (EPI_BIAS_RESID: x += A W^T + bias; EPI_F32_OUT: out = A W^T + bias) on a pair of
+// CTAs in a cluster of two:
 // one tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), issued by the even CTA, reads the pair's
 // 256 A rows from both CTAs' shared memory (128 each) and the 256 W rows likewise (128 each), and
 // leaves rows 0-127 of the 256 x 256 accumulator in the even CTA's TMEM and rows 128-255 in the odd
@@ -923,7 +924,7 @@ __device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar) {
 // pairs of CTAs: pair p = blockIdx.x / 2 takes the work gemm_tc_kernel gives CTA p of gridDim.x / 2.
 // A stream-K partial is handed between the CTAs of equal rank in neighbouring pairs (slot blockIdx.x,
 // taken from slot blockIdx.x + 2).
-template <int MODE>
+template <int EPI, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -1153,14 +1154,15 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           const int n0 = nb * BN + c * 32;
           if (n0 >= args.N) continue;
           uint32_t w[32];
-          finish_chunk<EPI_BIAS_RESID, 32>(args, r + h * 32, args.bias != nullptr ? my_bias + c * 32 : nullptr, w);
-          if (lane == 0) bulk_wait_read<0>();          // the previous reduce-add has read the box
+          finish_chunk<EPI, 32>(args, r + h * 32, args.bias != nullptr ? my_bias + c * 32 : nullptr, w);
+          if (lane == 0) bulk_wait_read<0>();          // the previous store has read the box
           __syncwarp();
           stage_row(my_stage, lane, w);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d(&tmC, my_stage, n0, m0);
+            if (EPI == EPI_BIAS_RESID) tma_reduce_add_2d(&tmC, my_stage, n0, m0);   // x += tile, in L2
+            else tma_store_2d(&tmC, my_stage, n0, m0);
             bulk_commit();
           }
         }
@@ -1183,12 +1185,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   cluster_sync_all();
 }
 
-template <int MODE>
+template <int EPI, int MODE>
 cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                              int pairs, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                PairLayout::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -1207,7 +1209,7 @@ cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, con
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MODE>, tmA, tmB, tmC, a);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, MODE>, tmA, tmB, tmC, a);
 }
 
 template <int EPI, int MODE, bool MN = false>
@@ -1288,7 +1290,7 @@ int gemm_pair_capacity() {
   static int cap = -1;
   if (cap < 0) {
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::SMEM) ==
+    if (cudaFuncSetAttribute(gemm_pair_kernel<EPI_BIAS_RESID, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::SMEM) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2);
@@ -1301,7 +1303,7 @@ int gemm_pair_capacity() {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<1>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI_BIAS_RESID, 1>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();                    // a refused query leaves no error behind
     cap = n;
@@ -1309,8 +1311,9 @@ int gemm_pair_capacity() {
   return cap;
 }
 
-cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
-                             int max_pairs, cudaStream_t s) {
+template <int EPI>
+cudaError_t launch_pair_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                            int max_pairs, cudaStream_t s) {
   if (a.mn_major) return cudaErrorInvalidValue;
   const int cap0 = gemm_pair_capacity();
   const int cap = cap0 < max_pairs ? cap0 : max_pairs;
@@ -1321,13 +1324,20 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, con
   if (tiles == 0) return cudaSuccess;
   const int KB = (a.K + BK - 1) / BK;
   if (a.ksplit > 1) {                      // split-K: (pair tile, K slice) units, each reduce-added
-    if (a.bias != nullptr || a.ksplit > KB) return cudaErrorInvalidValue;
+    if (EPI != EPI_BIAS_RESID || a.bias != nullptr || a.ksplit > KB) return cudaErrorInvalidValue;
     const long long units = static_cast<long long>(tiles) * a.ksplit;
-    return launch_pair_inst<2>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
+    return launch_pair_inst<EPI, 2>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
   }
   if (a.sk_part != nullptr && a.sk_flag != nullptr && KB >= kSplitMinKB && tiles > cap && tiles % cap != 0)
-    return launch_pair_inst<1>(tmA, tmB, tmC, a, cap, s);
-  return launch_pair_inst<0>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
+    return launch_pair_inst<EPI, 1>(tmA, tmB, tmC, a, cap, s);
+  return launch_pair_inst<EPI, 0>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
+                             int epi, int max_pairs, cudaStream_t s) {
+  if (epi == EPI_BIAS_RESID) return launch_pair_epi<EPI_BIAS_RESID>(tmA, tmB, tmC, a, max_pairs, s);
+  if (epi == EPI_F32_OUT) return launch_pair_epi<EPI_F32_OUT>(tmA, tmB, tmC, a, max_pairs, s);
+  return cudaErrorInvalidValue;
 }
 int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
 

@@ -96,9 +96,10 @@ int forward_maps(gpt_model* m, int B, int T);
 int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
               int K, const float* bias, void* out, int epi, cudaStream_t s);
 // c_fc of the training forward: g = gelu(a W^T + b) through tm_g and the GELU's input u through tm_u.
-// x += A W^T + bias (fp32 x through tmC): on CTA pairs for long K where they can run, else as gemm_bf16.
-int gemm_bf16_resid(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
-                    const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* x, cudaStream_t s);
+// An fp32 product, epi EPI_BIAS_RESID (out += A W^T + bias) or EPI_F32_OUT (out = A W^T + bias), through
+// tmC: on CTA pairs for long K where they can run (tmB_pair: W with 128-row boxes), else as gemm_bf16.
+int gemm_bf16_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
+                   const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* out, int epi, cudaStream_t s);
 int gemm_bf16_gelu_u(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tm_g,
                      const CUtensorMap& tm_u, int M, int N, int K, const float* bias, void* g, cudaStream_t s);
 int shape_ok(const gpt_model* m, int B, int T);

@@ -1,10 +1,10 @@
-"""The residual product on CTA pairs (gptk_gemm_pair: clusters of two, tcgen05.mma.cta_group::2,
+"""The fp32 products on CTA pairs (gptk_gemm_pair: clusters of two, tcgen05.mma.cta_group::2,
 256 x 256 tiles) against the fp64 oracle, element by element, through the C ABI.
 
-out (fp32) += A W^T + bias with exact bf16 inputs; the bound is the fp32 accumulation bound of
-the single-CTA tests (K 2^-23 sum|a||w|) plus the roundings of the additions into out: one for
-whole tiles and stream-K (the finishing CTA adds the other's partial before its one reduce-add),
-one per slice for split-K.
+out (fp32) += A W^T + bias (the residual add) or out = A W^T + bias, with exact bf16 inputs; the
+bound is the fp32 accumulation bound of the single-CTA tests (K 2^-23 sum|a||w|) plus the roundings
+of the additions into out: one for whole tiles and stream-K (the finishing CTA adds the other's
+partial before its one store), one per slice for split-K.
 """
 import numpy as np
 import pytest
@@ -30,18 +30,26 @@ def _inputs(M, N, K, seed, bias=True):
 
 def _check_rows(A, W, b, x0, got, r0, r1, adds):
     K = A.shape[1]
-    ref = x0[r0:r1].astype(np.float64) + oracle.linear(A[r0:r1], W, b if b is not None else np.zeros(W.shape[0], np.float32))
+    ref = oracle.linear(A[r0:r1], W, b if b is not None else np.zeros(W.shape[0], np.float32))
+    if x0 is not None:
+        ref = ref + x0[r0:r1].astype(np.float64)
     tol = K * EPS23 * (np.abs(A[r0:r1]).astype(np.float64) @ np.abs(W).astype(np.float64).T) + 1e-6
     tol = tol + (3 + adds) * EPS23 * np.abs(ref)
     bad = np.abs(got - ref) > tol
     assert not bad.any(), f"rows {r0}:{r1}: {bad.sum()} of {bad.size} outside bound; worst {np.max(np.abs(got - ref) - tol)}"
 
 
-def _run(M, N, K, seed, ksplit=0, bias=True):
+def _run(M, N, K, seed, ksplit=0, bias=True, store=False):
+    """store: out = A W^T + bias over a buffer of NaNs (every element must be written)."""
     from decoder_only_transformer_gpt_gb300 import binding
     A, W, b, x0 = _inputs(M, N, K, seed, bias)
-    out = dev_f32(x0)
-    binding.gemm_pair(dev_bf16(A), dev_bf16(W), dev_f32(b) if b is not None else None, out, ksplit)
+    if store:
+        x0 = None
+        out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    else:
+        out = dev_f32(x0)
+    epi = binding.EPI_F32 if store else binding.EPI_BIAS_RESID
+    binding.gemm_pair(dev_bf16(A), dev_bf16(W), dev_f32(b) if b is not None else None, out, ksplit, epi)
     binding.status()
     return A, W, b, x0, out
 
@@ -61,8 +69,15 @@ def test_gemm_pair_whole_tiles(gpt_lib, M, N, K):
 # (4000, 2304, 1544) 144 tiles with a ragged last K block, (5000, 1600, 1600) 140 tiles with a ragged
 # last column tile (the GPT-2 XL width).
 @pytest.mark.parametrize("M,N,K", [(6500, 768, 3072), (4000, 2304, 1544), (5000, 1600, 1600)])
-def test_gemm_pair_stream_k(gpt_lib, M, N, K):
-    A, W, b, x0, out = _run(M, N, K, seed=K)
+@pytest.mark.parametrize("store", [False, True])
+def test_gemm_pair_stream_k(gpt_lib, M, N, K, store):
+    A, W, b, x0, out = _run(M, N, K, seed=K, store=store)
+    _check_rows(A, W, b, x0, host(out), 0, M, 1)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 192), (129, 768, 2304)])
+def test_gemm_pair_store_whole_tiles(gpt_lib, M, N, K):
+    A, W, b, x0, out = _run(M, N, K, seed=M + K, store=True)
     _check_rows(A, W, b, x0, host(out), 0, M, 1)
 
 
@@ -111,3 +126,7 @@ def test_gemm_pair_rejects_bad_arguments(gpt_lib):
         binding.gemm_pair(A, W, b, out, 2)               # split-K with a bias
     with pytest.raises(binding.GptError):
         binding.gemm_pair(A, W, None, out, 5)            # more slices than K blocks
+    with pytest.raises(binding.GptError):
+        binding.gemm_pair(A, W, None, out, 2, binding.EPI_F32)   # split-K of a store
+    with pytest.raises(binding.GptError):
+        binding.gemm_pair(A, W, b, out, 0, binding.EPI_BIAS)     # a bf16 output
