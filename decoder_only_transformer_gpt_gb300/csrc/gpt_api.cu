@@ -223,6 +223,9 @@ int gpt_create(const gpt_config* cfg, const gpt_weights* w, gpt_model** out) {
                       make_tmap_2d_bf16(&d.tm_proj_w, d.proj_w, C, C, gemm_tc_bn()) &&
                       make_tmap_2d_bf16(&d.tm_fc_w, d.fc_w, F, C, gemm_tc_bn()) &&
                       make_tmap_2d_bf16(&d.tm_mp_w, d.mp_w, C, F, gemm_tc_bn()) &&
+                      make_tmap_2d_bf16(&d.tm_attn_w_pair, d.attn_w, 3 * C, C, kGemmBM) &&
+                      make_tmap_2d_bf16(&d.tm_proj_w_pair, d.proj_w, C, C, kGemmBM) &&
+                      make_tmap_2d_bf16(&d.tm_fc_w_pair, d.fc_w, F, C, kGemmBM) &&
                       make_tmap_2d_bf16(&d.tm_mp_w_pair, d.mp_w, C, F, kGemmBM);
       if (!ok) { set_detail_text("weight tensor map"); rc = GPT_ECUDA; }
     }

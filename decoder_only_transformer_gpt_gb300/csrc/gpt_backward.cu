@@ -459,7 +459,7 @@ int train_forward(gpt_model* m, gpt_train* t, const int32_t* ids, const int32_t*
     gpt_layer_act& q = t->la[l];
     void* next_a = (l + 1 < L) ? t->la[l + 1].a1 : m->a;
     GPT_CUDA(cudaMemcpyAsync(q.x, m->x, MC4, cudaMemcpyDeviceToDevice, s));
-    BW(gemm_bf16(m, q.A_a1, w.tm_attn_w, q.C_qkv, M, 3 * C, C, w.attn_b, q.qkv, EPI_BIAS_OUT, s));
+    BW(gemm_bf16_long(m, q.A_a1, w.tm_attn_w, w.tm_attn_w_pair, q.C_qkv, M, 3 * C, C, w.attn_b, q.qkv, EPI_BIAS_OUT, s));
     BW(cu(launch_attention_tc(q.Q3, q.y, B, T, c.H, C / c.H, m->err, m->attn_sched, s, q.lse2), "attention"));
     BW(gemm_bf16(m, q.A_y, w.tm_proj_w, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
     GPT_CUDA(cudaMemcpyAsync(q.s1, m->x, MC4, cudaMemcpyDeviceToDevice, s));

@@ -101,13 +101,19 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   return GPT_OK;
 }
 
-// An fp32 product (EPI_BIAS_RESID: x += A W^T + bias, or EPI_F32_OUT: out = A W^T + bias). Long K (at
-// least 1536: the MLP down-projection, the input gradients through W_fc and W_attn) runs on CTA pairs
-// (256 x 256 tiles, a six-stage ring of 32 KB per CTA; tmB_pair has 128-row boxes); shorter products,
-// or a device where clusters of two cannot be resident, take the single-CTA kernel.
+// A product with a tensor-store epilogue (EPI_BIAS_RESID, EPI_F32_OUT, EPI_BIAS_OUT, EPI_BIAS_GELU_OUT) on
+// CTA pairs (256 x 256 tiles, a six-stage ring of 32 KB per CTA; tmB_pair has 128-row boxes) where they
+// were measured faster in the GPT-2 small step at 16,384 tokens: long K (at least 1536: mlp c_proj
+// 66 -> 61 us, the input gradients through W_fc and W_attn) and the QKV projection (N = 2304, bf16 out:
+// 46.6 -> 44.5 us). Not c_fc (59 -> 64 us: its GELU epilogue bounds each tile, and the pair ties both
+// CTAs' epilogues to one accumulator hand-off) nor the attention c_proj (32 us either way). Elsewhere,
+// or where clusters of two cannot be resident, the single-CTA kernel.
+constexpr int kPairMinK = 1536;
+bool pair_pays(int N, int K, int epi) { return K >= kPairMinK || (epi == EPI_BIAS_OUT && N >= 2048); }
+
 int tc_gemm_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
-                 const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* out, int epi, cudaStream_t s) {
-  if (pair_enabled() && K >= 1536 && gemm_pair_capacity() > 0) {
+                 const CUtensorMap& tmC, int M, int N, int K, const float* bias, void* out, int epi, cudaStream_t s) {
+  if (pair_enabled() && pair_pays(N, K, epi) && gemm_pair_capacity() > 0) {
     const GemmArgs a = tc_args(m, M, N, K, bias, out);
     GPT_CUDA(launch_gemm_pair(tmA, tmB_pair, tmC, a, epi, m->num_sms / 2, s));
     return GPT_OK;
@@ -147,7 +153,7 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
   }
   for (int l = 0; l < L; ++l) {
     const gpt_layer_dev& w = m->layers[l];
-    GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm(m, m->tm_a, w.tm_attn_w, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
+    GPT_STEP(GPT_STEP_C_ATTN, l, tc_gemm_long(m, m->tm_a, w.tm_attn_w, w.tm_attn_w_pair, m->tm_qkv_out, M, 3 * C, C, w.attn_b, m->qkv, EPI_BIAS_OUT, s));
     if (m->kv_fill) {                       // prefill: keep every token's key and value
       ++m->launches;
       rc = cu(launch_kv_store(m->qkv, kv_layer(m, l), B, T, C, c.ctx, s), "kv_store");
@@ -163,10 +169,10 @@ int forward_bf16(gpt_model* m, const int32_t* ids, const int32_t* tg, int B, int
       if (l + 1 < L) out = {m->layers[l + 1].ln1_g, m->layers[l + 1].ln1_b};
       else if (c.final_ln) out = {m->lnf_g, m->lnf_b};
     }
-    GPT_STEP(GPT_STEP_C_PROJ, l, tc_gemm(m, m->tm_y, w.tm_proj_w, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
+    GPT_STEP(GPT_STEP_C_PROJ, l, tc_gemm_long(m, m->tm_y, w.tm_proj_w, w.tm_proj_w_pair, m->tm_x_out, M, C, C, w.proj_b, m->x, EPI_BIAS_RESID, s));
     GPT_STEP(GPT_STEP_LN_MID, l,
              cu(launch_layernorm(m->x, mid.g, mid.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
-    GPT_STEP(GPT_STEP_C_FC, l, tc_gemm(m, m->tm_a, w.tm_fc_w, m->tm_g_out, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
+    GPT_STEP(GPT_STEP_C_FC, l, tc_gemm_long(m, m->tm_a, w.tm_fc_w, w.tm_fc_w_pair, m->tm_g_out, M, F, C, w.fc_b, m->g, EPI_BIAS_GELU_OUT, s));
     GPT_STEP(GPT_STEP_MLP_PROJ, l, tc_gemm_long(m, m->tm_g, w.tm_mp_w, w.tm_mp_w_pair, m->tm_x_out, M, C, F, w.mp_b, m->x, EPI_BIAS_RESID, s));
     GPT_STEP(GPT_STEP_LN_OUT, l,
              cu(launch_layernorm(m->x, out.g, out.b, m->a, 1, pre ? nullptr : m->x, M, C, c.ln_eps, s), "ln"));
@@ -436,7 +442,7 @@ int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, cons
 }
 
 int gemm_bf16_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
-                   const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* out, int epi, cudaStream_t s) {
+                   const CUtensorMap& tmC, int M, int N, int K, const float* bias, void* out, int epi, cudaStream_t s) {
   return tc_gemm_long(m, tmA, tmB, tmB_pair, tmC, M, N, K, bias, out, epi, s);
 }
 

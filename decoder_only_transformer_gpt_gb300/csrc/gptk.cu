@@ -91,10 +91,10 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
   return GPT_OK;
 }
 
-int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
+int gptk_gemm_pair(const void* A, const void* W, const float* bias, void* out, int32_t M, int32_t N, int32_t K,
                    int32_t epilogue, int32_t ksplit, void* stream) {
   if (!A || !W || !out || M < 0 || N <= 0 || K <= 0) return GPT_EINVAL;
-  if (epilogue != GPTK_EPI_BIAS_RESID && epilogue != GPTK_EPI_F32) return GPT_EINVAL;
+  if (epilogue < GPTK_EPI_BIAS || epilogue > GPTK_EPI_F32) return GPT_EINVAL;
   if (ksplit > 1 && epilogue != GPTK_EPI_BIAS_RESID) return GPT_EINVAL;
   if ((K % 8) || (N % 8) || !aligned16(A) || !aligned16(W) || !aligned16(out)) return GPT_EINVAL;
   if (ksplit > 1 && (bias != nullptr || ksplit > (K + kGemmBK - 1) / kGemmBK)) return GPT_EINVAL;
@@ -104,8 +104,9 @@ int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, 
   int* err = err_word();
   if (!err) return GPT_ENOMEM;
   CUtensorMap tmA, tmB, tmC;
+  const bool bf16_out = epilogue == GPTK_EPI_BIAS || epilogue == GPTK_EPI_BIAS_GELU;
   if (!make_tmap_2d_bf16(&tmA, A, M, K, kGemmBM) || !make_tmap_2d_bf16(&tmB, W, N, K, kGemmBM) ||
-      !make_tmap_2d(&tmC, out, 4, M, N, 32, kEpiRows)) {
+      !(bf16_out ? make_tmap_2d(&tmC, out, 2, M, N, 64, kEpiRows) : make_tmap_2d(&tmC, out, 4, M, N, 32, kEpiRows))) {
     set_detail_text("gemm tensor map");
     return GPT_ECUDA;
   }
@@ -117,7 +118,7 @@ int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, 
   a.ksplit = ksplit > 1 ? ksplit : 0;
   const int grid = num_sms();
   uint8_t* skws = nullptr;                 // stream-K partial tiles + flags, on the stream
-  if (ksplit <= 1) {
+  if (ksplit <= 1 && gemm_pair_stream_k(M, N, K, grid / 2)) {
     const size_t pbytes = gemm_sk_part_floats(grid) * sizeof(float);
     const size_t fbytes = gemm_sk_flag_ints(grid) * sizeof(int);
     GPT_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&skws), pbytes + fbytes, s));
@@ -130,8 +131,10 @@ int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, 
       return GPT_ECUDA;
     }
   }
-  const cudaError_t e =
-      launch_gemm_pair(tmA, tmB, tmC, a, epilogue == GPTK_EPI_F32 ? EPI_F32_OUT : EPI_BIAS_RESID, grid / 2, s);
+  const int epi = epilogue == GPTK_EPI_BIAS ? EPI_BIAS_OUT
+                  : epilogue == GPTK_EPI_BIAS_GELU ? EPI_BIAS_GELU_OUT
+                  : epilogue == GPTK_EPI_F32 ? EPI_F32_OUT : EPI_BIAS_RESID;
+  const cudaError_t e = launch_gemm_pair(tmA, tmB, tmC, a, epi, grid / 2, s);
   if (skws) cudaFreeAsync(skws, s);
   if (e != cudaSuccess) {
     set_detail("launch_gemm_pair", e);

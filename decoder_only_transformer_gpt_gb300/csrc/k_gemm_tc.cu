@@ -815,8 +815,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ---------------------------------------------------------------- CTA-pair kernel (cta_group::2)
 
-// The fp32 products (EPI_BIAS_RESID: x += A W^T + bias; EPI_F32_OUT: out = A W^T + bias) on a pair of
-// CTAs in a cluster of two:
+// The products with a tensor-store epilogue (EPI_BIAS_RESID: x += A W^T + bias; EPI_F32_OUT: out = A W^T
+// + bias; EPI_BIAS_OUT, EPI_BIAS_GELU_OUT: bf16 out) on a pair of CTAs in a cluster of two:
 // one tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), issued by the even CTA, reads the pair's
 // 256 A rows from both CTAs' shared memory (128 each) and the 256 W rows likewise (128 each), and
 // leaves rows 0-127 of the 256 x 256 accumulator in the even CTA's TMEM and rows 128-255 in the odd
@@ -1148,13 +1148,14 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + p4.w);
           }
         }
+        constexpr int CW = (EPI == EPI_BIAS_RESID || EPI == EPI_F32_OUT) ? 32 : 64;   // columns per 128-byte row
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = c2 * 2 + h;                    // 32-column chunk within the tile
-          const int n0 = nb * BN + c * 32;
+        for (int h = 0; h < 64 / CW; ++h) {
+          const int c = c2 * (64 / CW) + h;            // chunk of CW columns within the tile
+          const int n0 = nb * BN + c * CW;
           if (n0 >= args.N) continue;
           uint32_t w[32];
-          finish_chunk<EPI, 32>(args, r + h * 32, args.bias != nullptr ? my_bias + c * 32 : nullptr, w);
+          finish_chunk<EPI, CW>(args, r + h * CW, args.bias != nullptr ? my_bias + c * CW : nullptr, w);
           if (lane == 0) bulk_wait_read<0>();          // the previous store has read the box
           __syncwarp();
           stage_row(my_stage, lane, w);
@@ -1311,6 +1312,15 @@ int gemm_pair_capacity() {
   return cap;
 }
 
+bool pair_split(int tiles, int KB, int cap) { return KB >= kSplitMinKB && tiles > cap && tiles % cap != 0; }
+
+bool gemm_pair_stream_k(int M, int N, int K, int max_pairs) {
+  const int cap0 = gemm_pair_capacity();
+  const int cap = cap0 < max_pairs ? cap0 : max_pairs;
+  const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
+  return cap > 0 && pair_split(tiles, (K + BK - 1) / BK, cap);
+}
+
 template <int EPI>
 cudaError_t launch_pair_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                             int max_pairs, cudaStream_t s) {
@@ -1328,16 +1338,20 @@ cudaError_t launch_pair_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     const long long units = static_cast<long long>(tiles) * a.ksplit;
     return launch_pair_inst<EPI, 2>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
   }
-  if (a.sk_part != nullptr && a.sk_flag != nullptr && KB >= kSplitMinKB && tiles > cap && tiles % cap != 0)
+  if (a.sk_part != nullptr && a.sk_flag != nullptr && pair_split(tiles, KB, cap))
     return launch_pair_inst<EPI, 1>(tmA, tmB, tmC, a, cap, s);
   return launch_pair_inst<EPI, 0>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
 }
 
 cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                              int epi, int max_pairs, cudaStream_t s) {
-  if (epi == EPI_BIAS_RESID) return launch_pair_epi<EPI_BIAS_RESID>(tmA, tmB, tmC, a, max_pairs, s);
-  if (epi == EPI_F32_OUT) return launch_pair_epi<EPI_F32_OUT>(tmA, tmB, tmC, a, max_pairs, s);
-  return cudaErrorInvalidValue;
+  switch (epi) {
+    case EPI_BIAS_RESID: return launch_pair_epi<EPI_BIAS_RESID>(tmA, tmB, tmC, a, max_pairs, s);
+    case EPI_F32_OUT: return launch_pair_epi<EPI_F32_OUT>(tmA, tmB, tmC, a, max_pairs, s);
+    case EPI_BIAS_OUT: return launch_pair_epi<EPI_BIAS_OUT>(tmA, tmB, tmC, a, max_pairs, s);
+    case EPI_BIAS_GELU_OUT: return launch_pair_epi<EPI_BIAS_GELU_OUT>(tmA, tmB, tmC, a, max_pairs, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 int gemm_tc_num_ntiles(int N) { return (N + BN - 1) / BN; }
 

@@ -78,10 +78,10 @@ int gemm_tc_num_ntiles(int N);
 constexpr int kEpiRows = 32;
 cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const GemmArgs& a, int epi, int grid_limit, cudaStream_t s);
-// EPI_BIAS_RESID (out fp32 += A W^T + bias) or EPI_F32_OUT (out fp32 = A W^T + bias) on CTA pairs
-// (clusters of two, tcgen05.mma.cta_group::2): 256 x 256 tiles, each CTA staging its 128 A rows and
-// 128 of the tile's W rows per K block, so tmB must have a box of 128 rows (kGemmBM) instead of
-// gemm_tc_bn(); tmC is the fp32 [M, N] map with 32 x 32 boxes. Whole tiles, stream-K (given the
+// EPI_BIAS_RESID (out fp32 += A W^T + bias), EPI_F32_OUT (out fp32 = A W^T + bias), EPI_BIAS_OUT or
+// EPI_BIAS_GELU_OUT (bf16 out) on CTA pairs (clusters of two, tcgen05.mma.cta_group::2): 256 x 256
+// tiles, each CTA staging its 128 A rows and 128 of the tile's W rows per K block, so tmB must have a
+// box of 128 rows (kGemmBM) instead of gemm_tc_bn(); tmC as for launch_gemm_tc. Whole tiles, stream-K (given the
 // workspace, for K >= 1536 where whole tiles leave a part-idle last wave) or split-K (EPI_BIAS_RESID,
 // ksplit > 1, no bias). At most max_pairs pairs (and no more than can be resident).
 // cudaErrorNotSupported: clusters of two with this kernel's shared memory cannot run on this device
@@ -89,6 +89,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                              int epi, int max_pairs, cudaStream_t s);
 int gemm_pair_capacity();               // CTA pairs of that kernel resident at once (0: none)
+bool gemm_pair_stream_k(int M, int N, int K, int max_pairs);   // whether it splits tiles (needs the workspace)
 // The same with a second output map (EPI_BIAS_GELU_UOUT: tmC2 receives the GELU's input).
 cudaError_t launch_gemm_tc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                             const CUtensorMap& tmC2, const GemmArgs& a, int epi, int grid_limit, cudaStream_t s);

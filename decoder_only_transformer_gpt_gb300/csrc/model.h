@@ -10,7 +10,7 @@ struct gpt_layer_dev {
   void *attn_w, *proj_w, *fc_w, *mp_w;                     // bf16 or fp32 [out, in]
   float *attn_b, *proj_b, *fc_b, *mp_b, *ln1_g, *ln1_b, *ln2_g, *ln2_b;
   CUtensorMap tm_attn_w, tm_proj_w, tm_fc_w, tm_mp_w;      // bf16 path only
-  CUtensorMap tm_mp_w_pair;                                // mp_w with 128-row boxes (launch_gemm_pair)
+  CUtensorMap tm_attn_w_pair, tm_proj_w_pair, tm_fc_w_pair, tm_mp_w_pair;   // 128-row boxes (launch_gemm_pair)
 };
 
 struct gpt_train;                 // backward-pass workspace and gradients (gpt_backward.cu)
@@ -96,10 +96,11 @@ int forward_maps(gpt_model* m, int B, int T);
 int gemm_bf16(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M, int N,
               int K, const float* bias, void* out, int epi, cudaStream_t s);
 // c_fc of the training forward: g = gelu(a W^T + b) through tm_g and the GELU's input u through tm_u.
-// An fp32 product, epi EPI_BIAS_RESID (out += A W^T + bias) or EPI_F32_OUT (out = A W^T + bias), through
-// tmC: on CTA pairs for long K where they can run (tmB_pair: W with 128-row boxes), else as gemm_bf16.
+// A product with epi EPI_BIAS_RESID (out fp32 += A W^T + bias), EPI_F32_OUT (out fp32 = A W^T + bias),
+// EPI_BIAS_OUT or EPI_BIAS_GELU_OUT (bf16 out) through tmC: on CTA pairs where they pay and can run
+// (tmB_pair: W with 128-row boxes), else as gemm_bf16.
 int gemm_bf16_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,
-                   const CUtensorMap& tmC, int M, int N, int K, const float* bias, float* out, int epi, cudaStream_t s);
+                   const CUtensorMap& tmC, int M, int N, int K, const float* bias, void* out, int epi, cudaStream_t s);
 int gemm_bf16_gelu_u(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tm_g,
                      const CUtensorMap& tm_u, int M, int N, int K, const float* bias, void* g, cudaStream_t s);
 int shape_ok(const gpt_model* m, int B, int T);

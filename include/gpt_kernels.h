@@ -42,18 +42,19 @@ int gptk_gemm(const void* A, const void* W, const float* bias, void* out, int32_
               int32_t K, int32_t epilogue, int32_t dtype, void* stream);
 
 /*
- * The fp32 products on pairs of CTAs: clusters of two whose tcgen05.mma.cta_group::2 computes
+ * The bf16 products on pairs of CTAs: clusters of two whose tcgen05.mma.cta_group::2 computes
  * 256 x 256 tiles, each CTA staging 128 rows of A and 128 of the tile's W rows per K step.
- * epilogue GPTK_EPI_BIAS_RESID: out[M,N] += A[M,K] . W[N,K]^T + bias[N] (the residual add);
- * GPTK_EPI_F32: out = A W^T + bias. A and W bf16 row-major, K and N multiples of 8, 16-byte
- * aligned pointers; bias fp32 [N] or NULL; out fp32 row-major [M, N]. ksplit <= 1: whole tiles,
+ * The epilogues of gptk_gemm: GPTK_EPI_BIAS and GPTK_EPI_BIAS_GELU (out bf16), GPTK_EPI_BIAS_RESID
+ * (out fp32 += A W^T + bias, the residual add), GPTK_EPI_F32 (out fp32 = A W^T + bias). A and W
+ * bf16 row-major [M,K] and [N,K], K and N multiples of 8, 16-byte aligned pointers; bias fp32 [N]
+ * or NULL; out row-major [M, N]. ksplit <= 1: whole tiles,
  * or stream-K (as gptk_gemm, workspace on the stream) where whole tiles would leave a part-idle
  * last wave and K >= 1536; ksplit > 1 (GPTK_EPI_BIAS_RESID only): each tile's K range is cut
  * into ksplit slices whose partial products are added into out separately (bias must be NULL;
  * the order of those fp32 additions varies between runs). GPT_ECONFIG if clusters of two with
  * this kernel's shared memory cannot be resident on the device.
  */
-int gptk_gemm_pair(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
+int gptk_gemm_pair(const void* A, const void* W, const float* bias, void* out, int32_t M, int32_t N,
                    int32_t K, int32_t epilogue, int32_t ksplit, void* stream);
 
 /*

@@ -89,11 +89,12 @@ def main():
         if a.pair:
             out_t = torch.zeros(a.M, a.N, device=dev, dtype=torch.float32)
             pb = bias if a.ksplit <= 1 else None
-            ms = _time(lambda: binding.gemm_pair(A, W, pb, out_t, a.ksplit), a.warmup, a.iters)
+            pe = binding.EPI_F32 if a.epi == binding.EPI_F32 else binding.EPI_BIAS_RESID
+            ms = _time(lambda: binding.gemm_pair(A, W, pb, out_t, a.ksplit, pe), a.warmup, a.iters)
         else:
             ms = _time(lambda: binding.gemm(A, W, bias, out_t, a.epi), a.warmup, a.iters)
         flop = 2.0 * a.M * a.N * a.K
-        name = f"gemm_pair_ks{a.ksplit}" if a.pair else f"gemm_epi{a.epi}"
+        name = f"gemm_pair_epi{a.epi}_ks{a.ksplit}" if a.pair else f"gemm_epi{a.epi}"
         out = {"kernel": name, "shape": [a.M, a.N, a.K], "ms": ms, "tflops": flop / ms / 1e9}
     elif a.kernel == "head":
         h = torch.randn(a.M, a.C, device=dev).to(torch.bfloat16)

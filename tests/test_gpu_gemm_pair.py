@@ -129,4 +129,31 @@ def test_gemm_pair_rejects_bad_arguments(gpt_lib):
     with pytest.raises(binding.GptError):
         binding.gemm_pair(A, W, None, out, 2, binding.EPI_F32)   # split-K of a store
     with pytest.raises(binding.GptError):
-        binding.gemm_pair(A, W, b, out, 0, binding.EPI_BIAS)     # a bf16 output
+        binding.gemm_pair(A, W, b, out, 0, 7)                    # no such epilogue
+
+
+# bf16 outputs on pairs (the QKV projection and c_fc's epilogues): one bf16 ulp of the value on top of
+# the accumulation bound, and tanh.approx's error for the GELU (as for the single-CTA kernel).
+@pytest.mark.parametrize("M,N,K", [(300, 520, 192), (2000, 3072, 768), (6500, 768, 3072), (129, 2304, 768)])
+@pytest.mark.parametrize("gelu", [False, True])
+def test_gemm_pair_bf16_out(gpt_lib, M, N, K, gelu):
+    from decoder_only_transformer_gpt_gb300 import binding
+    from gpu_util import bf16_ulp
+    rng = np.random.default_rng(M + N + K + gelu)
+    A = rand_bf16(rng, (M, K))
+    W = rand_bf16(rng, (N, K), 0.5)
+    b = rng.standard_normal(N).astype(np.float32)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    epi = binding.EPI_BIAS_GELU if gelu else binding.EPI_BIAS
+    binding.gemm_pair(dev_bf16(A), dev_bf16(W), dev_f32(b), out, 0, epi)
+    binding.status()
+    got = host(out)
+    ref_lin = oracle.linear(A, W, b)
+    acc = K * EPS23 * (np.abs(A).astype(np.float64) @ np.abs(W).astype(np.float64).T) + 1e-6
+    if gelu:
+        ref = oracle.gelu(ref_lin)
+        tol = bf16_ulp(ref) + 1.2 * acc + 0.5 * np.abs(ref_lin) * 6e-4
+    else:
+        ref, tol = ref_lin, bf16_ulp(ref_lin) + acc
+    bad = ~(np.abs(got - ref) <= tol)
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside bound"
