@@ -62,14 +62,14 @@ NCU_TRAFFIC = {
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
                   "digest": "1458438068a7e65286a8c275768f49580badcdc5"},
-    "head": {"bytes": 102.547712e6 + 17.439744e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+    "head": {"bytes": 102.550272e6 + 17.419520e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "cec56c43b5b204774fa6ba2985407178ea08ed0d"},
-    "mlp_proj": {"bytes": 164.021504e6 + 24.960256e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+             "digest": "ae792f59bdc073ff4bd900c4ab4b82f05ba81329"},
+    "mlp_proj": {"bytes": 179.670528e6 + 31.233280e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                 "digest": "cec56c43b5b204774fa6ba2985407178ea08ed0d"},
+                 "digest": "ae792f59bdc073ff4bd900c4ab4b82f05ba81329"},
 }
 
 # The same for the training step's dominant step at B = 16, T = 1024: the attention derivative (Dsum,
@@ -86,12 +86,12 @@ TRAIN_NCU_TRAFFIC = {
 
 KERNEL_OF_STEP = {
     "embed": "embed_kernel (token + position rows, fused first LayerNorm)",
-    "c_attn": "gemm_tc_kernel<EPI_BIAS_OUT> (fused QKV projection)",
+    "c_attn": "gemm_pair_kernel<EPI_BIAS_OUT> (fused QKV projection, CTA pairs)",
     "attention": "attn_fwd_tc_kernel<64> (causal attention, online softmax)",
     "c_proj": "gemm_tc_kernel<EPI_BIAS_RESID> (attention output projection + residual)",
     "ln_mid": "layernorm_kernel (ln_2)",
     "c_fc": "gemm_tc_kernel<EPI_BIAS_GELU_OUT> (MLP up-projection + GELU)",
-    "mlp_proj": "gemm_tc_kernel<EPI_BIAS_RESID> (MLP down-projection + residual)",
+    "mlp_proj": "gemm_pair_kernel<EPI_BIAS_RESID> (MLP down-projection + residual, CTA pairs, stream-K)",
     "ln_out": "layernorm_kernel (next ln_1 / ln_f)",
     "head": "gemm_tc_kernel<EPI_CE> (tied LM head + cross-entropy partials)",
     "ce_combine": "ce_combine_kernel",
@@ -548,18 +548,18 @@ def run_decode(args, rank, world, local_rank):
 # backward steps that gpt_backward can bracket with the probe: (name, step id, per block, kernel)
 TRAIN_STEP_KINDS = [
     ("b_dz", 16, False, "gemm_tc_kernel<EPI_CE_GRAD> (recomputed logits -> cross-entropy gradient dz)"),
-    ("b_dh", 17, False, "gemm_tc_kernel<EPI_BIAS_RESID> (dh = dz E)"),
+    ("b_dh", 17, False, "gemm_pair_kernel<EPI_BIAS_RESID> split-K (dh = dz E, CTA pairs)"),
     ("b_de", 18, False, "gemm_tc_kernel<EPI_BIAS_RESID> (head share of the table gradient, dz^T h)"),
     ("b_mp_w", 19, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP down-projection weight gradient)"),
     ("b_dg", 20, True, "gemm_tc_kernel<EPI_GELU_GRAD> (du = (dx W_mp) gelu'(u))"),
     ("b_fc_w", 21, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP up-projection weight gradient)"),
-    ("b_da2", 22, True, "gemm_tc_kernel<EPI_F32> (du W_fc)"),
+    ("b_da2", 22, True, "gemm_pair_kernel<EPI_F32_OUT> (du W_fc, CTA pairs)"),
     ("b_proj_w", 23, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (attention output projection weight gradient)"),
     ("b_dy", 24, True, "gemm_tc_kernel<EPI_BIAS_OUT> (dy = ds1 W_proj)"),
     ("b_attn", 25, True, "attn_bwd_tc_kernel<64> + attn_bwd_dsum_kernel<64> + attn_bwd_dq_convert_kernel + memset "
                          "(causal attention derivative on tcgen05)"),
     ("b_attn_w", 26, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (QKV projection weight gradient)"),
-    ("b_da1", 27, True, "gemm_tc_kernel<EPI_F32> (dqkv W_attn)"),
+    ("b_da1", 27, True, "gemm_pair_kernel<EPI_F32_OUT> (dqkv W_attn, CTA pairs)"),
 ]
 
 

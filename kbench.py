@@ -7,9 +7,10 @@
     python kbench.py head --M 16384 --V 50257 --C 768
     python kbench.py layernorm --M 16384 --C 768
     python kbench.py train --B 16 --T 1024
+    python kbench.py forward --B 16 --T 1024
 
 (`train`: one gpt_backward call, forward + loss + every gradient, of GPT-2 small on
-seeded synthetic tokens. `attention_bwd`: one gptk_attention_bwd call, the attention
+seeded synthetic tokens; `forward`: one gpt_forward call, forward + loss, on the same. `attention_bwd`: one gptk_attention_bwd call, the attention
 derivative's memset and three kernels, after one gptk_attention_lse for its inputs.)
 
 Inputs are random device tensors; the figure printed is algorithmic TFLOP/s
@@ -43,7 +44,7 @@ def _time(fn, warmup, iters):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["attention", "attention_bwd", "gemm", "head", "layernorm", "train"])
+    ap.add_argument("kernel", choices=["attention", "attention_bwd", "gemm", "head", "layernorm", "train", "forward"])
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=1024)
     ap.add_argument("--H", type=int, default=12)
@@ -104,7 +105,7 @@ def main():
         ms = _time(lambda: binding.lmhead_ce(h, E, tg, nll), a.warmup, a.iters)
         flop = 2.0 * a.M * a.V * a.C
         out = {"kernel": "head_ce", "shape": [a.M, a.V, a.C], "ms": ms, "tflops": flop / ms / 1e9}
-    elif a.kernel == "train":
+    elif a.kernel in ("train", "forward"):
         from workloads import workload
         from workloads.generate import generate
         wl = workload("gpt2_small")
@@ -112,9 +113,12 @@ def main():
         m = binding.GPTModel(wl.cfg, w, a.B * a.T)
         d_ids, d_tg = torch.from_numpy(ids).to(dev), torch.from_numpy(tg).to(dev)
         loss = torch.zeros(1, device=dev)
-        ms = _time(lambda: m.backward(d_ids, d_tg, loss, check=False), a.warmup, a.iters)
+        if a.kernel == "train":
+            ms = _time(lambda: m.backward(d_ids, d_tg, loss, check=False), a.warmup, a.iters)
+        else:
+            ms = _time(lambda: m.forward(d_ids, d_tg, loss, None, check=False), a.warmup, a.iters)
         m.status()
-        out = {"kernel": "train", "shape": [a.B, a.T], "ms": ms, "tokens_per_s": a.B * a.T / ms * 1e3,
+        out = {"kernel": a.kernel, "shape": [a.B, a.T], "ms": ms, "tokens_per_s": a.B * a.T / ms * 1e3,
                "launches_per_call": m.lib.gpt_last_launch_count(m.handle)}
         m.close()
     else:
