@@ -104,14 +104,13 @@ int tc_gemm(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const 
 // A product with a tensor-store epilogue (EPI_BIAS_RESID, EPI_F32_OUT, EPI_BIAS_OUT, EPI_BIAS_GELU_OUT) on
 // CTA pairs (256 x 256 tiles, a six-stage ring of 32 KB per CTA; tmB_pair has 128-row boxes) where they
 // were measured faster in the GPT-2 small step at 16,384 tokens: long K (at least 1536: mlp c_proj
-// 66 -> 61 us, the input gradients through W_fc and W_attn) and the QKV projection (N = 2304, bf16 out:
-// 46.6 -> 44.5 us). Not the GELU product c_fc (59 -> 64 us: its epilogue bounds each tile, and the pair
-// ties both CTAs' epilogues to one accumulator hand-off) nor the attention c_proj (32 us either way).
+// 66 -> 61 us, the input gradients through W_fc and W_attn), the QKV projection (N = 2304, bf16 out:
+// 46.6 -> 44.5 us) and the GELU product c_fc (with eight epilogue warps and five stages: 60.5 -> 59.1 us;
+// with four it was 64: its epilogue bounds each tile). Not the attention c_proj (32 us either way).
 // Elsewhere, or where clusters of two cannot be resident, the single-CTA kernel.
 constexpr int kPairMinK = 1536;
 bool pair_pays(int N, int K, int epi) {
-  if (epi == EPI_BIAS_GELU_OUT) return false;
-  return K >= kPairMinK || (epi == EPI_BIAS_OUT && N >= 2048);
+  return epi == EPI_BIAS_GELU_OUT || K >= kPairMinK || (epi == EPI_BIAS_OUT && N >= 2048);
 }
 
 int tc_gemm_long(gpt_model* m, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB_pair,

@@ -825,23 +825,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // four. Each CTA's TMA copies land in its own shared memory and count towards the even CTA's "full"
 // barrier; the even CTA's commits arrive on both CTAs' barriers at once (multicast). Warp roles as
 // in gemm_tc_kernel; the odd CTA's warp 1 only allocates and frees TMEM.
-constexpr int P_STAGES = 6;
+constexpr int P_MAX_STAGES = 6;
 constexpr int P_A_BYTES = BM * BK * 2;            // this CTA's 128 of the pair's 256 A rows
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;      // this CTA's 128 of the tile's 256 W rows
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-struct PairLayout {
-  static constexpr int STAGING = P_STAGES * P_STAGE_BYTES;
-  static constexpr int BIAS = STAGING + EPI_WARPS * EPI_BUF;
-  static constexpr int BAR = BIAS + EPI_WARPS * BN * 4;
+// EW epilogue warps per CTA: 4 (one per TMEM lane quarter, all 256 columns each; six stages) or 8 (two
+// per lane quarter, 128 columns each, for the GELU epilogue whose arithmetic bounds a tile; their staging
+// boxes leave room for five stages).
+template <int EW>
+struct PairCfg {
+  static constexpr int THREADS = 64 + 32 * EW;
+  static constexpr int STAGES = EW == 4 ? 6 : 5;
+  static constexpr int CHUNKS = (BN / 64) * 4 / EW;   // 64-column chunks per epilogue warp
+  static constexpr int STAGING = STAGES * P_STAGE_BYTES;
+  static constexpr int BIAS = STAGING + EW * EPI_BUF;
+  static constexpr int BAR = BIAS + EW * BN * 4;
   static constexpr int SMEM = BAR + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(STAGES <= P_MAX_STAGES, "barrier arrays");
 };
 
 struct __align__(8) PairBars {
-  uint64_t full[P_STAGES];    // even CTA: both CTAs' copies of the stage have landed (2 x 32 KB)
-  uint64_t empty[P_STAGES];   // each CTA: the pair's MMAs have read its copy of the stage
+  uint64_t full[P_MAX_STAGES];    // even CTA: both CTAs' copies of the stage have landed (2 x 32 KB)
+  uint64_t empty[P_MAX_STAGES];   // each CTA: the pair's MMAs have read its copy of the stage
   uint64_t tfull[2];          // each CTA: its half of the accumulator is complete
-  uint64_t tempty[2];         // even CTA: both CTAs' epilogue warps (8) have read the accumulator
+  uint64_t tempty[2];         // even CTA: both CTAs' epilogue warps (2 EW) have read the accumulator
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -924,18 +932,21 @@ __device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar) {
 // pairs of CTAs: pair p = blockIdx.x / 2 takes the work gemm_tc_kernel gives CTA p of gridDim.x / 2.
 // A stream-K partial is handed between the CTAs of equal rank in neighbouring pairs (slot blockIdx.x,
 // taken from slot blockIdx.x + 2).
-template <int EPI, int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int EPI, int MODE, int EW>
+__global__ void __launch_bounds__(PairCfg<EW>::THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+  using CF = PairCfg<EW>;
+  constexpr int P_STAGES = CF::STAGES;
+  static_assert(EW == 4 || MODE != 1, "stream-K partials are laid out for four epilogue warps");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;   // the same in both CTAs
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;
   uint8_t* sB = smem + P_STAGES * P_A_BYTES;
-  uint8_t* sE = smem + PairLayout::STAGING;
-  float* sBias = reinterpret_cast<float*>(smem + PairLayout::BIAS);
-  PairBars* bars = reinterpret_cast<PairBars*>(smem + PairLayout::BAR);
+  uint8_t* sE = smem + CF::STAGING;
+  float* sBias = reinterpret_cast<float*>(smem + CF::BIAS);
+  PairBars* bars = reinterpret_cast<PairBars*>(smem + CF::BAR);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -952,7 +963,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) { mbar_init(&bars->full[s], 1); mbar_init(&bars->empty[s], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&bars->tfull[i], 1); mbar_init(&bars->tempty[i], 2 * EPI_WARPS); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bars->tfull[i], 1); mbar_init(&bars->tempty[i], 2 * EW); }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -1062,10 +1073,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
   } else {
     // ------------------------------------------------ epilogue warps (each CTA its 128 rows)
-    const int sub = warp & 3;
+    const int ew = warp - 2;                         // 0 .. EW-1
+    const int sub = warp & 3;                        // TMEM lane quarter this warp may read
+    const int c2a = (ew / 4) * CF::CHUNKS;           // its first 64-column chunk of the tile
     const int row = sub * 32 + lane;
-    uint8_t* my_stage = sE + sub * EPI_BUF;
-    float* my_bias = sBias + sub * BN;
+    uint8_t* my_stage = sE + ew * EPI_BUF;
+    float* my_bias = sBias + ew * BN;
     pdl_wait();
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -1133,11 +1146,11 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         ppart = reinterpret_cast<const float4*>(args.sk_part) + ((size_t)(blockIdx.x + 2) * 4 + sub) * (BN / 64) * 16 * 32 + lane;
       }
 #pragma unroll 1
-      for (int c2 = 0; c2 < BN / 64; ++c2) {
+      for (int c2 = c2a; c2 < c2a + CF::CHUNKS; ++c2) {
         uint32_t r[64];
         tmem_ld_32x32b_x64(tbase + c2 * 64, r);
         tmem_ld_wait();
-        if (c2 == BN / 64 - 1) release_acc();
+        if (c2 == c2a + CF::CHUNKS - 1) release_acc();
         if (SK && ppart != nullptr) {
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
@@ -1186,20 +1199,20 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   cluster_sync_all();
 }
 
-template <int EPI, int MODE>
+template <int EPI, int MODE, int EW>
 cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                              int pairs, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               PairLayout::SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI, MODE, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               PairCfg<EW>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = PairLayout::SMEM;
+  cfg.blockDim = dim3(PairCfg<EW>::THREADS);
+  cfg.dynamicSmemBytes = PairCfg<EW>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1210,7 +1223,7 @@ cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, con
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, MODE>, tmA, tmB, tmC, a);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, MODE, EW>, tmA, tmB, tmC, a);
 }
 
 template <int EPI, int MODE, bool MN = false>
@@ -1291,12 +1304,12 @@ int gemm_pair_capacity() {
   static int cap = -1;
   if (cap < 0) {
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_pair_kernel<EPI_BIAS_RESID, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::SMEM) ==
-        cudaSuccess) {
+    if (cudaFuncSetAttribute(gemm_pair_kernel<EPI_BIAS_RESID, 1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairCfg<4>::SMEM) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2);
-      cfg.blockDim = dim3(THREADS);
-      cfg.dynamicSmemBytes = PairLayout::SMEM;
+      cfg.blockDim = dim3(PairCfg<4>::THREADS);
+      cfg.dynamicSmemBytes = PairCfg<4>::SMEM;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = 2;
@@ -1304,7 +1317,7 @@ int gemm_pair_capacity() {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI_BIAS_RESID, 1>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI_BIAS_RESID, 1, 4>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();                    // a refused query leaves no error behind
     cap = n;
@@ -1333,14 +1346,19 @@ cudaError_t launch_pair_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
   const int tiles = MB * NB;
   if (tiles == 0) return cudaSuccess;
   const int KB = (a.K + BK - 1) / BK;
-  if (a.ksplit > 1) {                      // split-K: (pair tile, K slice) units, each reduce-added
-    if (EPI != EPI_BIAS_RESID || a.bias != nullptr || a.ksplit > KB) return cudaErrorInvalidValue;
-    const long long units = static_cast<long long>(tiles) * a.ksplit;
-    return launch_pair_inst<EPI, 2>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
+  if constexpr (EPI == EPI_BIAS_GELU_OUT) {   // eight epilogue warps, whole tiles only
+    if (a.ksplit > 1) return cudaErrorInvalidValue;
+    return launch_pair_inst<EPI, 0, 8>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
+  } else {
+    if (a.ksplit > 1) {                    // split-K: (pair tile, K slice) units, each reduce-added
+      if (EPI != EPI_BIAS_RESID || a.bias != nullptr || a.ksplit > KB) return cudaErrorInvalidValue;
+      const long long units = static_cast<long long>(tiles) * a.ksplit;
+      return launch_pair_inst<EPI, 2, 4>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
+    }
+    if (a.sk_part != nullptr && a.sk_flag != nullptr && pair_split(tiles, KB, cap))
+      return launch_pair_inst<EPI, 1, 4>(tmA, tmB, tmC, a, cap, s);
+    return launch_pair_inst<EPI, 0, 4>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
   }
-  if (a.sk_part != nullptr && a.sk_flag != nullptr && pair_split(tiles, KB, cap))
-    return launch_pair_inst<EPI, 1>(tmA, tmB, tmC, a, cap, s);
-  return launch_pair_inst<EPI, 0>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
 }
 
 cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
