@@ -62,14 +62,14 @@ NCU_TRAFFIC = {
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
                   "digest": "1458438068a7e65286a8c275768f49580badcdc5"},
-    "head": {"bytes": 102.550272e6 + 17.419520e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+    "head": {"bytes": 102.547968e6 + 17.524992e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "ae792f59bdc073ff4bd900c4ab4b82f05ba81329"},
-    "mlp_proj": {"bytes": 179.670528e6 + 31.233280e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+             "digest": "8689d5059823cc28ca6314c311330246d437f79d"},
+    "mlp_proj": {"bytes": 173.692160e6 + 28.377600e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                 "digest": "ae792f59bdc073ff4bd900c4ab4b82f05ba81329"},
+                 "digest": "8689d5059823cc28ca6314c311330246d437f79d"},
 }
 
 # The same for the training step's dominant step at B = 16, T = 1024: the attention derivative (Dsum,
@@ -86,12 +86,12 @@ TRAIN_NCU_TRAFFIC = {
 
 KERNEL_OF_STEP = {
     "embed": "embed_kernel (token + position rows, fused first LayerNorm)",
-    "c_attn": "gemm_pair_kernel<EPI_BIAS_OUT> (fused QKV projection, CTA pairs)",
+    "c_attn": "gemm_pair_kernel<EPI_BIAS_OUT, 0, 4> (fused QKV projection, CTA pairs)",
     "attention": "attn_fwd_tc_kernel<64> (causal attention, online softmax)",
     "c_proj": "gemm_tc_kernel<EPI_BIAS_RESID> (attention output projection + residual)",
     "ln_mid": "layernorm_kernel (ln_2)",
-    "c_fc": "gemm_tc_kernel<EPI_BIAS_GELU_OUT> (MLP up-projection + GELU)",
-    "mlp_proj": "gemm_pair_kernel<EPI_BIAS_RESID> (MLP down-projection + residual, CTA pairs, stream-K)",
+    "c_fc": "gemm_pair_kernel<EPI_BIAS_GELU_OUT, 0, 8> (MLP up-projection + GELU, CTA pairs, eight epilogue warps)",
+    "mlp_proj": "gemm_pair_kernel<EPI_BIAS_RESID, 1, 4> (MLP down-projection + residual, CTA pairs, stream-K)",
     "ln_out": "layernorm_kernel (next ln_1 / ln_f)",
     "head": "gemm_tc_kernel<EPI_CE> (tied LM head + cross-entropy partials)",
     "ce_combine": "ce_combine_kernel",
