@@ -62,14 +62,14 @@ NCU_TRAFFIC = {
                   "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_attn_tc.cu",
                               "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
                   "digest": "1458438068a7e65286a8c275768f49580badcdc5"},
-    "head": {"bytes": 102.547968e6 + 17.524992e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
+    "head": {"bytes": 102.692096e6 + 17.542656e6, "profile": "profiles/head_ce_gemm_m16384_v50257_c768.md",
              "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                          "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-             "digest": "8689d5059823cc28ca6314c311330246d437f79d"},
-    "mlp_proj": {"bytes": 173.692160e6 + 28.377600e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
+             "digest": "f178bf16f28b49e4bd9873c0482bfb5e717633a7"},
+    "mlp_proj": {"bytes": 173.873408e6 + 28.476928e6, "profile": "profiles/mlp_proj_gemm_m16384_n768_k3072.md",
                  "sources": ["decoder_only_transformer_gpt_gb300/csrc/k_gemm_tc.cu",
                              "decoder_only_transformer_gpt_gb300/csrc/common.cuh"],
-                 "digest": "8689d5059823cc28ca6314c311330246d437f79d"},
+                 "digest": "f178bf16f28b49e4bd9873c0482bfb5e717633a7"},
 }
 
 # The same for the training step's dominant step at B = 16, T = 1024: the attention derivative (Dsum,
@@ -91,7 +91,7 @@ KERNEL_OF_STEP = {
     "c_proj": "gemm_tc_kernel<EPI_BIAS_RESID> (attention output projection + residual)",
     "ln_mid": "layernorm_kernel (ln_2)",
     "c_fc": "gemm_pair_kernel<EPI_BIAS_GELU_OUT, 0, 8> (MLP up-projection + GELU, CTA pairs, eight epilogue warps)",
-    "mlp_proj": "gemm_pair_kernel<EPI_BIAS_RESID, 1, 4> (MLP down-projection + residual, CTA pairs, stream-K)",
+    "mlp_proj": "gemm_pair_kernel<EPI_BIAS_RESID, 1, 4, 0> (MLP down-projection + residual, CTA pairs, stream-K)",
     "ln_out": "layernorm_kernel (next ln_1 / ln_f)",
     "head": "gemm_tc_kernel<EPI_CE> (tied LM head + cross-entropy partials)",
     "ce_combine": "ce_combine_kernel",
@@ -549,16 +549,16 @@ def run_decode(args, rank, world, local_rank):
 TRAIN_STEP_KINDS = [
     ("b_dz", 16, False, "gemm_tc_kernel<EPI_CE_GRAD> (recomputed logits -> cross-entropy gradient dz)"),
     ("b_dh", 17, False, "gemm_pair_kernel<EPI_BIAS_RESID> split-K (dh = dz E, CTA pairs)"),
-    ("b_de", 18, False, "gemm_tc_kernel<EPI_BIAS_RESID> (head share of the table gradient, dz^T h)"),
-    ("b_mp_w", 19, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP down-projection weight gradient)"),
+    ("b_de", 18, False, "gemm_pair_kernel<EPI_BIAS_RESID, MN> (head share of the table gradient, dz^T h, CTA pairs)"),
+    ("b_mp_w", 19, True, "gemm_pair_kernel<EPI_BIAS_RESID, MN> split-K (MLP down-projection weight gradient, CTA pairs)"),
     ("b_dg", 20, True, "gemm_tc_kernel<EPI_GELU_GRAD> (du = (dx W_mp) gelu'(u))"),
-    ("b_fc_w", 21, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (MLP up-projection weight gradient)"),
+    ("b_fc_w", 21, True, "gemm_pair_kernel<EPI_BIAS_RESID, MN> split-K (MLP up-projection weight gradient, CTA pairs)"),
     ("b_da2", 22, True, "gemm_pair_kernel<EPI_F32_OUT> (du W_fc, CTA pairs)"),
-    ("b_proj_w", 23, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (attention output projection weight gradient)"),
+    ("b_proj_w", 23, True, "gemm_pair_kernel<EPI_BIAS_RESID, MN> split-K (attention output projection weight gradient, CTA pairs)"),
     ("b_dy", 24, True, "gemm_tc_kernel<EPI_BIAS_OUT> (dy = ds1 W_proj)"),
     ("b_attn", 25, True, "attn_bwd_tc_kernel<64> + attn_bwd_dsum_kernel<64> + attn_bwd_dq_convert_kernel + memset "
                          "(causal attention derivative on tcgen05)"),
-    ("b_attn_w", 26, True, "gemm_tc_kernel<EPI_BIAS_RESID> split-K (QKV projection weight gradient)"),
+    ("b_attn_w", 26, True, "gemm_pair_kernel<EPI_BIAS_RESID, MN> split-K (QKV projection weight gradient, CTA pairs)"),
     ("b_da1", 27, True, "gemm_pair_kernel<EPI_F32_OUT> (dqkv W_attn, CTA pairs)"),
 ]
 

@@ -319,8 +319,20 @@ int grad_gemm(gpt_model* m, const CUtensorMap& A, const CUtensorMap& Bm, const C
   a.err = m->err;
   a.m_fastest = (N1 > N0) ? 1 : 0;
   a.mn_major = 1;
-  const int tiles = ((N0 + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(N1);
   const int KB = (M + kGemmBK - 1) / kGemmBK;
+  const int pairs = pair_enabled() ? gemm_pair_capacity() : 0;
+  if (pairs > 0) {                        // CTA pairs: 256 x 256 tiles, the same boxes (two per operand and CTA)
+    const int grid = pairs < m->num_sms / 2 ? pairs : m->num_sms / 2;
+    const int tiles = ((N0 + 2 * kGemmBM - 1) / (2 * kGemmBM)) * gemm_tc_num_ntiles(N1);
+    a.ksplit = grad_ksplit(tiles, KB, grid);
+    if (a.ksplit == 1) {
+      a.sk_part = m->sk_part;
+      a.sk_flag = m->sk_flag;
+    }
+    GPT_CUDA(launch_gemm_pair(A, Bm, out_map, a, EPI_BIAS_RESID, m->num_sms / 2, s));
+    return GPT_OK;
+  }
+  const int tiles = ((N0 + kGemmBM - 1) / kGemmBM) * gemm_tc_num_ntiles(N1);
   const int ks = grad_ksplit(tiles, KB, m->num_sms);
   a.ksplit = ks;
   if (ks == 1) {                          // enough tiles: whole tiles (stream-K where it applies)

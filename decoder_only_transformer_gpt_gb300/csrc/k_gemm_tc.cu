@@ -932,7 +932,7 @@ __device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar) {
 // pairs of CTAs: pair p = blockIdx.x / 2 takes the work gemm_tc_kernel gives CTA p of gridDim.x / 2.
 // A stream-K partial is handed between the CTAs of equal rank in neighbouring pairs (slot blockIdx.x,
 // taken from slot blockIdx.x + 2).
-template <int EPI, int MODE, int EW>
+template <int EPI, int MODE, int EW, bool MN = false>
 __global__ void __launch_bounds__(PairCfg<EW>::THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -988,13 +988,27 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       uint32_t phase = 0;
       uint32_t issued = 0, last_par = 0;
       bool ok = true;
+      // MN: both operands stored [K][M or N] (the weight gradients): this CTA's 128 rows of M (or N) are
+      // two boxes of 64 (M or N) x 64 (K) at 8 KB strides, as in gemm_tc_kernel's MN-major stages
       auto load_a = [&](int st, int kb, int mb) {
-        tma_load_2d_pair(sA + st * P_A_BYTES, &tmA, cluster_addr(smem_u32(&bars->full[st]), 0), kb * BK,
-                         mb * 2 * BM + static_cast<int>(rank) * BM);
+        const uint32_t fb = cluster_addr(smem_u32(&bars->full[st]), 0);
+        const int m0 = mb * 2 * BM + static_cast<int>(rank) * BM;
+        if (MN) {
+#pragma unroll
+          for (int i = 0; i < BM / 64; ++i) tma_load_2d_pair(sA + st * P_A_BYTES + i * 8192, &tmA, fb, m0 + 64 * i, kb * BK);
+        } else {
+          tma_load_2d_pair(sA + st * P_A_BYTES, &tmA, fb, kb * BK, m0);
+        }
       };
       auto load_b = [&](int st, int kb, int nb) {
-        tma_load_2d_pair(sB + st * P_B_BYTES, &tmB, cluster_addr(smem_u32(&bars->full[st]), 0), kb * BK,
-                         nb * BN + static_cast<int>(rank) * (BN / 2));
+        const uint32_t fb = cluster_addr(smem_u32(&bars->full[st]), 0);
+        const int n0 = nb * BN + static_cast<int>(rank) * (BN / 2);
+        if (MN) {
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i) tma_load_2d_pair(sB + st * P_B_BYTES + i * 8192, &tmB, fb, n0 + 64 * i, kb * BK);
+        } else {
+          tma_load_2d_pair(sB + st * P_B_BYTES, &tmB, fb, kb * BK, n0);
+        }
       };
       int pre = 0;
       SegIter it = make_seg_iter_of(SK, KS, num_tiles, KB, args.ksplit, npairs, pair);
@@ -1038,9 +1052,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (even CTA; whole warp, one elected lane issues)
     if (leader) {
-      const uint32_t idesc = idesc_bf16_f32(2 * BM, BN, false);
-      const uint64_t da0 = smem_desc(smem_u32(sA), 16, 1024, SWZ_128B);
-      const uint64_t db0 = smem_desc(smem_u32(sB), 16, 1024, SWZ_128B);
+      const uint32_t idesc = idesc_bf16_f32(2 * BM, BN, MN) | (MN ? (1u << 15) : 0u);   // bit 15: A MN-major
+      const uint64_t da0 = smem_desc(smem_u32(sA), MN ? 8192 : 16, 1024, SWZ_128B);
+      const uint64_t db0 = smem_desc(smem_u32(sB), MN ? 8192 : 16, 1024, SWZ_128B);
+      constexpr uint64_t kstep = MN ? (16 * 128) >> 4 : 2;    // one K step of 16, in 16-byte units
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -1059,7 +1074,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           const uint64_t db = db0 + static_cast<uint64_t>((stage * P_B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_pair_warp(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            tc_mma_pair_warp(d_tmem, da + kstep * k, db + kstep * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           tc_commit_pair_both_warp(&bars->empty[stage]);
           if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -1199,12 +1214,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   cluster_sync_all();
 }
 
-template <int EPI, int MODE, int EW>
+template <int EPI, int MODE, int EW, bool MN = false>
 cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                              int pairs, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI, MODE, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<EPI, MODE, EW, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                PairCfg<EW>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -1223,7 +1238,7 @@ cudaError_t launch_pair_inst(const CUtensorMap& tmA, const CUtensorMap& tmB, con
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, MODE, EW>, tmA, tmB, tmC, a);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, MODE, EW, MN>, tmA, tmB, tmC, a);
 }
 
 template <int EPI, int MODE, bool MN = false>
@@ -1337,7 +1352,7 @@ bool gemm_pair_stream_k(int M, int N, int K, int max_pairs) {
 template <int EPI>
 cudaError_t launch_pair_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmArgs& a,
                             int max_pairs, cudaStream_t s) {
-  if (a.mn_major) return cudaErrorInvalidValue;
+  if (a.mn_major && (EPI != EPI_BIAS_RESID || a.bias != nullptr)) return cudaErrorInvalidValue;
   const int cap0 = gemm_pair_capacity();
   const int cap = cap0 < max_pairs ? cap0 : max_pairs;
   if (cap <= 0) return cudaErrorNotSupported;
@@ -1353,7 +1368,18 @@ cudaError_t launch_pair_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     if (a.ksplit > 1) {                    // split-K: (pair tile, K slice) units, each reduce-added
       if (EPI != EPI_BIAS_RESID || a.bias != nullptr || a.ksplit > KB) return cudaErrorInvalidValue;
       const long long units = static_cast<long long>(tiles) * a.ksplit;
-      return launch_pair_inst<EPI, 2, 4>(tmA, tmB, tmC, a, units < cap ? static_cast<int>(units) : cap, s);
+      const int pairs = units < cap ? static_cast<int>(units) : cap;
+      if constexpr (EPI == EPI_BIAS_RESID) {
+        if (a.mn_major) return launch_pair_inst<EPI, 2, 4, true>(tmA, tmB, tmC, a, pairs, s);
+      }
+      return launch_pair_inst<EPI, 2, 4>(tmA, tmB, tmC, a, pairs, s);
+    }
+    if constexpr (EPI == EPI_BIAS_RESID) {
+      if (a.mn_major) {
+        if (a.sk_part != nullptr && a.sk_flag != nullptr && pair_split(tiles, KB, cap))
+          return launch_pair_inst<EPI, 1, 4, true>(tmA, tmB, tmC, a, cap, s);
+        return launch_pair_inst<EPI, 0, 4, true>(tmA, tmB, tmC, a, tiles < cap ? tiles : cap, s);
+      }
     }
     if (a.sk_part != nullptr && a.sk_flag != nullptr && pair_split(tiles, KB, cap))
       return launch_pair_inst<EPI, 1, 4>(tmA, tmB, tmC, a, cap, s);
