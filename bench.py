@@ -593,7 +593,7 @@ def run_train(args, rank, world, local_rank):
     """--train: tokens/s of a whole training step, a second measurement beside the forward line: the
     forward and loss, the gradient of every parameter (gpt_backward) and one AdamW update of every
     weight (gpt_adamw_step, lr 1e-4). FLOPs per step = 3 x the forward's (the forward, then twice its
-    products for the input and weight gradients); the extra c_fc launch and the optimiser's
+    products for the input and weight gradients); recomputed logits and scores and the optimiser's
     elementwise work are not counted. The dominant probed step's launches are timed inside the timed
     region for the roofline."""
     import torch
