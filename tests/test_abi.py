@@ -77,3 +77,24 @@ def test_gradient_parameter_ids_match_the_binding():
     assert sorted(ids.values()) == list(range(len(binding.GRAD_PARAMS)))
     for i, name in enumerate(binding.GRAD_PARAMS):
         assert ids[name] == i, name
+
+
+def test_gemm_pair_validates_arguments_before_the_device(lib):
+    # every argument check of gptk_gemm_pair runs on the host before any device call (the pointers
+    # below are never dereferenced); without a GPU the entry then reports GPT_ECONFIG (clusters of two
+    # cannot be resident), never a launch
+    import ctypes
+    from decoder_only_transformer_gpt_gb300 import binding
+    P = ctypes.c_void_p(0x10000)
+    f = lib.gptk_gemm_pair
+    resid, store = binding.EPI_BIAS_RESID, binding.EPI_F32
+    assert f(None, P, None, P, 1, 8, 8, resid, 0, None) == binding.GPT_EINVAL          # no A
+    assert f(P, P, None, P, 1, 8, 8, 7, 0, None) == binding.GPT_EINVAL                 # no such epilogue
+    assert f(P, P, None, P, 1, 8, 64, store, 2, None) == binding.GPT_EINVAL            # split-K of a store
+    assert f(P, P, P, P, 1, 8, 64, resid, 2, None) == binding.GPT_EINVAL               # split-K with a bias
+    assert f(P, P, None, P, 1, 8, 64, resid, 2, None) == binding.GPT_EINVAL            # 2 slices of 1 K block
+    assert f(P, P, None, P, 1, 8, 12, resid, 0, None) == binding.GPT_EINVAL            # K not a multiple of 8
+    assert f(P, P, None, P, 0, 8, 8, resid, 0, None) == binding.GPT_OK                 # nothing to do
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert f(P, P, None, P, 1, 8, 8, resid, 0, None) == binding.GPT_ECONFIG
